@@ -1,0 +1,191 @@
+"""ctypes wrapper around the C oracle (``nvfp4_oracle.c``).
+
+Test infrastructure only (see the package docstring). Arrays cross the
+boundary as numpy arrays: bfloat16 tensors travel as their uint16 bit
+patterns, packed codes and E4M3 scales as uint8.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "nvfp4_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_f64p = ctypes.POINTER(ctypes.c_double)
+_i64 = ctypes.c_int64
+
+
+def lib_path() -> str:
+    return _LIB
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` next to its source (gcc, OpenMP, no FMA
+    contraction, no fast-math). Rebuilds whenever the source is newer."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-D_DEFAULT_SOURCE", "-fPIC", "-shared",
+           "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-Wall",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        build()
+        lib = ctypes.CDLL(_LIB)
+        lib.oracle_e2m1_value.restype = ctypes.c_double
+        lib.oracle_e2m1_value.argtypes = [ctypes.c_int]
+        lib.oracle_e4m3_value.restype = ctypes.c_double
+        lib.oracle_e4m3_value.argtypes = [ctypes.c_int]
+        lib.oracle_e4m3_rne_satfinite.restype = ctypes.c_uint8
+        lib.oracle_e4m3_rne_satfinite.argtypes = [ctypes.c_float]
+        lib.oracle_e2m1_rne_satfinite.restype = ctypes.c_int
+        lib.oracle_e2m1_rne_satfinite.argtypes = [ctypes.c_float]
+        lib.oracle_bf16_from_double.restype = ctypes.c_uint16
+        lib.oracle_bf16_from_double.argtypes = [ctypes.c_double]
+        lib.oracle_global_scale.restype = ctypes.c_float
+        lib.oracle_global_scale.argtypes = [_u16p, _i64, _i64, _i64]
+        lib.oracle_quantize.restype = None
+        lib.oracle_quantize.argtypes = [_u16p, _i64, _i64, _i64, ctypes.c_float,
+                                        _u8p, _u8p]
+        lib.oracle_dequantize.restype = None
+        lib.oracle_dequantize.argtypes = [_u8p, _u8p, ctypes.c_float, _i64, _i64,
+                                          _f64p]
+        lib.oracle_gemm_rows.restype = None
+        lib.oracle_gemm_rows.argtypes = [_u8p, _u8p, ctypes.c_float, _u8p, _u8p,
+                                         ctypes.c_float, _i64, _i64, _i64,
+                                         _i64p, _i64, _u16p, _f64p]
+        lib.oracle_symmetric_quantize.restype = ctypes.c_double
+        lib.oracle_symmetric_quantize.argtypes = [_f64p, _i64, ctypes.c_int,
+                                                  _i32p, _f64p]
+        lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_num_threads.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray, t):
+    return a.ctypes.data_as(t)
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def num_threads() -> int:
+    """Threads the oracle's parallel loops use (OpenMP)."""
+    return int(_load().oracle_num_threads())
+
+
+def e2m1_value(code: int) -> float:
+    return float(_load().oracle_e2m1_value(int(code)))
+
+
+def e4m3_value(byte: int) -> float:
+    return float(_load().oracle_e4m3_value(int(byte)))
+
+
+def e4m3_rne_satfinite(v: float) -> int:
+    return int(_load().oracle_e4m3_rne_satfinite(float(v)))
+
+
+def e2m1_rne_satfinite(y: float) -> int:
+    return int(_load().oracle_e2m1_rne_satfinite(float(y)))
+
+
+def bf16_from_double(y: float) -> int:
+    return int(_load().oracle_bf16_from_double(float(y)))
+
+
+def global_scale(x_bits: np.ndarray) -> float:
+    """Per-tensor global scale of a 2-D bfloat16 tensor given as uint16 bits."""
+    x = _c(x_bits, np.uint16)
+    rows, cols = x.shape
+    return float(_load().oracle_global_scale(_ptr(x, _u16p), rows, cols, cols))
+
+
+def quantize(x_bits: np.ndarray, g: float):
+    """Quantize a 2-D bfloat16 tensor (uint16 bits, cols % 16 == 0) with the
+    decode-direction global scale ``g``. Returns (codes uint8 rows x cols/2,
+    scales uint8 rows x cols/16), both row-major."""
+    x = _c(x_bits, np.uint16)
+    rows, cols = x.shape
+    if cols % 16:
+        raise ValueError("cols must be a multiple of 16")
+    q = np.empty((rows, cols // 2), np.uint8)
+    s = np.empty((rows, cols // 16), np.uint8)
+    _load().oracle_quantize(_ptr(x, _u16p), rows, cols, cols, float(g),
+                            _ptr(q, _u8p), _ptr(s, _u8p))
+    return q, s
+
+
+def dequantize(q: np.ndarray, s: np.ndarray, g: float) -> np.ndarray:
+    q = _c(q, np.uint8)
+    s = _c(s, np.uint8)
+    rows, half = q.shape
+    out = np.empty((rows, half * 2), np.float64)
+    _load().oracle_dequantize(_ptr(q, _u8p), _ptr(s, _u8p), float(g), rows,
+                              half * 2, _ptr(out, _f64p))
+    return out
+
+
+def gemm_rows(xq, xs, g_x, wq, ws, g_w, rows=None, want_fp64=False):
+    """Reference Y = bf16((Xhat @ What^T) * g_x * g_w) for the listed rows of
+    X (all rows if ``rows`` is None). Returns uint16 bf16 bits (and the FP64
+    values before rounding when ``want_fp64``)."""
+    xq = _c(xq, np.uint8)
+    xs = _c(xs, np.uint8)
+    wq = _c(wq, np.uint8)
+    ws = _c(ws, np.uint8)
+    M, kh = xq.shape
+    N = wq.shape[0]
+    K = kh * 2
+    if rows is None:
+        ids = None
+        n_rows = M
+    else:
+        ids = _c(rows, np.int64)
+        n_rows = ids.shape[0]
+    y = np.empty((n_rows, N), np.uint16)
+    yd = np.empty((n_rows, N), np.float64) if want_fp64 else None
+    _load().oracle_gemm_rows(
+        _ptr(xq, _u8p), _ptr(xs, _u8p), float(g_x), _ptr(wq, _u8p),
+        _ptr(ws, _u8p), float(g_w), M, N, K,
+        None if ids is None else _ptr(ids, _i64p), n_rows,
+        _ptr(y, _u16p), None if yd is None else _ptr(yd, _f64p))
+    return (y, yd) if want_fp64 else y
+
+
+def gemm(xq, xs, g_x, wq, ws, g_w, want_fp64=False):
+    return gemm_rows(xq, xs, g_x, wq, ws, g_w, None, want_fp64)
+
+
+def symmetric_quantize(x, bits: int):
+    """Symmetric integer quantization (FP64). Returns (s, q int32, x_hat)."""
+    xx = _c(x, np.float64)
+    n = xx.shape[0]
+    q = np.empty(n, np.int32)
+    xh = np.empty(n, np.float64)
+    s = _load().oracle_symmetric_quantize(_ptr(xx, _f64p), n, int(bits),
+                                          _ptr(q, _i32p), _ptr(xh, _f64p))
+    return float(s), q, xh

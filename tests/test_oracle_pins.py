@@ -1,0 +1,434 @@
+"""Pins for the CPU oracle, against what the pages and the mathematics fix.
+
+Each test ties an oracle function to something other than itself: the format
+definitions and the worked example printed on the pages (tests/golden/),
+library routines (torch's float8_e4m3fn decode and rounding, torch's
+float32 -> bfloat16 rounding, numpy's float64 matmul), closed forms,
+invariants and brute force on tiny inputs.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+E2M1 = _golden("e2m1_grid.json")["magnitudes_by_code"]
+
+
+def e4m3_torch(byte):
+    """E4M3 value through torch's own float8_e4m3fn decode (library pin)."""
+    t = torch.tensor([byte], dtype=torch.uint8).view(torch.float8_e4m3fn)
+    return float(t.to(torch.float64))
+
+
+def e4m3_round_torch(v):
+    """torch's float32 -> float8_e4m3fn rounding; valid for 0 <= v <= 464."""
+    t = torch.tensor([v], dtype=torch.float32).to(torch.float8_e4m3fn)
+    return int(t.view(torch.uint8))
+
+
+def e2m1_round_thresholds(y):
+    """E2M1 round-to-nearest-even written as thresholds at the midpoints of
+    the grid {0,.5,1,1.5,2,3,4,6}: a midpoint goes to the even code."""
+    if not (y <= 6.0):
+        return 7
+    if y <= 0.25:
+        return 0   # midpoint 0.25: codes 0 (even) / 1
+    if y < 0.75:
+        return 1   # midpoint 0.75: codes 1 / 2 (even)
+    if y <= 1.25:
+        return 2   # midpoint 1.25: codes 2 (even) / 3
+    if y < 1.75:
+        return 3   # midpoint 1.75: codes 3 / 4 (even)
+    if y <= 2.5:
+        return 4   # midpoint 2.5: codes 4 (even) / 5
+    if y < 3.5:
+        return 5   # midpoint 3.5: codes 5 / 6 (even)
+    if y <= 5.0:
+        return 6   # midpoint 5: codes 6 (even) / 7
+    return 7
+
+
+def bf16_bits(x_float32):
+    t = torch.tensor(np.asarray(x_float32, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bits_to_f32(bits):
+    return (np.asarray(bits, np.uint32) << 16).view(np.float32)
+
+
+# ------------------------------------------------------------------ formats
+
+def test_e2m1_decode_matches_page_grid(oracle_mod):
+    for c in range(16):
+        mag = E2M1[c & 7]
+        want = -mag if c & 8 else mag
+        got = oracle_mod.e2m1_value(c)
+        assert got == want and math.copysign(1, got) == math.copysign(1, want if c & 8 == 0 else -1.0)
+
+
+def test_e4m3_decode_matches_torch_all_bytes(oracle_mod):
+    for b in range(256):
+        got = oracle_mod.e4m3_value(b)
+        want = e4m3_torch(b)
+        if math.isnan(want):
+            assert math.isnan(got), b
+        else:
+            assert got == want, (b, got, want)
+    # largest finite value 448 (the constant behind g = amax / (6 * 448))
+    assert oracle_mod.e4m3_value(0x7E) == 448.0
+
+
+def _e4m3_probe_values():
+    vals = [0.0]
+    finite = sorted({e4m3_torch(b) for b in range(0x7F)})
+    for a, b in zip(finite, finite[1:]):
+        mid = np.float32((a + b) / 2)
+        vals += [a, b, float(mid),
+                 float(np.nextafter(mid, np.float32(0))),
+                 float(np.nextafter(mid, np.float32(1e9)))]
+    rng = np.random.default_rng(7)
+    vals += list(np.exp2(rng.uniform(-14, 8.8, 4000)).astype(np.float32))
+    return [float(np.float32(v)) for v in vals if v <= 448.0]
+
+
+def test_e4m3_rounding_matches_torch(oracle_mod):
+    for v in _e4m3_probe_values():
+        assert oracle_mod.e4m3_rne_satfinite(v) == e4m3_round_torch(v), v
+
+
+def test_e4m3_rounding_saturates_and_underflows(oracle_mod):
+    assert oracle_mod.e4m3_rne_satfinite(448.0) == 0x7E
+    assert oracle_mod.e4m3_rne_satfinite(449.0) == 0x7E
+    assert oracle_mod.e4m3_rne_satfinite(1e30) == 0x7E
+    assert oracle_mod.e4m3_rne_satfinite(float("inf")) == 0x7E
+    # smallest subnormal 2^-9; half of it is a tie between codes 0 and 1
+    assert oracle_mod.e4m3_rne_satfinite(2.0 ** -10) == 0x00
+    assert oracle_mod.e4m3_rne_satfinite(float(np.nextafter(np.float32(2.0 ** -10), np.float32(1)))) == 0x01
+    assert oracle_mod.e4m3_rne_satfinite(2.0 ** -9) == 0x01
+    assert oracle_mod.e4m3_rne_satfinite(1e-30) == 0x00
+
+
+def test_e2m1_rounding_matches_thresholds(oracle_mod):
+    vals = []
+    for a, b in zip(E2M1, E2M1[1:]):
+        mid = np.float32((a + b) / 2)
+        vals += [a, b, mid, np.nextafter(mid, np.float32(0)),
+                 np.nextafter(mid, np.float32(10))]
+    vals += list(np.linspace(0, 8, 3001, dtype=np.float32))
+    vals += [6.0, np.nextafter(np.float32(6), np.float32(10)), 7.0, 1e30,
+             float("inf"), 1e-40]
+    for y in vals:
+        y = float(np.float32(y))
+        assert oracle_mod.e2m1_rne_satfinite(y) == e2m1_round_thresholds(y), y
+
+
+def test_e2m1_rounding_is_nearest_by_exhaustion(oracle_mod):
+    """Brute force: the chosen magnitude is at least as close as every other
+    grid value, and on an exact tie it is the even code."""
+    rng = np.random.default_rng(3)
+    for y in rng.uniform(0, 6, 5000).astype(np.float32):
+        c = oracle_mod.e2m1_rne_satfinite(float(y))
+        d = abs(float(y) - E2M1[c])
+        for o in range(8):
+            do = abs(float(y) - E2M1[o])
+            assert d <= do
+            if do == d and o != c:
+                assert c % 2 == 0
+
+
+def test_bf16_rounding_matches_torch_on_float32(oracle_mod):
+    rng = np.random.default_rng(11)
+    xs = np.concatenate([
+        rng.standard_normal(3000).astype(np.float32) * np.float32(1000),
+        np.exp2(rng.uniform(-130, 127, 2000)).astype(np.float32),
+    ])
+    # exact bfloat16 midpoints and their neighbours
+    base = bits_to_f32(rng.integers(0x0080, 0x7F00, 500).astype(np.uint16))
+    mids = (base.view(np.uint32) | np.uint32(0x8000)).view(np.float32)
+    xs = np.concatenate([xs, mids, np.nextafter(mids, np.float32(0)),
+                         np.nextafter(mids, np.float32(np.inf)), -mids])
+    want = bf16_bits(xs)
+    for x, w in zip(xs, want):
+        assert oracle_mod.bf16_from_double(float(x)) == int(w), float(x)
+
+
+def test_bf16_rounding_is_single_rounding_from_double(oracle_mod):
+    # 1 + 2^-8 is the midpoint between 1 and 1 + 2^-7; a double just above it
+    # must round up, although rounding through float32 first would hit the
+    # midpoint and tie down to 1.0.
+    assert oracle_mod.bf16_from_double(1.0 + 2.0 ** -8 + 2.0 ** -30) == 0x3F81
+    assert oracle_mod.bf16_from_double(1.0 + 2.0 ** -8) == 0x3F80
+    assert oracle_mod.bf16_from_double(1.0 + 3 * 2.0 ** -8) == 0x3F82
+    assert oracle_mod.bf16_from_double(-0.0) == 0x8000
+    assert oracle_mod.bf16_from_double(1e39) == 0x7F80
+    assert oracle_mod.bf16_from_double(-1e39) == 0xFF80
+
+
+# ---------------------------------------------------------------- quantizer
+
+def _scale_value(S):
+    return e4m3_torch(S)
+
+
+def test_global_scale_closed_form(oracle_mod):
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((33, 48)).astype(np.float32) * 3
+    bits = bf16_bits(x)
+    amax = np.max(np.abs(bits_to_f32(bits)))
+    assert oracle_mod.global_scale(bits) == float(np.float32(amax) / np.float32(2688.0))
+    assert oracle_mod.global_scale(np.zeros((4, 32), np.uint16)) == 1.0
+    assert oracle_mod.global_scale(np.full((2, 16), 0x8000, np.uint16)) == 1.0
+
+
+def test_nibble_order_even_element_low(oracle_mod):
+    x = np.zeros((1, 16), np.float32)
+    x[0, 0] = 6.0
+    q, s = oracle_mod.quantize(bf16_bits(x), 1.0)
+    assert q[0, 0] == 0x07 and s[0, 0] == 0x38  # scale 1.0
+    x = np.zeros((1, 16), np.float32)
+    x[0, 1] = 6.0
+    q, s = oracle_mod.quantize(bf16_bits(x), 1.0)
+    assert q[0, 0] == 0x70 and s[0, 0] == 0x38
+
+
+def test_closed_form_ladder_block(oracle_mod):
+    # [6,4,3,2,1.5,1,0.5,0] * k with k a power of two and g = 1: the block
+    # scale is exactly k and every element lands on its own grid point.
+    ladder = [6.0, 4.0, 3.0, 2.0, 1.5, 1.0, 0.5, 0.0]
+    for k in (2.0 ** -6, 0.25, 1.0, 4.0, 64.0):
+        row = np.array(ladder + [-v for v in ladder], np.float32) * np.float32(k)
+        q, s = oracle_mod.quantize(bf16_bits(row[None, :]), 1.0)
+        assert _scale_value(int(s[0, 0])) == k
+        codes = [(q[0, j // 2] >> (4 * (j % 2))) & 15 for j in range(16)]
+        assert codes[:8] == [7, 6, 5, 4, 3, 2, 1, 0]
+        assert codes[8:] == [15, 14, 13, 12, 11, 10, 9, 8]  # sign bit kept on -0
+
+
+def test_closed_form_constant_block(oracle_mod):
+    rng = np.random.default_rng(9)
+    for c in rng.uniform(0.01, 100, 50).astype(np.float32):
+        g = float(np.float32(rng.uniform(0.001, 1)))
+        cb = bf16_bits(np.full((1, 16), c, np.float32))
+        q, s = oracle_mod.quantize(cb, g)
+        cf = float(bits_to_f32(cb)[0, 0])
+        v = np.float32(np.float32(cf) / np.float32(6)) / np.float32(g)
+        want = 0x7E if v > 448 else e4m3_round_torch(float(v))  # satfinite
+        assert int(s[0, 0]) == want
+        # every element is the block max; it maps to the top code unless the
+        # rounded scale overshoots enough that y falls to 4 (y <= 5), which
+        # the scale rounding (< 1/16 relative) never allows.
+        assert np.all(q == 0x77)
+
+
+def test_sign_and_zero_conventions(oracle_mod):
+    x = np.zeros((1, 32), np.float32)
+    x[0, 16:] = 1.0
+    x[0, 17] = -1e-3           # rounds to zero magnitude, keeps sign bit
+    bits = bf16_bits(x)
+    bits[0, 3] = 0x8000        # -0.0 in an otherwise zero block
+    q, s = oracle_mod.quantize(bits, 1.0)
+    assert s[0, 0] == 0 and s[0, 1] != 0
+    codes = [(q[0, j // 2] >> (4 * (j % 2))) & 15 for j in range(32)]
+    assert codes[3] == 8 and all(c == 0 for i, c in enumerate(codes[:16]) if i != 3)
+    assert codes[17] == 8
+
+
+def test_brute_force_all_codes_all_scales(oracle_mod):
+    """For every nonzero finite E4M3 scale S and g = 1: a block whose max is
+    6 s gets exactly scale S, and each element's code equals the threshold
+    rounding of fl(|x| * fl(1/s)) -- over all 16 codes, every grid midpoint
+    and the bfloat16 neighbours of each midpoint."""
+    probes = []
+    for a, b in zip(E2M1, E2M1[1:]):
+        probes += [a, (a + b) / 2]
+    probes.append(6.0)
+    for S in range(1, 0x7F):
+        s = _scale_value(S)
+        if 6 * s > 3e38:
+            continue
+        vals = [6 * s]
+        for p in probes:
+            vals.append(p * s)
+        for p in probes[1:-1]:
+            v = np.float32(p * s)
+            b = bf16_bits(np.array([v]))[0]
+            vals += [float(bits_to_f32(np.array([b - 1]))[0]),
+                     float(bits_to_f32(np.array([b + 1]))[0])]
+        vals = vals[:32] + [0.0] * max(0, 32 - len(vals))
+        signs = np.array([1 if i % 3 else -1 for i in range(32)], np.float32)
+        row = (np.array(vals, np.float32) * signs)[None, :]
+        row[0, 16] = np.float32(6 * s)            # second block: same max
+        bits = bf16_bits(row)
+        xs = bits_to_f32(bits)[0]
+        q, sf = oracle_mod.quantize(bits, 1.0)
+        assert int(sf[0, 0]) == S and int(sf[0, 1]) == S, S
+        r = np.float32(1.0) / np.float32(s)
+        for j in range(32):
+            y = float(np.float32(abs(xs[j])) * r)
+            want = e2m1_round_thresholds(y) | (8 if np.signbit(xs[j]) else 0)
+            got = (q[0, j // 2] >> (4 * (j % 2))) & 15
+            assert got == want, (S, j, xs[j], y)
+
+
+def test_round_trip_of_representable_blocks(oracle_mod):
+    rng = np.random.default_rng(17)
+    rows, blocks = 64, 8
+    for g in (1.0, 2.0 ** -5, 2.0 ** 3):
+        codes = rng.integers(0, 16, (rows, blocks * 16))
+        codes[:, ::16] = rng.choice([7, 15], (rows, blocks))  # max code per block
+        S = rng.integers(1, 0x7F, (rows, blocks)).astype(np.uint8)
+        svals = np.array([[_scale_value(int(b)) for b in r] for r in S])
+        mags = np.array(E2M1)[codes & 7] * np.where(codes & 8, -1.0, 1.0)
+        x = mags * np.repeat(svals, 16, axis=1) * g
+        ok = np.all(np.abs(x) < 3e38, axis=1)
+        x, codes, S = x[ok], codes[ok], S[ok]
+        bits = bf16_bits(x.astype(np.float32))
+        assert np.array_equal(bits_to_f32(bits).astype(np.float64), x)  # exact in bf16
+        q, sf = oracle_mod.quantize(bits, g)
+        assert np.array_equal(sf, S)
+        packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+        # a code whose magnitude is 0 may carry either sign; compare values
+        zero = (codes & 7) == 0
+        want = packed.copy()
+        got_codes = np.stack([q & 15, q >> 4], axis=-1).reshape(q.shape[0], -1)
+        assert np.array_equal(np.where(zero, 0, got_codes & 7), np.where(zero, 0, codes & 7))
+        assert np.array_equal((got_codes >> 3)[~zero], (codes >> 3)[~zero])
+        del want
+
+
+def test_error_bound_half_grid_step(oracle_mod):
+    """|x - x_hat| <= (1/2) * (local E2M1 step) * s * g, the NVFP4 form of
+    the s/2 bound of the symmetric map on the course page; saturated
+    elements (y > 6) err by exactly |x| - 6 s g."""
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal((64, 512)).astype(np.float32)
+    x[:, rng.choice(512, 3, replace=False)] *= 50
+    bits = bf16_bits(x)
+    xs = bits_to_f32(bits).astype(np.float64)
+    g = oracle_mod.global_scale(bits)
+    q, sf = oracle_mod.quantize(bits, g)
+    xh = oracle_mod.dequantize(q, sf, g)
+    svals = np.vectorize(_scale_value)(sf.astype(np.int64))
+    sg = np.repeat(svals, 16, axis=1) * g
+    y = np.abs(xs) / np.where(sg > 0, sg, np.inf)
+    step = np.where(y < 2, 0.5, np.where(y < 4, 1.0, 2.0))
+    bound = np.where(y <= 6, 0.5 * step * sg, np.abs(xs) - 6 * sg)
+    err = np.abs(xs - xh)
+    # fp32 rounding of 1/(s g) and |x| * r moves y by a few ulps
+    assert np.all(err <= bound * (1 + 1e-6) + np.abs(xs) * 2.0 ** -21)
+
+
+def test_outlier_only_changes_its_own_block(oracle_mod):
+    rng = np.random.default_rng(29)
+    x = rng.standard_normal((4, 128)).astype(np.float32)
+    g = 0.01
+    q0, s0 = oracle_mod.quantize(bf16_bits(x), g)
+    x2 = x.copy()
+    x2[2, 37] *= 50.0            # block 2 of row 2
+    q1, s1 = oracle_mod.quantize(bf16_bits(x2), g)
+    changed_s = np.argwhere(s0 != s1)
+    assert changed_s.tolist() == [[2, 2]]
+    diff = np.argwhere(q0 != q1)
+    assert all(r == 2 and 16 <= 2 * c < 48 for r, c in diff)
+    assert len(diff) > 0
+
+
+def test_quantize_row_stride_independent(oracle_mod):
+    rng = np.random.default_rng(31)
+    x = bf16_bits(rng.standard_normal((8, 64)).astype(np.float32))
+    qa, sa = oracle_mod.quantize(x, 0.003)
+    qb, sb = oracle_mod.quantize(x[:, :32], 0.003)
+    assert np.array_equal(qa[:, :16], qb) and np.array_equal(sa[:, :2], sb)
+
+
+# --------------------------------------------------------------------- GEMM
+
+def _dequant_indep(q, s, g):
+    """Dequantize with the page grid and torch's E4M3 decode (independent of
+    the oracle's decoders)."""
+    lo = (q & 15).astype(np.int64)
+    hi = (q >> 4).astype(np.int64)
+    codes = np.stack([lo, hi], axis=-1).reshape(q.shape[0], -1)
+    grid = np.array(E2M1 + [-v for v in E2M1])
+    sv = torch.from_numpy(s.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return grid[codes] * np.repeat(sv, 16, axis=1) * g
+
+
+def test_gemm_matches_numpy_float64_matmul(oracle_mod):
+    rng = np.random.default_rng(37)
+    M, N, K = 19, 23, 96            # non-square: a transposed operand fails
+    x = bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    w = bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    gx, gw = oracle_mod.global_scale(x), oracle_mod.global_scale(w)
+    xq, xs = oracle_mod.quantize(x, gx)
+    wq, ws = oracle_mod.quantize(w, gw)
+    y, yd = oracle_mod.gemm(xq, xs, gx, wq, ws, gw, want_fp64=True)
+    ref = _dequant_indep(xq, xs, 1.0) @ _dequant_indep(wq, ws, 1.0).T * (gx * gw)
+    assert np.allclose(yd, ref, rtol=1e-12, atol=1e-300)
+    assert np.array_equal(y, np.vectorize(oracle_mod.bf16_from_double, otypes=[np.uint16])(yd))
+    # row sampling computes the same rows
+    rows = np.array([18, 0, 7])
+    ys = oracle_mod.gemm_rows(xq, xs, gx, wq, ws, gw, rows)
+    assert np.array_equal(ys, y[rows])
+
+
+def test_gemm_integer_closed_form(oracle_mod):
+    M, N, K = 3, 5, 64
+    xq = np.full((M, K // 2), 0x22, np.uint8)     # every element 1.0
+    xs = np.full((M, K // 16), 0x38, np.uint8)    # scale 1.0
+    wq = np.zeros((N, K // 2), np.uint8)
+    for n in range(N):
+        wq[n, : (n + 1)] = 0x44                    # 2(n+1) elements of 2.0
+    ws = np.full((N, K // 16), 0x38, np.uint8)
+    y, yd = oracle_mod.gemm(xq, xs, 1.0, wq, ws, 0.5, want_fp64=True)
+    want = np.array([2.0 * 2 * (n + 1) * 0.5 for n in range(N)])
+    assert np.array_equal(yd, np.tile(want, (M, 1)))
+
+
+def test_gemm_selects_one_column(oracle_mod):
+    rng = np.random.default_rng(41)
+    M, K = 6, 32
+    x = bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    gx = oracle_mod.global_scale(x)
+    xq, xs = oracle_mod.quantize(x, gx)
+    xh = oracle_mod.dequantize(xq, xs, gx)
+    N = K
+    wq = np.zeros((N, K // 2), np.uint8)
+    for n in range(N):                             # W row n = e_n (value 1.0)
+        wq[n, n // 2] = 0x02 << (4 * (n % 2))
+    ws = np.full((N, K // 16), 0x38, np.uint8)
+    _, yd = oracle_mod.gemm(xq, xs, gx, wq, ws, 1.0, want_fp64=True)
+    assert np.array_equal(yd, xh)
+
+
+# -------------------------------------------------------- page worked example
+
+def test_symmetric_int8_worked_example(oracle_mod):
+    ex = _golden("int8_worked_example.json")
+    s, q, xh = oracle_mod.symmetric_quantize(np.array(ex["w"]), ex["bits"])
+    assert round(s, 5) == ex["s"]
+    assert q.tolist() == ex["q"]
+    # printed to 4 decimals, some truncated rather than rounded (-0.88268 is
+    # printed -0.8826): allow one unit in the last printed digit
+    assert np.allclose(xh, ex["x_hat"], atol=1e-4)
+    err = np.abs(np.array(ex["w"]) - xh)
+    assert np.allclose(err, ex["abs_err"], atol=1e-4)
+    assert np.all(err <= s / 2) and round(s / 2, 4) == ex["err_bound"]
+    o = ex["outlier"]
+    s2, q2, xh2 = oracle_mod.symmetric_quantize(np.array(o["w"]), ex["bits"])
+    assert round(s2, 4) == o["s"]
+    assert q2[:4].tolist() == o["q_first4"]
+    assert np.allclose(xh2[:4], o["x_hat_first4"], atol=5e-4)
+    assert abs(np.max(np.abs(np.array(o["w"][:4]) - xh2[:4])) - o["max_abs_err_first4"]) < 2e-3
