@@ -1,0 +1,217 @@
+/*
+ * nvfp4.h -- C ABI of the B300 (sm_103a) NVFP4 linear-layer library.
+ *
+ * The operation (pages "nvfp4-gemma4", section 2, and "nvfp4-difusion",
+ * section 2): an NVFP4 tensor stores each element as a 4-bit E2M1 code
+ * (1 sign, 2 exponent, 1 mantissa bit), two codes per byte, and one FP8 E4M3
+ * scale for every 16 consecutive elements along the reduction axis K.
+ * Weights are stored (N, K/2) uint8 with scales (N, K/16) E4M3; activations
+ * are quantized at run time; the linear layer is a block-scaled FP4 x FP4
+ * matrix product Y = X W^T written out in bfloat16.
+ *
+ * Readings this library takes where the pages are silent:
+ *  - a per-tensor FP32 global scale g in the decode direction,
+ *    x_hat = e2m1(code) * e4m3(S) * g, with g = amax(|T|) / (6 * 448)
+ *    (g = 1 for an all-zero tensor);
+ *  - block scale S = RNE_E4M3_satfinite((amax_block / 6) / g), codes =
+ *    RNE_E2M1_satfinite(x * (1 / (e4m3(S) * g))) with ties to the even code,
+ *    each step one IEEE binary32 operation; 1/(e4m3(S) * g) is taken as 0
+ *    when S = 0;
+ *  - the even-k element sits in the low nibble of its byte, and a code's
+ *    sign bit is the sign bit of x (a negative value that rounds to zero is
+ *    code 0x8).
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers of the current CUDA device. The
+ *    caller allocates and owns every buffer; the library never allocates,
+ *    frees or synchronizes, except nvfp4_device_error(), which synchronizes.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Work is enqueued asynchronously on it.
+ *  - bfloat16 tensors are passed as void* (2 bytes per element), row-major
+ *    with the given leading dimension (elements between consecutive rows).
+ *  - Packed codes are row-major (rows, K/2) bytes, contiguous.
+ *  - Errors are returned as nvfp4_status; nothing aborts the process. Checks
+ *    on arguments happen before anything is enqueued: on an error return,
+ *    no work was launched. A launch failure returns NVFP4_ERR_CUDA.
+ *    A kernel whose internal bounded wait runs out records
+ *    NVFP4_ERR_TIMEOUT in a device-side word that nvfp4_device_error()
+ *    reports.
+ */
+#ifndef NVFP4_B300_H
+#define NVFP4_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define NVFP4_API __attribute__((visibility("default")))
+#else
+#define NVFP4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nvfp4_status {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1,       /* null pointer, size < 0, bad enum value */
+    NVFP4_ERR_MISALIGNED = 2,        /* a pointer or leading dimension breaks its alignment rule */
+    NVFP4_ERR_UNSUPPORTED_SHAPE = 3, /* K (or cols) is not a multiple the entry point needs */
+    NVFP4_ERR_WORKSPACE_TOO_SMALL = 4,
+    NVFP4_ERR_CUDA = 5,              /* a CUDA runtime or driver call failed */
+    NVFP4_ERR_TIMEOUT = 6            /* a bounded wait inside a kernel ran out */
+} nvfp4_status;
+
+/* Layout of an E4M3 scale tensor of `rows` rows and K/16 scales per row. */
+typedef enum nvfp4_sf_layout {
+    /* (rows, K/16) row-major bytes: the layout the "nvfp4-difusion" page
+     * declares for weight_scale (section 2). */
+    NVFP4_SF_ROW_MAJOR = 0,
+    /* Tensor-core tile layout read directly by the GEMM: rows padded up to a
+     * multiple of 128, K/16 a multiple of 4. Scale (r, j) lives in the
+     * 512-byte tile t = (r / 128) * (K / 64) + j / 4, at byte
+     * (r % 32) * 16 + ((r % 128) / 32) * 4 + j % 4 of that tile. Padding
+     * rows hold 0. Same values as ROW_MAJOR, permuted. */
+    NVFP4_SF_MMA_128x4 = 1
+} nvfp4_sf_layout;
+
+/* Human-readable name of a status code (static string, never NULL). */
+NVFP4_API const char *nvfp4_status_string(int status);
+
+/* Bytes a scale tensor of `rows` x (K/16) needs in `layout`; 0 if K is not
+ * a multiple of 16 (ROW_MAJOR) or 64 (MMA_128x4), or on a bad argument. */
+NVFP4_API size_t nvfp4_sf_bytes(int64_t rows, int64_t K, int layout);
+
+/*
+ * Per-tensor global scale (decode direction) of a bfloat16 tensor:
+ *   *g = amax(|X|) / 2688.0f, or 1.0f if every element is +-0.
+ * X: rows x cols bfloat16, leading dimension ldx (>= cols) elements,
+ * 16-byte aligned, cols % 8 == 0 and ldx % 8 == 0.
+ * g: one float in device memory (4-byte aligned); it is also used as the
+ * reduction cell while the call runs, so it must not alias X.
+ * rows == 0 or cols == 0 writes 1.0f.
+ * Errors: INVALID_ARG (null, negative sizes), MISALIGNED, UNSUPPORTED_SHAPE
+ * (cols % 8 != 0), CUDA.
+ */
+NVFP4_API nvfp4_status nvfp4_global_scale(const void *X, int64_t rows, int64_t cols,
+                                int64_t ldx, float *g, void *stream);
+
+/*
+ * Dynamic NVFP4 quantization of a bfloat16 tensor ("nvfp4-difusion" page,
+ * section 2: the activation is quantized to FP4 at run time), with the
+ * global scale read from device memory.
+ * X: rows x cols bfloat16 (ldx >= cols, ldx % 8 == 0, 16-byte aligned),
+ * cols % 16 == 0 (cols % 64 == 0 for NVFP4_SF_MMA_128x4).
+ * g: device pointer to the decode-direction global scale (finite, > 0).
+ * q: rows x cols/2 bytes, contiguous, 8-byte aligned.
+ * sf: nvfp4_sf_bytes(rows, cols, sf_layout) bytes.
+ * Inputs must be finite. Errors: INVALID_ARG, MISALIGNED,
+ * UNSUPPORTED_SHAPE, CUDA.
+ */
+NVFP4_API nvfp4_status nvfp4_quantize(const void *X, int64_t rows, int64_t cols,
+                            int64_t ldx, const float *g, uint8_t *q,
+                            uint8_t *sf, int sf_layout, void *stream);
+
+/*
+ * Offline weight quantization ("nvfp4-difusion" page, section 2: qweight
+ * (out, in/2) uint8 and weight_scale (out, in/16) float8_e4m3fn):
+ * nvfp4_global_scale(W) into *g_w, then nvfp4_quantize(W, g_w).
+ * W: N x K bfloat16 with leading dimension ldw; Wq: N x K/2 bytes;
+ * Ws: nvfp4_sf_bytes(N, K, sf_layout) bytes; g_w: one device float.
+ * Same requirements and errors as the two calls it makes.
+ */
+NVFP4_API nvfp4_status nvfp4_quantize_weight(const void *W, int64_t N, int64_t K,
+                                   int64_t ldw, uint8_t *Wq, uint8_t *Ws,
+                                   float *g_w, int sf_layout, void *stream);
+
+/*
+ * Permute a row-major scale tensor (rows x K/16) into NVFP4_SF_MMA_128x4
+ * (padding rows set to 0). K % 64 == 0. sf_mma must not alias sf_row_major.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, CUDA.
+ */
+NVFP4_API nvfp4_status nvfp4_sf_to_mma_layout(const uint8_t *sf_row_major, int64_t rows,
+                                    int64_t K, uint8_t *sf_mma, void *stream);
+
+/*
+ * Block-scaled FP4 GEMM ("nvfp4-difusion" page, section 2: the _scaled_mm
+ * call on two float4_e2m1fn_x2 operands with their block scales, bfloat16
+ * out), as a tcgen05 kind::mxf4nvf4 tensor-core kernel:
+ *   Y[m, n] = bf16( g_a * g_b * sum_k e2m1(Aq[m,k]) e4m3(As[m,k/16])
+ *                                    e2m1(Bq[n,k]) e4m3(Bs[n,k/16]) )
+ * with FP32 accumulation.
+ * Aq: M x K/2, Bq: N x K/2 packed codes, 16-byte aligned.
+ * As, Bs: scales in NVFP4_SF_MMA_128x4 layout, 16-byte aligned.
+ * g_a, g_b: device pointers to the two global scales.
+ * Y: M x N bfloat16, leading dimension ldy >= N (rows that start 16-byte
+ * aligned, i.e. 16-byte aligned Y and ldy % 8 == 0, get 16-byte stores).
+ * K % 256 == 0; M, N >= 0 (0 is a no-op).
+ * workspace / workspace_bytes: scratch for the skinny-M split-K path; query
+ * nvfp4_gemm_workspace_bytes(). May be NULL when that returns 0.
+ * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_SHAPE,
+ * WORKSPACE_TOO_SMALL, CUDA.
+ */
+NVFP4_API nvfp4_status nvfp4_gemm(const uint8_t *Aq, const uint8_t *As, const float *g_a,
+                        const uint8_t *Bq, const uint8_t *Bs, const float *g_b,
+                        int64_t M, int64_t N, int64_t K, void *Y, int64_t ldy,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/* Scratch bytes nvfp4_gemm needs for this shape (0 for most shapes). */
+NVFP4_API size_t nvfp4_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* How nvfp4_linear produces the activation's FP4 operand. */
+typedef enum nvfp4_linear_mode {
+    /* nvfp4_quantize into the workspace, then nvfp4_gemm. */
+    NVFP4_LINEAR_UNFUSED = 0,
+    /* The GEMM's producer warps quantize bfloat16 X tiles straight into
+     * shared memory (same arithmetic, bit-identical output). */
+    NVFP4_LINEAR_FUSED = 1
+} nvfp4_linear_mode;
+
+/*
+ * NVFP4 linear layer (the "nvfp4-difusion" page's BlackwellLinear.forward,
+ * section 2): quantize the bfloat16 activation dynamically, then the
+ * block-scaled FP4 GEMM against pre-quantized weights, bfloat16 out.
+ *   Y = bf16( dequant(quantize(X, g_x)) * dequant(Wq, Ws, g_w)^T )
+ * X: M x K bfloat16 (ldx >= K, ldx % 8 == 0, 16-byte aligned), K % 256 == 0.
+ * Wq: N x K/2; Ws: NVFP4_SF_MMA_128x4 scales; g_w: device float.
+ * Y: M x N bfloat16, ldy >= N, 2-byte aligned.
+ * g_x: device pointer to the activation's global scale, or NULL to compute
+ * it from X on the device first (one extra read of X).
+ * mode: nvfp4_linear_mode.
+ * workspace: nvfp4_linear_workspace_bytes(M, N, K, mode) bytes (holds the
+ * quantized activation, its scales and, when g_x is NULL, g_x itself),
+ * 256-byte aligned.
+ * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_SHAPE,
+ * WORKSPACE_TOO_SMALL, CUDA.
+ */
+NVFP4_API nvfp4_status nvfp4_linear(const void *X, int64_t M, int64_t K, int64_t ldx,
+                          const uint8_t *Wq, const uint8_t *Ws,
+                          const float *g_w, int64_t N, void *Y, int64_t ldy,
+                          const float *g_x, int mode, void *workspace,
+                          size_t workspace_bytes, void *stream);
+
+NVFP4_API size_t nvfp4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int mode);
+
+/*
+ * Synchronize the current device, then return NVFP4_ERR_TIMEOUT if any
+ * kernel of this library recorded a bounded-wait timeout since the last
+ * clear, NVFP4_ERR_CUDA if the synchronization failed, else NVFP4_OK.
+ * clear != 0 resets the device-side word.
+ */
+NVFP4_API nvfp4_status nvfp4_device_error(int clear);
+
+/*
+ * Testing hook for the bounded waits (no fault is involved): with
+ * mode = 1 the next GEMM launches' TMA producer issues no loads, so the
+ * consumers' waits run out after timeout_us microseconds and the kernel
+ * records NVFP4_ERR_TIMEOUT and returns. mode = 0 restores normal
+ * operation; timeout_us = 0 restores the default limit (2 s).
+ */
+NVFP4_API nvfp4_status nvfp4_debug_set_fault_injection(int mode, uint32_t timeout_us);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_B300_H */

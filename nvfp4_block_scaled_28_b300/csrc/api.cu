@@ -1,0 +1,276 @@
+// C ABI of the NVFP4 library: argument checks, status codes, workspace
+// carving and the launch sequences of each entry point (see include/nvfp4.h).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "internal.h"
+#include "nvfp4.h"
+#include "ptx.cuh"
+
+namespace nvfp4 {
+
+// Device-side error word: kernels OR kDevErrTimeout into it when a bounded
+// wait runs out. Kernels receive its address as a parameter.
+__device__ unsigned int g_device_error = 0;
+
+unsigned int *device_error_word() {
+    static unsigned int *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<unsigned int *>(p);
+    }
+    return addr[dev];
+}
+
+const LaunchCfg &launch_cfg() {
+    static LaunchCfg cfg;
+    static bool init = false;
+    if (!init) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+            sms > 0)
+            cfg.num_sms = sms;
+        init = true;
+    }
+    return cfg;
+}
+
+DebugState &debug_state() {
+    static DebugState s;
+    return s;
+}
+
+namespace {
+
+inline bool aligned(const void *p, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+inline nvfp4_status from_cuda(cudaError_t e) {
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Limits of the 32-bit index arithmetic inside the kernels.
+constexpr int64_t kMaxBlocks = int64_t(1) << 31;
+constexpr int64_t kMaxDim = int64_t(1) << 30;
+
+nvfp4_status check_bf16_matrix(const void *X, int64_t rows, int64_t cols, int64_t ld) {
+    if (rows < 0 || cols < 0 || ld < cols) return NVFP4_ERR_INVALID_ARG;
+    if (rows > kMaxDim || cols > kMaxDim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (rows > 0 && cols > 0 && X == nullptr) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(X, 16) || (ld % 8) != 0) return NVFP4_ERR_MISALIGNED;
+    return NVFP4_OK;
+}
+
+nvfp4_status check_quantize(const void *X, int64_t rows, int64_t cols, int64_t ldx,
+                            const float *g, const uint8_t *q, const uint8_t *sf, int layout) {
+    if (layout != NVFP4_SF_ROW_MAJOR && layout != NVFP4_SF_MMA_128x4) return NVFP4_ERR_INVALID_ARG;
+    nvfp4_status s = check_bf16_matrix(X, rows, cols, ldx);
+    if (s != NVFP4_OK) return s;
+    if (cols % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (layout == NVFP4_SF_MMA_128x4 && cols % 64 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (rows * (cols / 16) >= kMaxBlocks) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (g == nullptr) return NVFP4_ERR_INVALID_ARG;
+    if (rows > 0 && cols > 0 && (q == nullptr || sf == nullptr)) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(g, 4) || !aligned(q, 8)) return NVFP4_ERR_MISALIGNED;
+    if (layout == NVFP4_SF_MMA_128x4 && !aligned(sf, 4)) return NVFP4_ERR_MISALIGNED;
+    return NVFP4_OK;
+}
+
+// Shapes, the weight-side operand and the output of a GEMM / linear call.
+nvfp4_status check_gemm_b_and_y(const uint8_t *Bq, const uint8_t *Bs, const float *g_b, int64_t M,
+                                int64_t N, int64_t K, const void *Y, int64_t ldy) {
+    if (M < 0 || N < 0 || K <= 0 || ldy < N) return NVFP4_ERR_INVALID_ARG;
+    if (K % 256 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || N == 0) return NVFP4_OK;
+    if (!Bq || !Bs || !g_b || !Y) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(Bq, 16) || !aligned(Bs, 16) || !aligned(g_b, 4) || !aligned(Y, 2))
+        return NVFP4_ERR_MISALIGNED;
+    return NVFP4_OK;
+}
+
+nvfp4_status check_gemm(const uint8_t *Aq, const uint8_t *As, const float *g_a,
+                        const uint8_t *Bq, const uint8_t *Bs, const float *g_b, int64_t M,
+                        int64_t N, int64_t K, const void *Y, int64_t ldy) {
+    nvfp4_status s = check_gemm_b_and_y(Bq, Bs, g_b, M, N, K, Y, ldy);
+    if (s != NVFP4_OK || M == 0 || N == 0) return s;
+    if (!Aq || !As || !g_a) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(Aq, 16) || !aligned(As, 16) || !aligned(g_a, 4)) return NVFP4_ERR_MISALIGNED;
+    return NVFP4_OK;
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" {
+
+const char *nvfp4_status_string(int status) {
+    switch (status) {
+        case NVFP4_OK: return "NVFP4_OK";
+        case NVFP4_ERR_INVALID_ARG: return "NVFP4_ERR_INVALID_ARG";
+        case NVFP4_ERR_MISALIGNED: return "NVFP4_ERR_MISALIGNED";
+        case NVFP4_ERR_UNSUPPORTED_SHAPE: return "NVFP4_ERR_UNSUPPORTED_SHAPE";
+        case NVFP4_ERR_WORKSPACE_TOO_SMALL: return "NVFP4_ERR_WORKSPACE_TOO_SMALL";
+        case NVFP4_ERR_CUDA: return "NVFP4_ERR_CUDA";
+        case NVFP4_ERR_TIMEOUT: return "NVFP4_ERR_TIMEOUT";
+        default: return "NVFP4_ERR_UNKNOWN";
+    }
+}
+
+size_t nvfp4_sf_bytes(int64_t rows, int64_t K, int layout) {
+    if (rows < 0 || K < 0) return 0;
+    if (layout == NVFP4_SF_ROW_MAJOR) {
+        if (K % 16) return 0;
+        return static_cast<size_t>(rows) * static_cast<size_t>(K / 16);
+    }
+    if (layout == NVFP4_SF_MMA_128x4) {
+        if (K % 64) return 0;
+        return static_cast<size_t>((rows + 127) / 128 * 128) * static_cast<size_t>(K / 16);
+    }
+    return 0;
+}
+
+nvfp4_status nvfp4_global_scale(const void *X, int64_t rows, int64_t cols, int64_t ldx, float *g,
+                                void *stream) {
+    nvfp4_status s = check_bf16_matrix(X, rows, cols, ldx);
+    if (s != NVFP4_OK) return s;
+    if (g == nullptr) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(g, 4)) return NVFP4_ERR_MISALIGNED;
+    if (cols % 8 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (rows * (cols / 8) >= kMaxBlocks) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    return from_cuda(launch_global_scale(static_cast<const uint16_t *>(X), rows, cols, ldx, g,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status nvfp4_quantize(const void *X, int64_t rows, int64_t cols, int64_t ldx, const float *g,
+                            uint8_t *q, uint8_t *sf, int sf_layout, void *stream) {
+    nvfp4_status s = check_quantize(X, rows, cols, ldx, g, q, sf, sf_layout);
+    if (s != NVFP4_OK) return s;
+    return from_cuda(launch_quantize(static_cast<const uint16_t *>(X), rows, cols, ldx, g, q, sf,
+                                     sf_layout, static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status nvfp4_quantize_weight(const void *W, int64_t N, int64_t K, int64_t ldw, uint8_t *Wq,
+                                   uint8_t *Ws, float *g_w, int sf_layout, void *stream) {
+    nvfp4_status s = check_quantize(W, N, K, ldw, g_w, Wq, Ws, sf_layout);
+    if (s != NVFP4_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_global_scale(static_cast<const uint16_t *>(W), N, K, ldw, g_w, st);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    return from_cuda(
+        launch_quantize(static_cast<const uint16_t *>(W), N, K, ldw, g_w, Wq, Ws, sf_layout, st));
+}
+
+nvfp4_status nvfp4_sf_to_mma_layout(const uint8_t *sf_row_major, int64_t rows, int64_t K,
+                                    uint8_t *sf_mma, void *stream) {
+    if (rows < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
+    if (K % 64 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (rows > kMaxDim || (rows + 127) / 128 * 128 * (K / 64) >= kMaxBlocks)
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0 || K == 0) return NVFP4_OK;
+    if (!sf_row_major || !sf_mma) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(sf_row_major, 4) || !aligned(sf_mma, 4)) return NVFP4_ERR_MISALIGNED;
+    return from_cuda(
+        launch_sf_to_mma(sf_row_major, rows, K, sf_mma, static_cast<cudaStream_t>(stream)));
+}
+
+size_t nvfp4_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    (void)M;
+    (void)N;
+    (void)K;
+    return 0;
+}
+
+nvfp4_status nvfp4_gemm(const uint8_t *Aq, const uint8_t *As, const float *g_a, const uint8_t *Bq,
+                        const uint8_t *Bs, const float *g_b, int64_t M, int64_t N, int64_t K,
+                        void *Y, int64_t ldy, void *workspace, size_t workspace_bytes,
+                        void *stream) {
+    nvfp4_status s = check_gemm(Aq, As, g_a, Bq, Bs, g_b, M, N, K, Y, ldy);
+    if (s != NVFP4_OK) return s;
+    if (workspace_bytes < nvfp4_gemm_workspace_bytes(M, N, K))
+        return NVFP4_ERR_WORKSPACE_TOO_SMALL;
+    (void)workspace;
+    if (M == 0 || N == 0) return NVFP4_OK;
+    GemmArgs a{Aq, As, g_a, Bq, Bs, g_b, M, N, K, static_cast<uint16_t *>(Y), ldy};
+    return from_cuda(launch_gemm(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t nvfp4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int mode) {
+    if (M < 0 || N < 0 || K < 0 || K % 256 != 0) return 0;
+    (void)mode;
+    size_t bytes = 256;  // g_x
+    bytes += round_up(static_cast<size_t>(M) * static_cast<size_t>(K / 2), 256);
+    bytes += round_up(nvfp4_sf_bytes(M, K, NVFP4_SF_MMA_128x4), 256);
+    bytes += nvfp4_gemm_workspace_bytes(M, N, K);
+    return bytes;
+}
+
+nvfp4_status nvfp4_linear(const void *X, int64_t M, int64_t K, int64_t ldx, const uint8_t *Wq,
+                          const uint8_t *Ws, const float *g_w, int64_t N, void *Y, int64_t ldy,
+                          const float *g_x, int mode, void *workspace, size_t workspace_bytes,
+                          void *stream) {
+    if (mode != NVFP4_LINEAR_UNFUSED && mode != NVFP4_LINEAR_FUSED) return NVFP4_ERR_INVALID_ARG;
+    nvfp4_status s = check_bf16_matrix(X, M, K, ldx);
+    if (s != NVFP4_OK) return s;
+    s = check_gemm_b_and_y(Wq, Ws, g_w, M, N, K, Y, ldy);
+    if (s != NVFP4_OK) return s;
+    if (M == 0 || N == 0) return NVFP4_OK;
+    if (g_x != nullptr && !aligned(g_x, 4)) return NVFP4_ERR_MISALIGNED;
+    const size_t need = nvfp4_linear_workspace_bytes(M, N, K, mode);
+    if (workspace_bytes < need) return NVFP4_ERR_WORKSPACE_TOO_SMALL;
+    if (workspace == nullptr) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return NVFP4_ERR_MISALIGNED;
+    if (M * (K / 16) >= kMaxBlocks) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *gx_slot = reinterpret_cast<float *>(ws);
+    uint8_t *xq = ws + 256;
+    uint8_t *xs = xq + round_up(static_cast<size_t>(M) * static_cast<size_t>(K / 2), 256);
+    const uint16_t *Xh = static_cast<const uint16_t *>(X);
+    cudaError_t e;
+    if (g_x == nullptr) {
+        e = launch_global_scale(Xh, M, K, ldx, gx_slot, st);
+        if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+        g_x = gx_slot;
+    }
+    // The fused mode shares the unfused launch sequence until its kernel lands.
+    e = launch_quantize(Xh, M, K, ldx, g_x, xq, xs, NVFP4_SF_MMA_128x4, st);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    GemmArgs a{xq, xs, g_x, Wq, Ws, g_w, M, N, K, static_cast<uint16_t *>(Y), ldy};
+    return from_cuda(launch_gemm(a, st));
+}
+
+nvfp4_status nvfp4_device_error(int clear) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return NVFP4_ERR_CUDA;
+    unsigned int word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_device_error, sizeof(word)) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    if (clear) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+    }
+    return (word & kDevErrTimeout) ? NVFP4_ERR_TIMEOUT : NVFP4_OK;
+}
+
+nvfp4_status nvfp4_debug_set_fault_injection(int mode, uint32_t timeout_us) {
+    if (mode != 0 && mode != 1) return NVFP4_ERR_INVALID_ARG;
+    debug_state().inject = mode;
+    debug_state().timeout_ns =
+        timeout_us == 0 ? 2000000000ull : static_cast<uint64_t>(timeout_us) * 1000ull;
+    return NVFP4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,70 @@
+// Internal launchers shared by the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "nvfp4.h"
+
+namespace nvfp4 {
+
+// 32-bit division by a runtime constant with a multiply-high and a shift
+// (round-up reciprocal method); valid for every 32-bit dividend.
+struct FastDiv {
+    uint32_t d, mul, shift;
+    FastDiv() : d(1), mul(0), shift(0) {}
+    explicit FastDiv(uint32_t divisor) : d(divisor), mul(0), shift(0) {
+        if (d > 1) {
+            uint32_t s = 0;
+            while ((1ull << s) < d) ++s;
+            shift = s;
+            mul = static_cast<uint32_t>(((1ull << 32) * ((1ull << s) - d)) / d + 1);
+        }
+    }
+    __device__ __forceinline__ uint32_t div(uint32_t n) const {
+        if (d == 1) return n;
+        return static_cast<uint32_t>(
+            (static_cast<uint64_t>(__umulhi(n, mul)) + n) >> shift);
+    }
+};
+
+struct LaunchCfg {
+    int num_sms = 148;
+};
+const LaunchCfg &launch_cfg();
+
+// global scale (g_out doubles as the reduction cell)
+cudaError_t launch_global_scale(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
+                                float *g_out, cudaStream_t st);
+
+cudaError_t launch_quantize(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
+                            const float *g, uint8_t *q, uint8_t *sf, int layout,
+                            cudaStream_t st);
+
+cudaError_t launch_sf_to_mma(const uint8_t *sf_rm, int64_t rows, int64_t K, uint8_t *sf_mma,
+                             cudaStream_t st);
+
+struct GemmArgs {
+    const uint8_t *Aq, *As;
+    const float *g_a;
+    const uint8_t *Bq, *Bs;
+    const float *g_b;
+    int64_t M, N, K;
+    uint16_t *Y;
+    int64_t ldy;
+};
+
+cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st);
+
+// Device address of the library's error word on the current device.
+unsigned int *device_error_word();
+
+// fault-injection state for the bounded-wait tests
+struct DebugState {
+    int inject = 0;
+    uint64_t timeout_ns = 2000000000ull;
+};
+DebugState &debug_state();
+
+}  // namespace nvfp4

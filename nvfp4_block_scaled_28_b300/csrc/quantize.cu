@@ -1,0 +1,257 @@
+// NVFP4 quantization kernels: per-tensor amax -> global scale, the
+// bandwidth-bound bfloat16 -> NVFP4 quantizer, and the scale-layout
+// permutation used by the tensor-core GEMM.
+//
+// Format ("nvfp4-gemma4" page, section 2; "nvfp4-difusion" page, section 2):
+// E2M1 codes two per byte, one E4M3 scale per 16 consecutive elements.
+// Scale rule (absmax, the same section's table) with the decode-direction
+// global scale g of this library:
+//   S = E4M3_rne_satfinite((amax_block / 6) / g)
+//   r = 1 / (e4m3(S) * g)   (0 when S == 0)
+//   code = E2M1_rne_satfinite(x * r), sign bit = sign bit of x.
+// Every float step is one IEEE binary32 operation (explicit _rn intrinsics,
+// never contracted), so the bytes do not depend on compiler flags.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Largest |x| of the 8 bfloat16 pairs as a bfloat16 magnitude bit pattern.
+// Non-negative floats order like their bit patterns, so this is exact.
+__device__ __forceinline__ uint32_t amax_bits16(uint4 a, uint4 b) {
+    const uint32_t m = 0x7FFF7FFFu;
+    uint32_t t0 = max_u16x2(a.x & m, a.y & m);
+    uint32_t t1 = max_u16x2(a.z & m, a.w & m);
+    uint32_t t2 = max_u16x2(b.x & m, b.y & m);
+    uint32_t t3 = max_u16x2(b.z & m, b.w & m);
+    uint32_t t = max_u16x2(max_u16x2(t0, t1), max_u16x2(t2, t3));
+    return max(t & 0xFFFFu, t >> 16);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Four E2M1 codes of the two bfloat16 pairs w0 (elements 0,1) and w1
+// (elements 2,3), packed little-end first.
+__device__ __forceinline__ uint32_t codes4(uint32_t w0, uint32_t w1, float r) {
+    uint32_t b0 = cvt_e2m1x2(__fmul_rn(bf16_lo(w0), r), __fmul_rn(bf16_hi(w0), r));
+    uint32_t b1 = cvt_e2m1x2(__fmul_rn(bf16_lo(w1), r), __fmul_rn(bf16_hi(w1), r));
+    return b0 | (b1 << 8);
+}
+
+// Quantize one 16-element block held in (a, b). Returns the scale byte and
+// writes the 8 code bytes into (lo, hi).
+__device__ __forceinline__ uint32_t quantize16(uint4 a, uint4 b, float g, uint32_t &lo,
+                                               uint32_t &hi) {
+    const float amax = __uint_as_float(amax_bits16(a, b) << 16);
+    const float v = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
+    const uint32_t S = cvt_e4m3_satfinite(v);
+    const float s = e4m3_to_f32(S);
+    const float denom = __fmul_rn(s, g);
+    const float r = denom > 0.0f ? __frcp_rn(denom) : 0.0f;
+    lo = codes4(a.x, a.y, r) | (codes4(a.z, a.w, r) << 16);
+    hi = codes4(b.x, b.y, r) | (codes4(b.z, b.w, r) << 16);
+    return S;
+}
+
+// Byte offset of scale (row, kb) in the 128x4 tensor-core tile layout.
+__device__ __forceinline__ uint64_t sf_mma_offset(uint32_t row, uint32_t kb, uint32_t kb4) {
+    const uint32_t R = row >> 7, r = row & 127u;
+    return ((static_cast<uint64_t>(R) * kb4 + (kb >> 2)) << 9) + ((r & 31u) << 4) +
+           ((r >> 5) << 2) + (kb & 3u);
+}
+
+// One thread per 16-element block, two blocks in flight per thread.
+template <int kLayout>
+__global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t *__restrict__ X,
+                                                            uint32_t rows, uint32_t kbpr,
+                                                            uint64_t ldx, FastDiv div_kbpr,
+                                                            const float *__restrict__ g_ptr,
+                                                            uint8_t *__restrict__ q,
+                                                            uint8_t *__restrict__ sf) {
+    const float g = *g_ptr;
+    const uint32_t total = rows * kbpr;
+    const uint32_t stride = gridDim.x * blockDim.x;
+    const uint32_t kb4 = kbpr >> 2;
+    for (uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += 2 * stride) {
+        const uint32_t i1 = i0 + stride;
+        const bool has1 = i1 < total;
+        const uint32_t row0 = div_kbpr.div(i0), kb0 = i0 - row0 * kbpr;
+        const uint32_t row1 = has1 ? div_kbpr.div(i1) : row0;
+        const uint32_t kb1 = has1 ? i1 - row1 * kbpr : kb0;
+        const uint4 *p0 = reinterpret_cast<const uint4 *>(X + row0 * ldx + kb0 * 16ull);
+        const uint4 *p1 = reinterpret_cast<const uint4 *>(X + row1 * ldx + kb1 * 16ull);
+        const uint4 a0 = ld_stream(p0), b0 = ld_stream(p0 + 1);
+        uint4 a1 = make_uint4(0, 0, 0, 0), b1 = a1;
+        if (has1) {
+            a1 = ld_stream(p1);
+            b1 = ld_stream(p1 + 1);
+        }
+        uint32_t lo, hi;
+        uint32_t S = quantize16(a0, b0, g, lo, hi);
+        *reinterpret_cast<uint2 *>(q + static_cast<uint64_t>(i0) * 8) = make_uint2(lo, hi);
+        if (kLayout == NVFP4_SF_ROW_MAJOR)
+            sf[i0] = static_cast<uint8_t>(S);
+        else
+            sf[sf_mma_offset(row0, kb0, kb4)] = static_cast<uint8_t>(S);
+        if (has1) {
+            S = quantize16(a1, b1, g, lo, hi);
+            *reinterpret_cast<uint2 *>(q + static_cast<uint64_t>(i1) * 8) = make_uint2(lo, hi);
+            if (kLayout == NVFP4_SF_ROW_MAJOR)
+                sf[i1] = static_cast<uint8_t>(S);
+            else
+                sf[sf_mma_offset(row1, kb1, kb4)] = static_cast<uint8_t>(S);
+        }
+    }
+}
+
+// amax(|X|) over 16-byte vectors as a bfloat16 magnitude bit pattern,
+// combined across the grid with atomicMax on `cell` (zeroed beforehand).
+__global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t *__restrict__ X,
+                                                        uint32_t rows, uint32_t vpr,
+                                                        uint64_t ldx, FastDiv div_vpr,
+                                                        uint32_t *cell) {
+    const uint32_t total = rows * vpr;
+    const uint32_t stride = gridDim.x * blockDim.x;
+    const uint32_t m = 0x7FFF7FFFu;
+    uint32_t acc = 0;
+    uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < total; i += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t j = i + u * stride;
+            const uint32_t r = div_vpr.div(j), c = j - r * vpr;
+            v[u] = ld_stream(reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            acc = max_u16x2(acc, max_u16x2(max_u16x2(v[u].x & m, v[u].y & m),
+                                           max_u16x2(v[u].z & m, v[u].w & m)));
+        }
+    }
+    for (; i < total; i += stride) {
+        const uint32_t r = div_vpr.div(i), c = i - r * vpr;
+        const uint4 v = ld_stream(reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull));
+        acc = max_u16x2(acc, max_u16x2(max_u16x2(v.x & m, v.y & m), max_u16x2(v.z & m, v.w & m)));
+    }
+    uint32_t a = max(acc & 0xFFFFu, acc >> 16);
+    a = __reduce_max_sync(0xFFFFFFFFu, a);
+    __shared__ uint32_t warp_max[kThreads / 32];
+    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = a;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        uint32_t b = threadIdx.x < kThreads / 32 ? warp_max[threadIdx.x] : 0u;
+        b = __reduce_max_sync(0xFFFFFFFFu, b);
+        if (threadIdx.x == 0 && b != 0) atomicMax(cell, b);
+    }
+}
+
+// g = amax / (6 * 448), or 1 for an all-zero tensor; in place over the cell.
+__global__ void global_scale_finalize(uint32_t *cell) {
+    const float amax = __uint_as_float(*cell << 16);
+    const float g = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+    *reinterpret_cast<float *>(cell) = g;
+}
+
+// Row-major scales -> 128x4 tile layout; one thread per group of 4 scales.
+__global__ void __launch_bounds__(kThreads) sf_to_mma_kernel(const uint8_t *__restrict__ src,
+                                                             uint32_t rows, uint32_t rows_pad,
+                                                             uint32_t kb4, FastDiv div_kb4,
+                                                             uint8_t *__restrict__ dst) {
+    const uint32_t total = rows_pad * kb4;
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += gridDim.x * blockDim.x) {
+        const uint32_t row = div_kb4.div(i), G = i - row * kb4;
+        uint32_t v = 0;
+        if (row < rows) v = *reinterpret_cast<const uint32_t *>(src + static_cast<uint64_t>(i) * 4);
+        *reinterpret_cast<uint32_t *>(dst + sf_mma_offset(row, G * 4, kb4)) = v;
+    }
+}
+
+int grid_for(uint64_t work_items, int per_thread) {
+    const uint64_t threads = (work_items + per_thread - 1) / per_thread;
+    uint64_t blocks = (threads + kThreads - 1) / kThreads;
+    const uint64_t cap = static_cast<uint64_t>(launch_cfg().num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return static_cast<int>(blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_global_scale(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
+                                float *g_out, cudaStream_t st) {
+    uint32_t *cell = reinterpret_cast<uint32_t *>(g_out);
+    cudaError_t e = cudaMemsetAsync(cell, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
+    const uint32_t vpr = static_cast<uint32_t>(cols / 8);
+    const uint64_t total = static_cast<uint64_t>(rows) * vpr;
+    if (total > 0) {
+        amax_kernel<<<grid_for(total, 4), kThreads, 0, st>>>(X, static_cast<uint32_t>(rows), vpr,
+                                                             static_cast<uint64_t>(ldx),
+                                                             FastDiv(vpr), cell);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    global_scale_finalize<<<1, 1, 0, st>>>(cell);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
+                            const float *g, uint8_t *q, uint8_t *sf, int layout,
+                            cudaStream_t st) {
+    const uint32_t kbpr = static_cast<uint32_t>(cols / 16);
+    const uint64_t total = static_cast<uint64_t>(rows) * kbpr;
+    if (layout == NVFP4_SF_MMA_128x4 && (rows % 128) != 0) {
+        // zero the last (partial) 128-row tile group so padding rows read 0
+        const uint64_t tile_bytes = static_cast<uint64_t>(kbpr / 4) * 512;
+        const uint64_t first = static_cast<uint64_t>(rows / 128) * tile_bytes;
+        cudaError_t e = cudaMemsetAsync(sf + first, 0, tile_bytes, st);
+        if (e != cudaSuccess) return e;
+    }
+    if (total == 0) return cudaSuccess;
+    const int grid = grid_for(total, 2);
+    if (layout == NVFP4_SF_ROW_MAJOR)
+        quantize_kernel<NVFP4_SF_ROW_MAJOR><<<grid, kThreads, 0, st>>>(
+            X, static_cast<uint32_t>(rows), kbpr, static_cast<uint64_t>(ldx), FastDiv(kbpr), g, q,
+            sf);
+    else
+        quantize_kernel<NVFP4_SF_MMA_128x4><<<grid, kThreads, 0, st>>>(
+            X, static_cast<uint32_t>(rows), kbpr, static_cast<uint64_t>(ldx), FastDiv(kbpr), g, q,
+            sf);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sf_to_mma(const uint8_t *sf_rm, int64_t rows, int64_t K, uint8_t *sf_mma,
+                             cudaStream_t st) {
+    const uint32_t kb4 = static_cast<uint32_t>(K / 64);
+    const uint32_t rows_pad = static_cast<uint32_t>((rows + 127) / 128 * 128);
+    const uint64_t total = static_cast<uint64_t>(rows_pad) * kb4;
+    if (total == 0) return cudaSuccess;
+    sf_to_mma_kernel<<<grid_for(total, 1), kThreads, 0, st>>>(
+        sf_rm, static_cast<uint32_t>(rows), rows_pad, kb4, FastDiv(kb4), sf_mma);
+    return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,209 @@
+"""Thin PyTorch binding over the C ABI (argument marshalling only).
+
+Each function checks dtypes, shapes, devices and contiguity, allocates the
+outputs it returns with torch (device memory is torch's job here), and calls
+the C entry point of the same name on the current CUDA stream. All
+arithmetic happens in the library's CUDA kernels.
+
+The checks guard the failure the "nvfp4-gemma4" page reports in section 4:
+a packed FP4 tensor read as bfloat16 has half the columns it should, so
+every packed operand is checked for dtype uint8 and shape (rows, K/2), and
+every scale tensor for its exact byte count.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _native as N
+
+SF_ROW_MAJOR = N.SF_ROW_MAJOR
+SF_MMA_128x4 = N.SF_MMA_128x4
+LINEAR_UNFUSED = N.LINEAR_UNFUSED
+LINEAR_FUSED = N.LINEAR_FUSED
+NVFP4Error = N.NVFP4Error
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _require(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def _check_cuda(*ts) -> None:
+    for t in ts:
+        if t is not None:
+            _require(t.is_cuda, "tensors must be on a CUDA device")
+
+
+def _check_bf16_2d(x: torch.Tensor, name: str) -> None:
+    _require(x.dtype == torch.bfloat16, "%s must be bfloat16, got %s" % (name, x.dtype))
+    _require(x.dim() == 2, "%s must be 2-D" % name)
+    _require(x.stride(1) == 1, "%s must have unit stride along K" % name)
+
+
+def _check_codes(q: torch.Tensor, rows: int, K: int, name: str) -> None:
+    _require(q.dtype == torch.uint8, "%s must be uint8 packed FP4, got %s" % (name, q.dtype))
+    _require(tuple(q.shape) == (rows, K // 2),
+             "%s must have shape (%d, %d) (two FP4 codes per byte), got %s"
+             % (name, rows, K // 2, tuple(q.shape)))
+    _require(q.is_contiguous(), "%s must be contiguous" % name)
+
+
+def _check_scales(s: torch.Tensor, rows: int, K: int, layout: int, name: str) -> None:
+    _require(s.dtype in (torch.uint8, torch.float8_e4m3fn),
+             "%s must be uint8 or float8_e4m3fn, got %s" % (name, s.dtype))
+    _require(s.is_contiguous(), "%s must be contiguous" % name)
+    need = sf_bytes(rows, K, layout)
+    _require(s.numel() == need, "%s must hold %d scale bytes for (%d rows, K=%d), got %d"
+             % (name, need, rows, K, s.numel()))
+
+
+def _check_g(g: torch.Tensor, name: str) -> None:
+    _require(g.dtype == torch.float32 and g.numel() >= 1, "%s must be a float32 tensor" % name)
+
+
+def sf_bytes(rows: int, K: int, layout: int) -> int:
+    return int(N.load().nvfp4_sf_bytes(rows, K, layout))
+
+
+def sf_shape(rows: int, K: int, layout: int):
+    if layout == SF_ROW_MAJOR:
+        return (rows, K // 16)
+    return ((rows + 127) // 128 * 128, K // 16)
+
+
+def nvfp4_global_scale(X: torch.Tensor, g: torch.Tensor | None = None) -> torch.Tensor:
+    """Decode-direction global scale amax(|X|) / (6 * 448) as a 1-element
+    float32 device tensor (1.0 for an all-zero X)."""
+    _check_bf16_2d(X, "X")
+    _check_cuda(X)
+    if g is None:
+        g = torch.empty(1, dtype=torch.float32, device=X.device)
+    _check_g(g, "g")
+    N.check("nvfp4_global_scale", N.load().nvfp4_global_scale(
+        _ptr(X), X.shape[0], X.shape[1], X.stride(0), _ptr(g), _stream()))
+    return g
+
+
+def nvfp4_quantize(X: torch.Tensor, g: torch.Tensor, sf_layout: int = SF_ROW_MAJOR,
+                   q: torch.Tensor | None = None, sf: torch.Tensor | None = None):
+    """Quantize bfloat16 X (rows, K) to packed E2M1 codes (rows, K/2) uint8
+    and E4M3 block scales (uint8 bytes) in ``sf_layout``."""
+    _check_bf16_2d(X, "X")
+    _check_g(g, "g")
+    _check_cuda(X, g)
+    rows, K = X.shape
+    _require(K % 16 == 0, "K must be a multiple of 16")
+    if q is None:
+        q = torch.empty((rows, K // 2), dtype=torch.uint8, device=X.device)
+    if sf is None:
+        sf = torch.empty(sf_shape(rows, K, sf_layout), dtype=torch.uint8, device=X.device)
+    _check_codes(q, rows, K, "q")
+    _check_scales(sf, rows, K, sf_layout, "sf")
+    N.check("nvfp4_quantize", N.load().nvfp4_quantize(
+        _ptr(X), rows, K, X.stride(0), _ptr(g), _ptr(q), _ptr(sf), sf_layout, _stream()))
+    return q, sf
+
+
+def nvfp4_quantize_weight(W: torch.Tensor, sf_layout: int = SF_MMA_128x4):
+    """Offline weight quantization: returns (Wq (N, K/2) uint8, Ws scales,
+    g_w 1-element float32)."""
+    _check_bf16_2d(W, "W")
+    _check_cuda(W)
+    rows, K = W.shape
+    Wq = torch.empty((rows, K // 2), dtype=torch.uint8, device=W.device)
+    Ws = torch.empty(sf_shape(rows, K, sf_layout), dtype=torch.uint8, device=W.device)
+    g = torch.empty(1, dtype=torch.float32, device=W.device)
+    N.check("nvfp4_quantize_weight", N.load().nvfp4_quantize_weight(
+        _ptr(W), rows, K, W.stride(0), _ptr(Wq), _ptr(Ws), _ptr(g), sf_layout, _stream()))
+    return Wq, Ws, g
+
+
+def nvfp4_sf_to_mma_layout(sf_row_major: torch.Tensor, rows: int, K: int) -> torch.Tensor:
+    _check_scales(sf_row_major, rows, K, SF_ROW_MAJOR, "sf_row_major")
+    _check_cuda(sf_row_major)
+    out = torch.empty(sf_shape(rows, K, SF_MMA_128x4), dtype=torch.uint8,
+                      device=sf_row_major.device)
+    N.check("nvfp4_sf_to_mma_layout", N.load().nvfp4_sf_to_mma_layout(
+        _ptr(sf_row_major), rows, K, _ptr(out), _stream()))
+    return out
+
+
+def gemm_workspace_bytes(M: int, Nn: int, K: int) -> int:
+    return int(N.load().nvfp4_gemm_workspace_bytes(M, Nn, K))
+
+
+def linear_workspace_bytes(M: int, Nn: int, K: int, mode: int = LINEAR_UNFUSED) -> int:
+    return int(N.load().nvfp4_linear_workspace_bytes(M, Nn, K, mode))
+
+
+def nvfp4_gemm(Aq, As, g_a, Bq, Bs, g_b, K: int, Y: torch.Tensor | None = None,
+               workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Block-scaled FP4 GEMM, scales in the 128x4 tile layout:
+    Y (M, N) bfloat16 = g_a g_b (A_hat @ B_hat^T)."""
+    M, Nn = Aq.shape[0], Bq.shape[0]
+    _check_codes(Aq, M, K, "Aq")
+    _check_codes(Bq, Nn, K, "Bq")
+    _check_scales(As, M, K, SF_MMA_128x4, "As")
+    _check_scales(Bs, Nn, K, SF_MMA_128x4, "Bs")
+    _check_g(g_a, "g_a")
+    _check_g(g_b, "g_b")
+    _check_cuda(Aq, As, g_a, Bq, Bs, g_b, Y, workspace)
+    if Y is None:
+        Y = torch.empty((M, Nn), dtype=torch.bfloat16, device=Aq.device)
+    _check_bf16_2d(Y, "Y")
+    _require(tuple(Y.shape) == (M, Nn), "Y must have shape (%d, %d)" % (M, Nn))
+    need = gemm_workspace_bytes(M, Nn, K)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=Aq.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    N.check("nvfp4_gemm", N.load().nvfp4_gemm(
+        _ptr(Aq), _ptr(As), _ptr(g_a), _ptr(Bq), _ptr(Bs), _ptr(g_b), M, Nn, K,
+        _ptr(Y), Y.stride(0), _ptr(workspace), ws_bytes, _stream()))
+    return Y
+
+
+def nvfp4_linear(X: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, g_w: torch.Tensor,
+                 g_x: torch.Tensor | None = None, mode: int = LINEAR_UNFUSED,
+                 Y: torch.Tensor | None = None,
+                 workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """NVFP4 linear layer: Y = bf16(quant(X) @ dequant(Wq, Ws, g_w)^T), the
+    activation quantized on the fly (g_x computed from X when None)."""
+    _check_bf16_2d(X, "X")
+    M, K = X.shape
+    Nn = Wq.shape[0]
+    _check_codes(Wq, Nn, K, "Wq")
+    _check_scales(Ws, Nn, K, SF_MMA_128x4, "Ws")
+    _check_g(g_w, "g_w")
+    if g_x is not None:
+        _check_g(g_x, "g_x")
+    _check_cuda(X, Wq, Ws, g_w, g_x, Y, workspace)
+    if Y is None:
+        Y = torch.empty((M, Nn), dtype=torch.bfloat16, device=X.device)
+    _check_bf16_2d(Y, "Y")
+    _require(tuple(Y.shape) == (M, Nn), "Y must have shape (%d, %d)" % (M, Nn))
+    need = linear_workspace_bytes(M, Nn, K, mode)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=X.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    N.check("nvfp4_linear", N.load().nvfp4_linear(
+        _ptr(X), M, K, X.stride(0), _ptr(Wq), _ptr(Ws), _ptr(g_w), Nn, _ptr(Y), Y.stride(0),
+        _ptr(g_x), mode, _ptr(workspace), ws_bytes, _stream()))
+    return Y
+
+
+def nvfp4_device_error(clear: bool = True) -> int:
+    """Synchronize and return the device-side status (OK or ERR_TIMEOUT)."""
+    return int(N.load().nvfp4_device_error(1 if clear else 0))
+
+
+def nvfp4_debug_set_fault_injection(mode: int, timeout_us: int = 0) -> None:
+    N.check("nvfp4_debug_set_fault_injection",
+            N.load().nvfp4_debug_set_fault_injection(mode, timeout_us))

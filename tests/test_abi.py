@@ -1,0 +1,127 @@
+"""The C-ABI library loads, exports every entry point include/nvfp4.h
+declares, and rejects bad arguments before launching anything (no GPU
+needed: every case here fails the host-side checks)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import nvfp4_block_scaled_28_b300 as nv
+from nvfp4_block_scaled_28_b300 import _native as N
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"NVFP4_API\s+[\w\s\*]+?\b(nvfp4_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from nvfp4_block_scaled_28_b300 import build
+    build.build()
+    return N.load()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("nvfp4_quantize", "nvfp4_quantize_weight", "nvfp4_linear", "nvfp4_gemm",
+                 "nvfp4_global_scale", "nvfp4_device_error"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert names
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(N.SIGNATURES), "binding and header disagree"
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "NVFP4_OK"), (1, "NVFP4_ERR_INVALID_ARG"), (2, "NVFP4_ERR_MISALIGNED"),
+                       (3, "NVFP4_ERR_UNSUPPORTED_SHAPE"), (4, "NVFP4_ERR_WORKSPACE_TOO_SMALL"),
+                       (5, "NVFP4_ERR_CUDA"), (6, "NVFP4_ERR_TIMEOUT"), (99, "NVFP4_ERR_UNKNOWN")]:
+        assert lib.nvfp4_status_string(code).decode() == name
+
+
+def test_sf_bytes(lib):
+    assert lib.nvfp4_sf_bytes(300, 256, 0) == 300 * 16
+    assert lib.nvfp4_sf_bytes(300, 256, 1) == 384 * 16
+    assert lib.nvfp4_sf_bytes(128, 64, 1) == 128 * 4
+    assert lib.nvfp4_sf_bytes(3, 40, 0) == 0  # K % 16
+    assert lib.nvfp4_sf_bytes(3, 48, 1) == 0  # K % 64
+    assert lib.nvfp4_sf_bytes(-1, 64, 0) == 0
+
+
+# fake, never-dereferenced addresses: every call below fails its checks first
+A16 = 0x10000
+ODD = 0x10001
+
+
+def test_quantize_argument_checks(lib):
+    q = lib.nvfp4_quantize
+    assert q(A16, 4, 40, 40, A16, A16, A16, 0, None) == N.ERR_UNSUPPORTED_SHAPE  # K % 16
+    assert q(A16, 4, 48, 48, A16, A16, A16, 1, None) == N.ERR_UNSUPPORTED_SHAPE  # K % 64 (tile)
+    assert q(ODD, 4, 64, 64, A16, A16, A16, 0, None) == N.ERR_MISALIGNED
+    assert q(A16, 4, 64, 60, A16, A16, A16, 0, None) == N.ERR_INVALID_ARG  # ld < cols
+    assert q(A16, 4, 64, 68, A16, A16, A16, 0, None) == N.ERR_MISALIGNED  # ld % 8
+    assert q(A16, 4, 64, 64, None, A16, A16, 0, None) == N.ERR_INVALID_ARG  # g
+    assert q(A16, 4, 64, 64, A16, None, A16, 0, None) == N.ERR_INVALID_ARG  # q
+    assert q(A16, 4, 64, 64, A16, A16, A16, 7, None) == N.ERR_INVALID_ARG  # layout
+    assert q(A16, -1, 64, 64, A16, A16, A16, 0, None) == N.ERR_INVALID_ARG
+    assert q(None, 4, 64, 64, A16, A16, A16, 0, None) == N.ERR_INVALID_ARG
+
+
+def test_gemm_argument_checks(lib):
+    g = lib.nvfp4_gemm
+    args = lambda **kw: [kw.get("Aq", A16), kw.get("As", A16), A16, kw.get("Bq", A16), A16, A16,
+                         kw.get("M", 128), kw.get("N", 256), kw.get("K", 512), kw.get("Y", A16),
+                         kw.get("ldy", 256), None, 0, None]
+    assert g(*args(K=320)) == N.ERR_UNSUPPORTED_SHAPE
+    assert g(*args(K=0)) == N.ERR_INVALID_ARG
+    assert g(*args(Aq=ODD)) == N.ERR_MISALIGNED
+    assert g(*args(Y=A16 + 1)) == N.ERR_MISALIGNED
+    assert g(*args(ldy=100)) == N.ERR_INVALID_ARG
+    assert g(*args(Bq=None)) == N.ERR_INVALID_ARG
+    assert g(*args(M=-3)) == N.ERR_INVALID_ARG
+
+
+def test_linear_argument_checks(lib):
+    f = lib.nvfp4_linear
+    base = dict(X=A16, M=64, K=512, ldx=512, Wq=A16, Ws=A16, gw=A16, N=128, Y=A16, ldy=128,
+                gx=None, mode=0, ws=A16 * 16, wsb=1 << 30)
+    call = lambda **kw: f(*[{**base, **kw}[k] for k in base], None)
+    assert call(mode=3) == N.ERR_INVALID_ARG
+    assert call(K=448, ldx=448) == N.ERR_UNSUPPORTED_SHAPE
+    assert call(wsb=16) == N.ERR_WORKSPACE_TOO_SMALL
+    assert call(ws=A16 + 16) == N.ERR_MISALIGNED
+    assert call(ws=None) == N.ERR_INVALID_ARG
+    assert call(X=ODD) == N.ERR_MISALIGNED
+    need = lib.nvfp4_linear_workspace_bytes(64, 128, 512, 0)
+    assert need >= 64 * 256 + 512 * 128 // 16
+
+
+def test_python_binding_rejects_packed_fp4_as_bf16():
+    """The "nvfp4-gemma4" page (section 4) reports a crash from packed FP4
+    weights read as bfloat16 with half the columns; the binding refuses
+    such tensors before any launch."""
+    X = torch.zeros(4, 512, dtype=torch.bfloat16)
+    Wq_as_bf16 = torch.zeros(128, 256, dtype=torch.bfloat16)
+    Ws = torch.zeros(128, 32, dtype=torch.uint8)
+    g = torch.ones(1)
+    with pytest.raises(ValueError, match="uint8 packed FP4"):
+        nv.nvfp4_linear(X, Wq_as_bf16, Ws, g)
+    Wq_half_rows = torch.zeros(64, 256, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="shape"):
+        nv.nvfp4_linear(X, Wq_half_rows.view(128, 128), Ws, g)
+    with pytest.raises(ValueError, match="bfloat16"):
+        nv.nvfp4_linear(X.float(), torch.zeros(128, 256, dtype=torch.uint8), Ws, g)
+    with pytest.raises(ValueError, match="scale bytes"):
+        nv.nvfp4_linear(X, torch.zeros(128, 256, dtype=torch.uint8),
+                        torch.zeros(128, 16, dtype=torch.uint8), g)
