@@ -1,0 +1,557 @@
+#!/usr/bin/env python
+"""Benchmark of the NVFP4 linear layer on B300.
+
+One step = one pass of the hot path over one batch of the LLM prefill
+projection (M=4096 tokens, K=5120 -> N=5120, X ~ N(0,1) with 0.1 % outlier
+channels x50, W ~ N(0, 0.02) quantized offline): per-tensor amax of X ->
+global scale, dynamic NVFP4 quantization of X, tcgen05 block-scaled FP4 GEMM
+against the NVFP4 weights, bfloat16 out.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+Prints one JSON line (rank 0). ``value`` is the whole-job TFLOP/s
+(2 M N K per step, summed over ranks, divided by the max-over-ranks time).
+Inputs rotate through enough independent sets that each step reads operands
+that are not L2-resident. The ``reference`` arm times the CPU oracle (test
+infrastructure) on a bounded row sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 linear TFLOPS & % dense-FP4 peak; quantize GB/s & % HBM peak (1 B300)"
+L2_BYTES = 126 * 1024 * 1024
+# dense FP4 peak = measured bf16 peak x the nominal fp4:bf16 ratio (13.5 / 2.25)
+FP4_OVER_BF16 = 13.5 / 2.25
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d["bf16_tflops_sustained"]),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+                "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        self.tmp = tempfile.TemporaryFile(mode="w+")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.seek(0)
+        rows = [r for r in csv.reader(io.StringIO(self.tmp.read())) if len(r) >= 8]
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+                pw.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[4:8]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def physical_gpu_index(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        try:
+            return int(vis.split(",")[local_rank])
+        except (ValueError, IndexError):
+            return local_rank
+    return local_rank
+
+
+# --------------------------------------------------------------- native arm
+
+class Direct:
+    """Pre-marshalled C-ABI calls (ctypes, no per-call Python checks) for
+    the timed loop; argument checks already ran once through the binding."""
+
+    def __init__(self, lib, stream):
+        self.lib = lib
+        self.stream = stream
+
+    def global_scale(self, X, g):
+        return self.lib.nvfp4_global_scale(X.data_ptr(), X.shape[0], X.shape[1], X.stride(0),
+                                           g.data_ptr(), self.stream)
+
+    def quantize(self, X, g, q, sf, layout):
+        return self.lib.nvfp4_quantize(X.data_ptr(), X.shape[0], X.shape[1], X.stride(0),
+                                       g.data_ptr(), q.data_ptr(), sf.data_ptr(), layout,
+                                       self.stream)
+
+    def gemm(self, Aq, As, ga, Bq, Bs, gb, M, N, K, Y):
+        return self.lib.nvfp4_gemm(Aq.data_ptr(), As.data_ptr(), ga.data_ptr(), Bq.data_ptr(),
+                                   Bs.data_ptr(), gb.data_ptr(), M, N, K, Y.data_ptr(),
+                                   Y.stride(0), None, 0, self.stream)
+
+    def linear(self, X, Wq, Ws, gw, Y, gx, mode, ws):
+        M, K = X.shape
+        return self.lib.nvfp4_linear(X.data_ptr(), M, K, X.stride(0), Wq.data_ptr(),
+                                     Ws.data_ptr(), gw.data_ptr(), Wq.shape[0], Y.data_ptr(),
+                                     Y.stride(0), None if gx is None else gx.data_ptr(), mode,
+                                     ws.data_ptr(), ws.numel(), self.stream)
+
+
+def _ok(status, what):
+    if status != 0:
+        raise RuntimeError("%s failed with status %d" % (what, status))
+
+
+def time_region(torch, fn, iters):
+    """Average milliseconds of fn() over iters calls, CUDA events on the
+    current stream."""
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record()
+    for i in range(iters):
+        fn(i)
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / iters
+
+
+def run_native(args):
+    import torch
+    import torch.distributed as dist
+
+    import nvfp4_block_scaled_28_b300 as nv
+    from nvfp4_block_scaled_28_b300 import workloads
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    lib = nv.load_library()
+    stream = torch.cuda.current_stream()
+    D = Direct(lib, stream.cuda_stream)
+    peaks = measured_peaks()
+
+    wl = workloads.WORKLOADS["prefill"]
+    M, K, Nn = wl.M[0], wl.K, wl.N[0]
+    flops = 2.0 * M * Nn * K
+    mode = nv.LINEAR_FUSED if args.mode == "fused" else nv.LINEAR_UNFUSED
+
+    # ---- input sets, rotated so that no step finds its operands in L2
+    set_bytes = (M * K * 2 + Nn * K // 2 + Nn * K // 16 + M * Nn * 2 + M * K // 2 + M * K // 16)
+    n_sets = max(2, math.ceil(3 * L2_BYTES / set_bytes))
+    sets = []
+    for r in range(n_sets):
+        X = workloads.make_x(wl.x_kind, M, K, workloads.x_seed(wl) + 1000 * r + 17 * rank,
+                             device="cuda")
+        W = workloads.make_w(Nn, K, workloads.w_seed(wl) + 1000 * r, device="cuda")
+        Wq, Ws, gw = nv.nvfp4_quantize_weight(W, nv.SF_MMA_128x4)
+        del W
+        gx = torch.empty(1, dtype=torch.float32, device="cuda")
+        Xq = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+        Xs = torch.empty(nv.sf_shape(M, K, nv.SF_MMA_128x4), dtype=torch.uint8, device="cuda")
+        Y = torch.empty((M, Nn), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(nv.linear_workspace_bytes(M, Nn, K, mode), dtype=torch.uint8,
+                         device="cuda")
+        sets.append(dict(X=X, Wq=Wq, Ws=Ws, gw=gw, gx=gx, Xq=Xq, Xs=Xs, Y=Y, ws=ws))
+    # one checked call through the binding before the raw loop
+    nv.nvfp4_linear(sets[0]["X"], sets[0]["Wq"], sets[0]["Ws"], sets[0]["gw"], Y=sets[0]["Y"],
+                    mode=mode)
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+
+    def step(i, timed):
+        s = sets[i % n_sets]
+        _ok(D.global_scale(s["X"], s["gx"]), "global_scale")
+        _ok(D.quantize(s["X"], s["gx"], s["Xq"], s["Xs"], nv.SF_MMA_128x4), "quantize")
+        if timed:
+            ev[i][0].record()
+        _ok(D.gemm(s["Xq"], s["Xs"], s["gx"], s["Wq"], s["Ws"], s["gw"], M, Nn, K, s["Y"]),
+            "gemm")
+        if timed:
+            ev[i][1].record()
+
+    kernels_per_step = 4  # amax, finalize, quantize, gemm (plus one memset)
+    for i in range(args.warmup):
+        step(i, False)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    sampler = ClockSampler(physical_gpu_index(local))
+    sampler.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record()
+    for i in range(args.steps):
+        step(i, True)
+    t1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+    gemm_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    assert nv.nvfp4_device_error() == 0, "a kernel recorded a bounded-wait timeout"
+
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    ms_per_step = elapsed_ms / args.steps
+    value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with host buffers: pinned X in,
+    # Y out, copies inside the timed region
+    s0 = sets[0]
+    Xh = s0["X"].cpu().pin_memory()
+    Yh = torch.empty((M, Nn), dtype=torch.bfloat16).pin_memory()
+    Xd, Yd = torch.empty_like(s0["X"]), s0["Y"]
+    e2e_iters = max(3, min(args.steps, 20))
+
+    def e2e_step(i):
+        Xd.copy_(Xh, non_blocking=True)
+        _ok(D.linear(Xd, s0["Wq"], s0["Ws"], s0["gw"], Yd, None, mode, s0["ws"]), "linear")
+        Yh.copy_(Yd, non_blocking=True)
+
+    e2e_step(0)
+    e2e_ms = time_region(torch, e2e_step, e2e_iters)
+    e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": int(Xh.numel() * 2), "d2h_bytes_per_step": int(Yh.numel() * 2),
+           "ms_per_step": e2e_ms}
+
+    # ---- roofline of the dominant kernel (the GEMM)
+    peak_sust = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
+    peak_burst = peaks["bf16_tflops"] * FP4_OVER_BF16
+    achieved = flops / (gemm_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": "gemm_kernel (tcgen05 kind::mxf4nvf4)",
+                "achieved": achieved, "peak": peak_sust, "unit": "TFLOP/s",
+                "frac": achieved / peak_sust, "frac_of_burst_peak": achieved / peak_burst,
+                "peak_note": "%s bf16 %s x %.0f (fp4:bf16 nominal 13.5:2.25), sustained"
+                             % (peaks["source"], peaks["bf16_tflops_sustained"], FP4_OVER_BF16),
+                "gemm_ms": gemm_ms, "traffic": None}
+
+    rows = {}
+    if not args.no_extras and rank == 0:
+        rows = extra_rows(torch, nv, D, workloads, peaks)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
+        "data": "synthetic (seeded; X ~ N(0,1) with 0.1% outlier channels x50, W ~ N(0,0.02))",
+        "config": {"workload": "LLM prefill projection M=4096 K=5120 N=5120 (NVFP4 linear, "
+                               "dynamic activation global scale)",
+                   "M": M, "N": Nn, "K": K, "mode": args.mode,
+                   "l2": "%d rotating input sets of %.0f MB (> 3x L2)" % (n_sets, set_bytes / 1e6),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": kernels_per_step * args.steps,
+        "clocks": clocks,
+        "rows": rows,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(rows_sample=args.cpu_rows)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def extra_rows(torch, nv, D, workloads, peaks):
+    """Per-row numbers on the other workloads (context, not the headline)."""
+    out = {}
+    hbm = peaks["hbm_gbs"]
+    # a2: standalone activation quantize, 16384 x 16384 (given global scale)
+    sq = workloads.WORKLOADS["square"]
+    X = workloads.make_x(sq.x_kind, sq.M[0], sq.K, workloads.x_seed(sq), device="cuda")
+    g = nv.nvfp4_global_scale(X)
+    q = torch.empty((sq.M[0], sq.K // 2), dtype=torch.uint8, device="cuda")
+    sf = torch.empty((sq.M[0], sq.K // 16), dtype=torch.uint8, device="cuda")
+    ms = time_region(torch, lambda i: _ok(D.quantize(X, g, q, sf, nv.SF_ROW_MAJOR), "q"), 20)
+    nbytes = sq.M[0] * sq.K * 2.5625
+    out["quantize_16384x16384"] = {"ms": ms, "GB/s": nbytes / ms / 1e6,
+                                   "frac_of_hbm": nbytes / ms / 1e6 / hbm}
+    ms = time_region(torch, lambda i: _ok(D.global_scale(X, g), "amax"), 20)
+    out["global_scale_16384x16384"] = {"ms": ms, "GB/s": sq.M[0] * sq.K * 2 / ms / 1e6}
+    # a4: square GEMM 16384^3
+    W = workloads.make_w(sq.N[0], sq.K, workloads.w_seed(sq), device="cuda")
+    Wq, Ws, gw = nv.nvfp4_quantize_weight(W, nv.SF_MMA_128x4)
+    del W
+    Xq, Xs = nv.nvfp4_quantize(X, g, nv.SF_MMA_128x4)
+    del X, q, sf
+    Y = torch.empty((sq.M[0], sq.N[0]), dtype=torch.bfloat16, device="cuda")
+    ms = time_region(torch, lambda i: _ok(D.gemm(Xq, Xs, g, Wq, Ws, gw, sq.M[0], sq.N[0], sq.K, Y),
+                                          "gemm"), 5)
+    fl = 2.0 * sq.M[0] * sq.N[0] * sq.K
+    out["gemm_16384^3"] = {"ms": ms, "TFLOP/s": fl / ms / 1e9}
+    del Xq, Xs, Wq, Ws, Y
+    torch.cuda.empty_cache()
+    # DiT block linears
+    dit = workloads.WORKLOADS["dit"]
+    Xd = workloads.make_x(dit.x_kind, dit.M[0], dit.K, workloads.x_seed(dit), device="cuda")
+    for n in dit.N:
+        W = workloads.make_w(n, dit.K, workloads.w_seed(dit) + n, device="cuda")
+        Wq, Ws, gw = nv.nvfp4_quantize_weight(W, nv.SF_MMA_128x4)
+        Y = torch.empty((dit.M[0], n), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(nv.linear_workspace_bytes(dit.M[0], n, dit.K), dtype=torch.uint8,
+                         device="cuda")
+        ms = time_region(torch, lambda i: _ok(D.linear(Xd, Wq, Ws, gw, Y, None, 0, ws), "lin"), 20)
+        out["dit_linear_4096x3072x%d" % n] = {"ms": ms,
+                                               "TFLOP/s": 2.0 * dit.M[0] * n * dit.K / ms / 1e9}
+    del Xd
+    # a5: decode (weight-bandwidth bound), rotating 3 weight copies (> L2)
+    dec = workloads.WORKLOADS["decode"]
+    n = dec.N[0]
+    wsets = []
+    for r in range(3):
+        W = workloads.make_w(n, dec.K, workloads.w_seed(dec) + r, device="cuda")
+        wsets.append(nv.nvfp4_quantize_weight(W, nv.SF_MMA_128x4))
+        del W
+    wbytes = n * dec.K // 2 + n * dec.K // 16
+    for m in dec.M:
+        Xm = workloads.make_x(dec.x_kind, m, dec.K, workloads.x_seed(dec) + m, device="cuda")
+        Y = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(nv.linear_workspace_bytes(m, n, dec.K), dtype=torch.uint8, device="cuda")
+
+        def f(i, Xm=Xm, Y=Y, ws=ws):
+            Wq, Ws, gw = wsets[i % 3]
+            _ok(D.linear(Xm, Wq, Ws, gw, Y, None, 0, ws), "lin")
+
+        f(0)
+        ms = time_region(torch, f, 30)
+        out["decode_linear_M%d" % m] = {"ms": ms, "weight_GB/s": wbytes / ms / 1e6,
+                                        "frac_of_hbm": wbytes / ms / 1e6 / hbm,
+                                        "TFLOP/s": 2.0 * m * n * dec.K / ms / 1e9}
+    torch.cuda.synchronize()
+    return out
+
+
+# ------------------------------------------------------------ CPU oracle leg
+
+def _oracle_prefill_sample(rows_sample: int):
+    """Quantize W once (offline in the real path), then time the oracle's
+    step on `rows_sample` rows of X: global scale, quantize, GEMM rows."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from nvfp4_block_scaled_28_b300 import workloads
+
+    wl = workloads.WORKLOADS["prefill"]
+    K, Nn = wl.K, wl.N[0]
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    wb = bits(workloads.make_w(Nn, K, workloads.w_seed(wl)))
+    gw = oracle.global_scale(wb)
+    wq, ws = oracle.quantize(wb, gw)
+    xb = bits(workloads.make_x(wl.x_kind, rows_sample, K, workloads.x_seed(wl)))
+
+    def step():
+        gx = oracle.global_scale(xb)
+        xq, xs = oracle.quantize(xb, gx)
+        return oracle.gemm(xq, xs, gx, wq, ws, gw)
+
+    return step, 2.0 * rows_sample * Nn * K
+
+
+def cpu_baseline(rows_sample: int):
+    import oracle
+    oracle.build()
+    step, fl = _oracle_prefill_sample(rows_sample)
+    t = time.perf_counter()
+    step()
+    dt = time.perf_counter() - t
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": "%d of 4096 rows of the prefill workload (global scale + quantize of the "
+                      "sample, FP64 GEMM against all 5120 weight rows)" % rows_sample}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    rows = max(1, min(256, 2048 // max(1, args.steps + args.warmup)))
+    step, fl = _oracle_prefill_sample(rows)
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t
+    value = fl * args.steps / dt / 1e12
+    sample = ("%d of 4096 rows per step of the prefill workload (global scale + quantize of the "
+              "sample, FP64 GEMM against all 5120 weight rows)" % rows)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+        "config": {"workload": "LLM prefill projection M=4096 K=5120 N=5120 (NVFP4 linear, "
+                               "dynamic activation global scale)", "M": 4096, "N": 5120,
+                   "K": 5120},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_single_op(args):
+    """One kernel on one shape, for profiling: --op gemm|quantize|linear
+    --shape M,N,K (quantize uses M,K). Prints the mean CUDA-event time."""
+    import torch
+
+    import nvfp4_block_scaled_28_b300 as nv
+    from nvfp4_block_scaled_28_b300 import workloads
+
+    lib = nv.load_library()
+    D = Direct(lib, torch.cuda.current_stream().cuda_stream)
+    if args.op == "mma_peak":
+        ctas = torch.cuda.get_device_properties(0).multi_processor_count
+        iters = args.iters
+        cyc = torch.zeros(1, dtype=torch.int64, device="cuda")
+        v = args.variant
+        n_mma = {0: 256, 1: 128, 2: 192}[v & 3]
+        fn = lambda i: _ok(lib.nvfp4_mma_peak_probe(ctas, iters, v, cyc.data_ptr(), D.stream),
+                           "peak")
+        for i in range(max(1, args.warmup)):
+            fn(i)
+        sampler = ClockSampler(physical_gpu_index(0))
+        sampler.start()
+        ms = time_region(torch, fn, args.steps)
+        clocks = sampler.stop()
+        k_mma = 16 if (v >> 6) & 1 else 64
+        fl = ctas * iters * 2.0 * 128 * n_mma * k_mma
+        c = int(cyc.item())
+        print(json.dumps({"op": "mma_peak", "variant": v, "N": n_mma, "K": k_mma,
+                          "two_issuers": (v >> 5) & 1,
+                          "accumulators": 1 << ((v >> 2) & 3), "sf_copies": (v >> 4) & 1,
+                          "ctas": ctas, "iters": iters, "ms": ms,
+                          "TFLOP/s": fl / ms / 1e9, "cycles_cta0": c,
+                          "cycles_per_mma": c / iters,
+                          "flop_per_cycle_per_sm": 2.0 * 128 * n_mma * k_mma * iters / c,
+                          "clocks": clocks}))
+        return
+    M, Nn, K = (int(v) for v in args.shape.split(","))
+    X = workloads.make_x("outlier", M, K, 1, device="cuda")
+    g = nv.nvfp4_global_scale(X)
+    if args.op == "quantize":
+        q = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+        sf = torch.empty((M, K // 16), dtype=torch.uint8, device="cuda")
+        fn = lambda i: _ok(D.quantize(X, g, q, sf, nv.SF_ROW_MAJOR), "quantize")
+        work, unit = M * K * 2.5625 / 1e9, "GB"
+    else:
+        W = workloads.make_w(Nn, K, 2, device="cuda")
+        Wq, Ws, gw = nv.nvfp4_quantize_weight(W, nv.SF_MMA_128x4)
+        del W
+        Y = torch.empty((M, Nn), dtype=torch.bfloat16, device="cuda")
+        if args.op == "gemm":
+            Xq, Xs = nv.nvfp4_quantize(X, g, nv.SF_MMA_128x4)
+            fn = lambda i: _ok(D.gemm(Xq, Xs, g, Wq, Ws, gw, M, Nn, K, Y), "gemm")
+        else:
+            mode = nv.LINEAR_FUSED if args.mode == "fused" else nv.LINEAR_UNFUSED
+            ws = torch.empty(nv.linear_workspace_bytes(M, Nn, K, mode), dtype=torch.uint8,
+                             device="cuda")
+            fn = lambda i: _ok(D.linear(X, Wq, Ws, gw, Y, None, mode, ws), "linear")
+        work, unit = 2.0 * M * Nn * K / 1e12, "TFLOP"
+    for i in range(args.warmup):
+        fn(i)
+    ms = time_region(torch, fn, args.steps)
+    assert nv.nvfp4_device_error() == 0
+    print(json.dumps({"op": args.op, "shape": [M, Nn, K], "ms": ms,
+                      "rate": work / (ms * 1e-3), "unit": unit + "/s"}))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--mode", choices=["unfused", "fused"], default="unfused")
+    ap.add_argument("--no-extras", action="store_true", help="skip the per-row extra numbers")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=256)
+    ap.add_argument("--op", choices=["gemm", "quantize", "linear", "mma_peak"], default=None,
+                    help="time a single kernel on --shape instead of the benchmark step")
+    ap.add_argument("--shape", default="8192,8192,8192", help="M,N,K for --op")
+    ap.add_argument("--iters", type=int, default=200000, help="--op mma_peak: MMAs per CTA")
+    ap.add_argument("--variant", type=int, default=0,
+                    help="--op mma_peak: N / accumulator-count / scale-copy variant")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.op is None:
+        ap.error("--warmup must be >= 3")
+    if args.op is not None:
+        run_single_op(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -49,6 +49,7 @@ SIGNATURES = {
                             _SZ, _P]),
     "nvfp4_linear_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
     "nvfp4_device_error": (_INT, [_INT]),
+    "nvfp4_mma_peak_probe": (_INT, [_INT, _INT, _INT, _P, _P]),
     "nvfp4_debug_set_fault_injection": (_INT, [_INT, _U32]),
 }
 

@@ -265,6 +265,24 @@ nvfp4_status nvfp4_device_error(int clear) {
     return (word & kDevErrTimeout) ? NVFP4_ERR_TIMEOUT : NVFP4_OK;
 }
 
+nvfp4_status nvfp4_mma_peak_probe(int ctas, int iters, int variant, unsigned long long *cycles,
+                                  void *stream) {
+    if (ctas <= 0 || iters <= 0 || cycles == nullptr) return NVFP4_ERR_INVALID_ARG;
+    // N (256, 128, 192) times the accumulator count must leave the scale
+    // columns 448..511 free
+    const int n_sel = variant & 3, accs = 1 << ((variant >> 2) & 3);
+    const int N = n_sel == 0 ? 256 : (n_sel == 1 ? 128 : 192);
+    const bool two_issuers = (variant >> 5) & 1;
+    const bool copy_warp = (variant >> 7) & 1;
+    if (variant < 0 || variant > 65535 || n_sel == 3 || ((variant >> 2) & 3) == 3 ||
+        N * accs > 448 || (two_issuers && (N * 2 > 448 || accs != 1)) ||
+        (copy_warp && (two_issuers || ((variant >> 4) & 1))))
+        return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(cycles, 8)) return NVFP4_ERR_MISALIGNED;
+    return from_cuda(launch_mma_peak(ctas, iters, variant, cycles,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
 nvfp4_status nvfp4_debug_set_fault_injection(int mode, uint32_t timeout_us) {
     if (mode != 0 && mode != 1) return NVFP4_ERR_INVALID_ARG;
     debug_state().inject = mode;

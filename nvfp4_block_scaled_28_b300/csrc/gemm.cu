@@ -8,18 +8,25 @@
 // written for Blackwell's fifth-generation tensor cores instead of a library
 // call.
 //
-// Structure of one CTA (one 128 x 256 output tile, K in steps of 256):
-//   warp 0   TMA producer: A/B tiles (128-byte swizzle) by cp.async.bulk.tensor,
-//            scale tiles (already in the 128x4 tile layout) by cp.async.bulk,
-//            into a STAGES-deep ring guarded by full/empty mbarriers;
-//   warp 1   allocates TMEM, then one lane copies each stage's scales
-//            shared->TMEM (tcgen05.cp) and issues 4 tcgen05.mma (K = 64
-//            each) accumulating into a 128 x 256 FP32 TMEM tile;
-//   warps 2-5 epilogue: tcgen05.ld the accumulator (each warp owns its
-//            32-lane TMEM quarter), scale by g_a * g_b, round to bfloat16
-//            and store.
-// Every mbarrier wait is bounded in time; a wait that runs out records a
-// timeout in the device error word and the CTA leaves cleanly.
+// Persistent kernel, one CTA per SM, 128 x 256 output tiles, K in stages of
+// 256 (4 MMAs of K = 64). Warp roles:
+//   warp 0    TMA producer: A/B tiles (128-byte swizzle) by
+//             cp.async.bulk.tensor, scale tiles (already in the 128x4 tile
+//             layout) by cp.async.bulk, into a STAGES-deep ring guarded by
+//             full/empty mbarriers;
+//   warp 1    MMA issuer: per stage, 12 tcgen05.cp copying the stage's scales
+//             shared -> TMEM, then 4 tcgen05.mma into a 128 x 256 FP32
+//             accumulator in TMEM (the copies are issued by the same thread,
+//             so they are ordered before the MMAs without an mbarrier
+//             round trip: measured faster than a separate copy warp);
+//   warp 2    allocates and frees TMEM;
+//   warps 3-10 epilogue, two warps per 32-lane TMEM quarter (one per
+//             128-column half): tcgen05.ld the accumulator into registers,
+//             release it to the MMA warp, then scale by g_a g_b, round to
+//             bfloat16 and store while the next tile's mainloop runs.
+// Every tcgen05 instruction is issued from a converged warp through
+// elect.sync. Every mbarrier wait is bounded in time; a wait that runs out
+// records a timeout in the device error word, and all roles leave cleanly.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -45,8 +52,11 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;            // 256 FP32 columns
 constexpr uint32_t SF_COL = 256;           // per stage: 16 (SFA) + 32 (SFB)
 constexpr uint32_t SF_COLS_PER_STAGE = 48;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kFirstEpiWarp = 3;
+constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);  // 352
 constexpr int GROUP_M = 16;                // tile raster: 16 M-tiles per column sweep
+constexpr unsigned kAll = 0xFFFFFFFFu;
 
 constexpr int SMEM_A = 0;
 constexpr int SMEM_B = SMEM_A + STAGES * A_BYTES;
@@ -56,7 +66,7 @@ constexpr int SMEM_BAR = SMEM_SFB + STAGES * SFB_BYTES;
 constexpr int SMEM_USED = SMEM_BAR + 256;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // room to align the base to 1024
 
-static_assert(STAGES * (SF_COLS_PER_STAGE) + SF_COL <= TMEM_COLS, "TMEM budget");
+static_assert(STAGES * SF_COLS_PER_STAGE + SF_COL <= TMEM_COLS, "TMEM budget");
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 
 struct Params {
@@ -68,6 +78,7 @@ struct Params {
     int64_t ldy;
     int M, N, K;
     int num_m_tiles, num_n_tiles;
+    int num_ctiles;      // cluster tiles: CM consecutive M-tiles sharing one N-tile
     int y_vec;           // rows of Y start 16-byte aligned: 16-byte stores
     int inject;          // 1: the producer issues nothing (bounded-wait test)
     uint64_t timeout_ns;
@@ -75,18 +86,22 @@ struct Params {
 };
 
 struct Shared {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
-    uint64_t acc_full;
+    uint64_t full[STAGES];     // TMA -> MMA: stage (A, B, scales) landed
+    uint64_t empty[STAGES];    // MMA -> TMA: stage consumed
+    uint64_t acc_full;         // MMA -> epilogue: accumulator complete
+    uint64_t acc_empty;        // epilogue -> MMA: accumulator drained
+    uint64_t drain_mma;        // teardown after an abort: MMAs issued have completed
     uint32_t tmem_base;
     volatile uint32_t abort_flag;
 };
+static_assert(sizeof(Shared) <= 256, "barrier area");
 
-__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int &mt, int &nt) {
-    const int per_group = GROUP_M * num_n;
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group_m, int &mt,
+                                            int &nt) {
+    const int per_group = group_m * num_n;
     const int group = t / per_group;
-    const int first_m = group * GROUP_M;
-    const int gsz = min(num_m - first_m, GROUP_M);
+    const int first_m = group * group_m;
+    const int gsz = min(num_m - first_m, group_m);
     const int local = t - group * per_group;
     mt = first_m + local % gsz;
     nt = local / gsz;
@@ -97,6 +112,46 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Bounded wait by lane 0 of a converged warp, also giving up once another
+// role has aborted; the verdict is broadcast to the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const Params &p,
+                                          Shared &sh) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        const uint32_t a = smem_addr(bar);
+        if (!mbar_try_wait(a, parity)) {
+            const uint64_t t0 = global_timer_ns();
+            while (true) {
+                if (mbar_try_wait(a, parity)) break;
+                if (sh.abort_flag) {
+                    ok = 0;
+                    break;
+                }
+                if (global_timer_ns() - t0 > p.timeout_ns) {
+                    record_timeout(p.err);
+                    sh.abort_flag = 1;
+                    ok = 0;
+                    break;
+                }
+            }
+        }
+    }
+    return __shfl_sync(kAll, ok, 0) != 0;
+}
+
+// M-tile of this CTA in cluster tile `ct` (CTA `rank` of a cluster of CM).
+template <int CM>
+__device__ __forceinline__ void cta_tile(int ct, int rank, const Params &p, int &mt, int &nt) {
+    const int num_cm = (p.num_m_tiles + CM - 1) / CM;
+    int cm;
+    tile_coords(ct, num_cm, p.num_n_tiles, GROUP_M / CM, cm, nt);
+    mt = cm * CM + rank;
+}
+
+// CM > 1: the CM CTAs of a cluster work on CM consecutive M-tiles of the same
+// N-tile in lockstep; each loads 1/CM of the shared B tile (and of its
+// scales) and multicasts it to all, so B is read from L2 once per cluster.
+template <int CM>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const Params p) {
@@ -107,176 +162,221 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    int mt, nt;
-    tile_coords(blockIdx.x, p.num_m_tiles, p.num_n_tiles, mt, nt);
-    const int m0 = mt * BM, n0 = nt * BN;
     const int num_k = p.K / BK;
     const int kb4 = p.K / 64;  // 512-byte scale tiles per 128-row group
     const int n_sf_groups = (p.N + 127) / 128;
+    const int rank = CM > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int cluster_id = blockIdx.x / CM;
+    const int num_clusters = gridDim.x / CM;
+    constexpr uint16_t kMask = static_cast<uint16_t>((1u << CM) - 1u);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&sh.full[s], 1);
-            mbar_init(&sh.empty[s], 1);
+            mbar_init(&sh.empty[s], CM);  // one release per CTA of the cluster
         }
         mbar_init(&sh.acc_full, 1);
+        mbar_init(&sh.acc_empty, kEpiWarps);
+        mbar_init(&sh.drain_mma, 1);
         sh.abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
-    if (warp == 1) {
+    if (warp == 2) {
         tmem_alloc(&sh.tmem_base, TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
+    if (CM > 1) cluster_sync_all();  // peers' barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
 
-    // Roles run warp-wide loops in which lane 0 waits and issues; the other
-    // lanes follow through __shfl_sync, so every warp reaches the final
-    // barrier and the .sync.aligned tcgen05 instructions converged.
-    constexpr unsigned kAll = 0xFFFFFFFFu;
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
         const uint64_t pol = policy_evict_last();
-        const bool two_groups = (nt * 2 + 1) < n_sf_groups;
-        const uint32_t tx = A_BYTES + B_BYTES + SFA_BYTES + (two_groups ? 2 : 1) * (SFB_BYTES / 2);
-        int issued_total = 0;
-        bool ok = true;
-        for (int kt = 0; kt < num_k && !p.inject; ++kt) {
-            const int s = kt % STAGES;
-            const uint32_t ph = (kt / STAGES) & 1;
-            int go = 1;
-            if (lane == 0) {
-                if (!mbar_wait(&sh.empty[s], ph ^ 1, p.timeout_ns)) {
-                    record_timeout(p.err);
-                    sh.abort_flag = 1;
-                    go = 0;
-                } else if (sh.abort_flag) {
-                    go = 0;
-                } else {
-                    mbar_arrive_expect_tx(&sh.full[s], tx);
-                    tma_load_2d(smem + SMEM_A + s * A_BYTES, &tmA, &sh.full[s], kt * (BK / 2), m0,
-                                pol);
-                    tma_load_2d(smem + SMEM_B + s * B_BYTES, &tmB, &sh.full[s], kt * (BK / 2), n0,
-                                pol);
-                    const uint8_t *sa = p.As + (static_cast<int64_t>(mt) * kb4 + kt * 4) * SF_TILE;
-                    bulk_load(smem + SMEM_SFA + s * SFA_BYTES, sa, SFA_BYTES, &sh.full[s], pol);
-                    const uint8_t *sb =
-                        p.Bs + (static_cast<int64_t>(nt * 2) * kb4 + kt * 4) * SF_TILE;
-                    bulk_load(smem + SMEM_SFB + s * SFB_BYTES, sb, SFB_BYTES / 2, &sh.full[s], pol);
-                    if (two_groups)
-                        bulk_load(smem + SMEM_SFB + s * SFB_BYTES + SFB_BYTES / 2,
-                                  sb + static_cast<int64_t>(kb4) * SF_TILE, SFB_BYTES / 2,
-                                  &sh.full[s], pol);
+        int g = 0;  // stage counter over this CTA's tiles
+        bool ok = !p.inject;
+        for (int ct = cluster_id; ok && ct < p.num_ctiles; ct += num_clusters) {
+            int mt, nt;
+            cta_tile<CM>(ct, rank, p, mt, nt);
+            const bool mt_valid = mt < p.num_m_tiles;  // a cluster's tail tile may be empty
+            const bool two_groups = (nt * 2 + 1) < n_sf_groups;
+            const uint32_t tx = A_BYTES + B_BYTES + (mt_valid ? SFA_BYTES : 0) +
+                                (two_groups ? 2 : 1) * (SFB_BYTES / 2);
+            for (int kt = 0; kt < num_k; ++kt, ++g) {
+                const int s = g % STAGES;
+                if (!warp_wait(&sh.empty[s], ((g / STAGES) & 1) ^ 1, p, sh)) {
+                    ok = false;
+                    break;
                 }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&sh.full[s], tx);
+                    tma_load_2d(smem + SMEM_A + s * A_BYTES, &tmA, &sh.full[s], kt * (BK / 2),
+                                mt * BM, pol);
+                    uint8_t *bdst = smem + SMEM_B + s * B_BYTES + rank * (B_BYTES / CM);
+                    if (CM == 1)
+                        tma_load_2d(bdst, &tmB, &sh.full[s], kt * (BK / 2), nt * BN, pol);
+                    else
+                        tma_load_2d_mc(bdst, &tmB, &sh.full[s], kt * (BK / 2),
+                                       nt * BN + rank * (BN / CM), kMask, pol);
+                    if (mt_valid) {
+                        const uint8_t *sa =
+                            p.As + (static_cast<int64_t>(mt) * kb4 + kt * 4) * SF_TILE;
+                        bulk_load(smem + SMEM_SFA + s * SFA_BYTES, sa, SFA_BYTES, &sh.full[s], pol);
+                    }
+                    // B scales: two 128-row groups of 2 KiB; CTA `rank` loads
+                    // bytes [rank * 4K / CM, +4K / CM) of the pair
+                    constexpr int piece = SFB_BYTES / CM;
+                    const int grp = (rank * piece) / (SFB_BYTES / 2);
+                    const int off = (rank * piece) % (SFB_BYTES / 2);
+                    if (grp == 0 || two_groups) {
+                        const uint8_t *sb =
+                            p.Bs + (static_cast<int64_t>(nt * 2 + grp) * kb4 + kt * 4) * SF_TILE +
+                            off;
+                        uint8_t *sdst = smem + SMEM_SFB + s * SFB_BYTES + rank * piece;
+                        if (CM == 1) {
+                            bulk_load(sdst, sb, SFB_BYTES / 2, &sh.full[s], pol);
+                            if (two_groups)
+                                bulk_load(sdst + SFB_BYTES / 2,
+                                          sb + static_cast<int64_t>(kb4) * SF_TILE,
+                                          SFB_BYTES / 2, &sh.full[s], pol);
+                        } else {
+                            bulk_load_mc(sdst, sb, piece, &sh.full[s], kMask, pol);
+                        }
+                    }
+                }
+                __syncwarp();
             }
-            go = __shfl_sync(kAll, go, 0);
-            if (!go) {
-                ok = false;
-                break;
-            }
-            ++issued_total;
         }
-        if (!ok && lane == 0) {
-            // let the copies already issued land before the CTA exits: the
-            // last fill of stage s completes phase (fills_of_s - 1)
-            for (int s = 0; s < STAGES && s < issued_total; ++s) {
-                const int fills = (issued_total - s + STAGES - 1) / STAGES;
+        if (!ok && !p.inject && lane == 0) {
+            // let copies already issued land before the CTA exits: the last
+            // fill of stage s completes that stage's phase (fills - 1)
+            for (int s = 0; s < STAGES && s < g; ++s) {
+                const int fills = (g - s + STAGES - 1) / STAGES;
                 mbar_wait(&sh.full[s], (fills - 1) & 1, p.timeout_ns);
+            }
+        }
+        if (CM > 1 && lane == 0 && !p.inject) {
+            // every CTA of the cluster releases every stage to every CTA:
+            // wait until the last releases addressed to this CTA have
+            // landed, so none arrives after it exits
+            for (int s = 0; s < STAGES && s < g; ++s) {
+                const int fills = (g - s + STAGES - 1) / STAGES;
+                mbar_wait(&sh.empty[s], (fills - 1) & 1, p.timeout_ns);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         constexpr uint32_t idesc = idesc_mxf4nvf4(BM, BN);
-        for (int kt = 0; kt < num_k; ++kt) {
-            const int s = kt % STAGES;
-            const uint32_t ph = (kt / STAGES) & 1;
-            int go = 1;
-            if (lane == 0) {
-                if (!mbar_wait(&sh.full[s], ph, p.timeout_ns)) {
-                    record_timeout(p.err);
-                    sh.abort_flag = 1;
-                    go = 0;
-                } else {
-                    tc_fence_after();
-                    const uint32_t sf_a = tmem + SF_COL + s * SF_COLS_PER_STAGE;
-                    const uint32_t sf_b = sf_a + 16;
-                    const uint32_t sfa_smem = smem_addr(smem + SMEM_SFA + s * SFA_BYTES);
-                    const uint32_t sfb_smem = smem_addr(smem + SMEM_SFB + s * SFB_BYTES);
-#pragma unroll
-                    for (int j = 0; j < MMAS_PER_STAGE; ++j) {
-                        tmem_cp_32x128b_x4(sf_a + j * 4, sdesc_sf(sfa_smem + j * SF_TILE));
-                        tmem_cp_32x128b_x4(sf_b + j * 8, sdesc_sf(sfb_smem + j * SF_TILE));
-                        tmem_cp_32x128b_x4(sf_b + j * 8 + 4,
-                                           sdesc_sf(sfb_smem + SFB_BYTES / 2 + j * SF_TILE));
-                    }
-                    const uint32_t a_smem = smem_addr(smem + SMEM_A + s * A_BYTES);
-                    const uint32_t b_smem = smem_addr(smem + SMEM_B + s * B_BYTES);
-#pragma unroll
-                    for (int j = 0; j < MMAS_PER_STAGE; ++j)
-                        mma_mxf4nvf4(tmem + ACC_COL, sdesc_sw128(a_smem + j * 32),
-                                     sdesc_sw128(b_smem + j * 32), idesc, sf_a + j * 4,
-                                     sf_b + j * 8, (kt | j) != 0);
-                    tc_commit(&sh.empty[s]);
-                }
+        int g = 0, it = 0;
+        bool ok = true;
+        for (int ct = cluster_id; ok && ct < p.num_ctiles; ct += num_clusters, ++it) {
+            if (!warp_wait(&sh.acc_empty, (it & 1) ^ 1, p, sh)) {
+                ok = false;
+                break;
             }
-            go = __shfl_sync(kAll, go, 0);
-            if (!go) break;
+            tc_fence_after();
+            for (int kt = 0; kt < num_k; ++kt, ++g) {
+                const int s = g % STAGES;
+                if (!warp_wait(&sh.full[s], (g / STAGES) & 1, p, sh)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // scales shared -> TMEM, issued in order ahead of the MMAs that
+                // read them (same-thread tcgen05.cp -> tcgen05.mma is ordered)
+                const uint32_t sf_a = tmem + SF_COL + s * SF_COLS_PER_STAGE;
+                const uint32_t sf_b = sf_a + 16;
+                const uint32_t sfa_smem = smem_addr(smem + SMEM_SFA + s * SFA_BYTES);
+                const uint32_t sfb_smem = smem_addr(smem + SMEM_SFB + s * SFB_BYTES);
+#pragma unroll
+                for (int j = 0; j < MMAS_PER_STAGE; ++j) {
+                    tmem_cp_32x128b_x4_elect(sf_a + j * 4, sdesc_sf(sfa_smem + j * SF_TILE));
+                    tmem_cp_32x128b_x4_elect(sf_b + j * 8, sdesc_sf(sfb_smem + j * SF_TILE));
+                    tmem_cp_32x128b_x4_elect(sf_b + j * 8 + 4,
+                                             sdesc_sf(sfb_smem + SFB_BYTES / 2 + j * SF_TILE));
+                }
+                const uint32_t a_smem = smem_addr(smem + SMEM_A + s * A_BYTES);
+                const uint32_t b_smem = smem_addr(smem + SMEM_B + s * B_BYTES);
+#pragma unroll
+                for (int j = 0; j < MMAS_PER_STAGE; ++j)
+                    mma_mxf4nvf4_elect(tmem + ACC_COL, sdesc_sw128(a_smem + j * 32),
+                                       sdesc_sw128(b_smem + j * 32), idesc, sf_a + j * 4,
+                                       sf_b + j * 8, (kt | j) != 0);
+                if (CM == 1)
+                    tc_commit_elect(&sh.empty[s]);
+                else
+                    tc_commit_mc_elect(&sh.empty[s], kMask);
+            }
+            if (ok) tc_commit_elect(&sh.acc_full);
         }
-        if (lane == 0) {
-            __threadfence_block();
-            tc_commit(&sh.acc_full);  // arrives once every MMA issued above has completed
+        if (!ok) {
+            // MMAs already issued must complete before TMEM is released
+            tc_commit_elect(&sh.drain_mma);
+            if (lane == 0) mbar_wait(&sh.drain_mma, 0, p.timeout_ns);
         }
         __syncwarp();
+    } else if (warp == 2) {
+        // TMEM allocator only
     } else {
         // -------------------------------------------------------- epilogue
         const int quarter = warp & 3;
-        int ok = mbar_wait(&sh.acc_full, 0, p.timeout_ns) ? 1 : 0;
-        ok = __all_sync(kAll, ok);
-        if (!ok && lane == 0) record_timeout(p.err);
-        tc_fence_after();
-        ok = __shfl_sync(kAll, ok && !sh.abort_flag, 0);
-        if (ok) {
-            const float alpha = __fmul_rn(*p.g_a, *p.g_b);
-            const int row = m0 + quarter * 32 + lane;
-            const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + ACC_COL;
-            uint16_t *yrow = p.Y + static_cast<int64_t>(row) * p.ldy;
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+        const int half = (warp - kFirstEpiWarp) >> 2;  // which 128 columns
+        const float alpha = __fmul_rn(*p.g_a, *p.g_b);
+        int it = 0;
+        for (int ct = cluster_id; ct < p.num_ctiles; ct += num_clusters, ++it) {
+            if (!warp_wait(&sh.acc_full, it & 1, p, sh)) break;
+            tc_fence_after();
+            int mt, nt;
+            cta_tile<CM>(ct, rank, p, mt, nt);
+            const uint32_t t_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + ACC_COL +
+                                    static_cast<uint32_t>(half * 128);
+            uint32_t packed[64];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
                 uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + c * 32, r);
+                tmem_ld_32x32b_x32(t_base + c * 32, r);
                 tmem_ld_wait();
-                const int n = n0 + c * 32;
-                if (row < p.M && n < p.N) {
-                    uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    packed[c * 16 + i] = pack_bf16x2(__uint_as_float(r[2 * i]) * alpha,
+                                                     __uint_as_float(r[2 * i + 1]) * alpha);
+            }
+            // accumulator drained into registers: hand it back to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.acc_empty);
+
+            const int row = mt * BM + quarter * 32 + lane;
+            const int n0 = nt * BN + half * 128;
+            if (row < p.M) {
+                uint16_t *yrow = p.Y + static_cast<int64_t>(row) * p.ldy;
+                if (p.y_vec && n0 + 128 <= p.N) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(yrow + n0);
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        packed[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * alpha,
-                                                __uint_as_float(r[2 * i + 1]) * alpha);
-                    if (n + 32 <= p.N && p.y_vec) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(yrow + n);
+                        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                            packed[4 * i + 3]);
+                } else {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                                packed[4 * i + 3]);
-                    } else {
-                        for (int i = 0; i < 32 && n + i < p.N; ++i)
-                            yrow[n + i] = static_cast<uint16_t>(
-                                (packed[i >> 1] >> ((i & 1) * 16)) & 0xFFFFu);
+                    for (int i = 0; i < 64; ++i) {
+                        const int n = n0 + 2 * i;
+                        if (n < p.N) yrow[n] = static_cast<uint16_t>(packed[i] & 0xFFFFu);
+                        if (n + 1 < p.N) yrow[n + 1] = static_cast<uint16_t>(packed[i] >> 16);
                     }
                 }
-                __syncwarp();
             }
         }
+        __syncwarp();
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (CM > 1) cluster_sync_all();  // no CTA leaves while a peer may still address it
+    if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
@@ -321,20 +421,68 @@ bool make_operand_map(CUtensorMap *map, const uint8_t *ptr, int64_t rows, int64_
     return r == CUDA_SUCCESS;
 }
 
+template <int CM>
+cudaError_t launch_cm(const CUtensorMap &tmA, const CUtensorMap &tmB, Params p, cudaStream_t st) {
+    static int max_clusters = -1;
+    if (max_clusters < 0) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<CM>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
+        max_clusters = launch_cfg().num_sms / CM;
+        if (CM > 1) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = CM;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(CM * max_clusters, 1, 1);
+            cfg.blockDim = dim3(kThreads, 1, 1);
+            cfg.dynamicSmemBytes = SMEM_ALLOC;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<CM>, &cfg) == cudaSuccess && n > 0 &&
+                n < max_clusters)
+                max_clusters = n;
+        }
+    }
+    p.num_ctiles = ((p.num_m_tiles + CM - 1) / CM) * p.num_n_tiles;
+    const int clusters = p.num_ctiles < max_clusters ? p.num_ctiles : max_clusters;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CM;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(CM * clusters, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_ALLOC;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<CM>, tmA, tmB, p);
+}
+
+int cluster_m() {
+    static int cm = 0;
+    if (cm == 0) {
+        cm = 1;
+        const char *env = getenv("NVFP4_GEMM_CLUSTER_M");  // tuning knob: 1, 2 or 4
+        if (env && (env[0] == '1' || env[0] == '2' || env[0] == '4') && env[1] == 0)
+            cm = env[0] - '0';
+    }
+    return cm;
+}
+
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e =
-            cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    const int CM = cluster_m();
     CUtensorMap tmA, tmB;
     if (!make_operand_map(&tmA, a.Aq, a.M, a.K, BM)) return cudaErrorInvalidValue;
-    if (!make_operand_map(&tmB, a.Bq, a.N, a.K, BN)) return cudaErrorInvalidValue;
+    if (!make_operand_map(&tmB, a.Bq, a.N, a.K, BN / CM)) return cudaErrorInvalidValue;
     Params p;
     p.As = a.As;
     p.Bs = a.Bs;
@@ -347,13 +495,20 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st) {
     p.K = static_cast<int>(a.K);
     p.num_m_tiles = static_cast<int>((a.M + BM - 1) / BM);
     p.num_n_tiles = static_cast<int>((a.N + BN - 1) / BN);
+    p.num_ctiles = 0;
     p.y_vec = (a.ldy % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.Y) & 15) == 0);
     p.inject = debug_state().inject;
     p.timeout_ns = debug_state().timeout_ns;
     p.err = device_error_word();
     if (p.err == nullptr) return cudaErrorInvalidSymbol;
-    const int tiles = p.num_m_tiles * p.num_n_tiles;
-    gemm_kernel<<<tiles, kThreads, SMEM_ALLOC, st>>>(tmA, tmB, p);
+    cudaError_t e;
+    if (CM == 4)
+        e = launch_cm<4>(tmA, tmB, p, st);
+    else if (CM == 2)
+        e = launch_cm<2>(tmA, tmB, p, st);
+    else
+        e = launch_cm<1>(tmA, tmB, p, st);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

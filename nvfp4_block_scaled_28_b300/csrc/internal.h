@@ -57,6 +57,9 @@ struct GemmArgs {
 
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st);
 
+cudaError_t launch_mma_peak(int ctas, int iters, int variant, unsigned long long *cycles,
+                            cudaStream_t st);
+
 // Device address of the library's error word on the current device.
 unsigned int *device_error_word();
 

@@ -64,25 +64,28 @@ def w_seed(w: Workload) -> int:
     return 4321 + w.index
 
 
-def make_x(kind: str, M: int, K: int, seed: int) -> torch.Tensor:
-    """Activation tensor (M, K) bfloat16 on the CPU."""
-    g = torch.Generator(device="cpu").manual_seed(seed)
-    x = torch.randn((M, K), generator=g, dtype=torch.float32)
+def make_x(kind: str, M: int, K: int, seed: int, device: str = "cpu") -> torch.Tensor:
+    """Activation tensor (M, K) bfloat16. The CPU generator (the default) is
+    what parity tests use; ``device="cuda"`` draws the same distribution
+    with the device generator (different values), for large benchmark
+    inputs."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    x = torch.randn((M, K), generator=g, dtype=torch.float32, device=device)
     if kind == "outlier":
         n_out = int(round(0.001 * K))
         if n_out:
-            cols = torch.randperm(K, generator=g)[:n_out]
+            cols = torch.randperm(K, generator=g, device=device)[:n_out]
             x[:, cols] *= 50.0
     elif kind == "token_scaled":
-        scale = torch.rand((M, 1), generator=g, dtype=torch.float32) * 3.5 + 0.5
+        scale = torch.rand((M, 1), generator=g, dtype=torch.float32, device=device) * 3.5 + 0.5
         x *= scale
     elif kind != "normal":
         raise ValueError("unknown activation kind %r" % kind)
     return x.to(torch.bfloat16)
 
 
-def make_w(N: int, K: int, seed: int, std: float = 0.02) -> torch.Tensor:
-    """Weight tensor (N, K) bfloat16 on the CPU."""
-    g = torch.Generator(device="cpu").manual_seed(seed)
-    w = torch.randn((N, K), generator=g, dtype=torch.float32) * std
+def make_w(N: int, K: int, seed: int, std: float = 0.02, device: str = "cpu") -> torch.Tensor:
+    """Weight tensor (N, K) bfloat16 (CPU generator by default)."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    w = torch.randn((N, K), generator=g, dtype=torch.float32, device=device) * std
     return w.to(torch.bfloat16)
