@@ -194,6 +194,36 @@ NVFP4_API nvfp4_status nvfp4_linear(const void *X, int64_t M, int64_t K, int64_t
 NVFP4_API size_t nvfp4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int mode);
 
 /*
+ * nvfp4_linear for callers that cannot allocate device memory. The pages
+ * have no counterpart: this is a deployment variant of nvfp4_linear.
+ *
+ * nvfp4_linear needs a caller-allocated workspace. Some callers have no way
+ * to provide one: a plugin inside a host application that owns the device
+ * memory pool and forbids outside allocations, a serving loop that reserves
+ * all of its memory up front so no request can fail on an allocation, or a
+ * C caller with no device allocator. This variant keeps the workspace in a
+ * fixed 16 MiB array inside the library (held on every GPU that loads the
+ * library until the process exits) and calls no cudaMalloc, cudaFree or
+ * allocating library routine. The caller still passes X, the weights and Y.
+ *
+ * Same arguments, layout rules and result as nvfp4_linear with
+ * mode = NVFP4_LINEAR_UNFUSED, minus the workspace. Limit:
+ * nvfp4_linear_workspace_bytes(M, N, K, NVFP4_LINEAR_UNFUSED) must not
+ * exceed 16 MiB (about M * K / 2 * 1.125 bytes; 4096 x 5120 fits), else
+ * NVFP4_ERR_WORKSPACE_TOO_SMALL and nothing is launched.
+ * The first call on each device looks the array's device address up
+ * (cudaGetSymbolAddress) while that device is current; make that first call
+ * before any stream capture begins. Every call shares the one array and it
+ * keeps the previous call's contents: calls whose work overlaps on the GPU
+ * (different streams, or different host threads without ordering) race on
+ * it, so serialize them.
+ */
+NVFP4_API nvfp4_status nvfp4_linear_noalloc(const void *X, int64_t M, int64_t K, int64_t ldx,
+                                           const uint8_t *Wq, const uint8_t *Ws,
+                                           const float *g_w, int64_t N, void *Y, int64_t ldy,
+                                           const float *g_x, void *stream);
+
+/*
  * Synchronize the current device, then return NVFP4_ERR_TIMEOUT if any
  * kernel of this library recorded a bounded-wait timeout since the last
  * clear, NVFP4_ERR_CUDA if the synchronization failed, else NVFP4_OK.

@@ -20,6 +20,7 @@ from .ops import (  # noqa: F401
     nvfp4_sf_to_mma_layout,
     nvfp4_gemm,
     nvfp4_linear,
+    nvfp4_linear_noalloc,
     gemm_workspace_bytes,
     linear_workspace_bytes,
     nvfp4_device_error,

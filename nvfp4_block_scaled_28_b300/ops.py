@@ -199,6 +199,32 @@ def nvfp4_linear(X: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, g_w: torch
     return Y
 
 
+def nvfp4_linear_noalloc(X: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor,
+                         g_w: torch.Tensor, g_x: torch.Tensor | None = None,
+                         Y: torch.Tensor | None = None) -> torch.Tensor:
+    """nvfp4_linear without a caller-provided workspace: the library keeps
+    the scratch in a fixed 16 MiB device array of its own, for callers that
+    cannot allocate device memory. Calls that overlap on the GPU race on
+    that array."""
+    _check_bf16_2d(X, "X")
+    M, K = X.shape
+    Nn = Wq.shape[0]
+    _check_codes(Wq, Nn, K, "Wq")
+    _check_scales(Ws, Nn, K, SF_MMA_128x4, "Ws")
+    _check_g(g_w, "g_w")
+    if g_x is not None:
+        _check_g(g_x, "g_x")
+    _check_cuda(X, Wq, Ws, g_w, g_x, Y)
+    if Y is None:
+        Y = torch.empty((M, Nn), dtype=torch.bfloat16, device=X.device)
+    _check_bf16_2d(Y, "Y")
+    _require(tuple(Y.shape) == (M, Nn), "Y must have shape (%d, %d)" % (M, Nn))
+    N.check("nvfp4_linear_noalloc", N.load().nvfp4_linear_noalloc(
+        _ptr(X), M, K, X.stride(0), _ptr(Wq), _ptr(Ws), _ptr(g_w), Nn, _ptr(Y), Y.stride(0),
+        _ptr(g_x), _stream()))
+    return Y
+
+
 def nvfp4_device_error(clear: bool = True) -> int:
     """Synchronize and return the device-side status (OK or ERR_TIMEOUT)."""
     return int(N.load().nvfp4_device_error(1 if clear else 0))
