@@ -39,6 +39,28 @@ L2_BYTES = 126 * 1024 * 1024
 FP4_OVER_BF16 = 13.5 / 2.25
 
 
+def gemm_traffic_per_launch():
+    """DRAM bytes per GEMM launch of the benchmark step from the committed
+    ncu capture, valid only while the kernel source is the one captured."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "gemm_prefill_traffic.json")) as f:
+            rec = json.load(f)
+        h = hashlib.sha256()
+        for name in ("gemm.cu", "ptx.cuh"):
+            with open(os.path.join(ROOT, "nvfp4_block_scaled_28_b300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() == rec["source_sha256"]:
+            return float(rec["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
+# Dense FP4 rate measured by the library's tcgen05 probe (profiles/mma_peak_probe.md)
+FP4_PROBE_PEAK_TFLOPS = 9230.0
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -288,7 +310,9 @@ def run_native(args):
                 "frac": achieved / peak_sust, "frac_of_burst_peak": achieved / peak_burst,
                 "peak_note": "%s bf16 %s x %.0f (fp4:bf16 nominal 13.5:2.25), sustained"
                              % (peaks["source"], peaks["bf16_tflops_sustained"], FP4_OVER_BF16),
-                "gemm_ms": gemm_ms, "traffic": None}
+                "frac_of_probe_peak": achieved / FP4_PROBE_PEAK_TFLOPS,
+                "gemm_ms": gemm_ms, "traffic": gemm_traffic_per_launch(),
+                "traffic_unit": "bytes per launch (ncu dram read + write)"}
 
     rows = {}
     if not args.no_extras and rank == 0:
