@@ -146,6 +146,9 @@ NVFP4_API nvfp4_status nvfp4_sf_to_mma_layout(const uint8_t *sf_row_major, int64
  * Y: M x N bfloat16, leading dimension ldy >= N (rows that start 16-byte
  * aligned, i.e. 16-byte aligned Y and ldy % 8 == 0, get 16-byte stores).
  * K % 256 == 0; M, N >= 0 (0 is a no-op).
+ * M <= 128 (decode) runs a weight-streaming kernel that computes Y^T = W X^T
+ * with the weights as the 128-row MMA operand; larger M runs the 128 x 256
+ * tile kernel.
  * workspace / workspace_bytes: scratch for the skinny-M split-K path; query
  * nvfp4_gemm_workspace_bytes(). May be NULL when that returns 0.
  * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_SHAPE,
@@ -163,8 +166,11 @@ NVFP4_API size_t nvfp4_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 typedef enum nvfp4_linear_mode {
     /* nvfp4_quantize into the workspace, then nvfp4_gemm. */
     NVFP4_LINEAR_UNFUSED = 0,
-    /* The GEMM's producer warps quantize bfloat16 X tiles straight into
-     * shared memory (same arithmetic, bit-identical output). */
+    /* For M <= 32 the GEMM quantizes bfloat16 X tiles in shared memory
+     * inside the kernel (same arithmetic, bit-identical output), so X's
+     * codes never travel through HBM. For M > 32 every N-tile would have to
+     * re-quantize the same rows, which costs more than one quantize pass,
+     * so this mode runs the unfused sequence. */
     NVFP4_LINEAR_FUSED = 1
 } nvfp4_linear_mode;
 

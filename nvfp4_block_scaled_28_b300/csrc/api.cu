@@ -202,14 +202,23 @@ nvfp4_status nvfp4_gemm(const uint8_t *Aq, const uint8_t *As, const float *g_a, 
         return NVFP4_ERR_WORKSPACE_TOO_SMALL;
     (void)workspace;
     if (M == 0 || N == 0) return NVFP4_OK;
+    if (M <= kSkinnyMaxM) {
+        // few activation rows: weights as the 128-row MMA operand
+        SkinnyArgs sa{Bq, Bs, g_b, Aq, As, nullptr, 0, g_a, M, N, K,
+                      static_cast<uint16_t *>(Y), ldy, 0};
+        return from_cuda(launch_gemm_skinny(sa, static_cast<cudaStream_t>(stream)));
+    }
     GemmArgs a{Aq, As, g_a, Bq, Bs, g_b, M, N, K, static_cast<uint16_t *>(Y), ldy};
     return from_cuda(launch_gemm(a, static_cast<cudaStream_t>(stream)));
 }
 
+// nvfp4_linear workspace: [g_x | amax partials] header, X codes, X scales.
+constexpr size_t kLinearHeader = 256 + sizeof(uint32_t) * kMaxAmaxPartials;
+
 size_t nvfp4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int mode) {
     if (M < 0 || N < 0 || K < 0 || K % 256 != 0) return 0;
     (void)mode;
-    size_t bytes = 256;  // g_x
+    size_t bytes = kLinearHeader;  // g_x and the amax partials
     bytes += round_up(static_cast<size_t>(M) * static_cast<size_t>(K / 2), 256);
     bytes += round_up(nvfp4_sf_bytes(M, K, NVFP4_SF_MMA_128x4), 256);
     bytes += nvfp4_gemm_workspace_bytes(M, N, K);
@@ -236,18 +245,34 @@ nvfp4_status nvfp4_linear(const void *X, int64_t M, int64_t K, int64_t ldx, cons
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     float *gx_slot = reinterpret_cast<float *>(ws);
-    uint8_t *xq = ws + 256;
+    uint32_t *partials = reinterpret_cast<uint32_t *>(ws + 256);
+    uint8_t *xq = ws + kLinearHeader;
     uint8_t *xs = xq + round_up(static_cast<size_t>(M) * static_cast<size_t>(K / 2), 256);
     const uint16_t *Xh = static_cast<const uint16_t *>(X);
+    if (mode == NVFP4_LINEAR_FUSED && M <= kSkinnyFusedMaxM) {
+        // one launch: the GEMM computes g_x (when not given) and quantizes X
+        // tiles in shared memory; no codes in HBM
+        SkinnyArgs sa{Wq, Ws, g_w, nullptr, nullptr, Xh, ldx, g_x, M, N, K,
+                      static_cast<uint16_t *>(Y), ldy, 1};
+        return from_cuda(launch_gemm_skinny(sa, st));
+    }
+    // unfused (and fused with more than 32 rows, where re-quantizing X in
+    // every N-tile's producer would cost more than one quantize pass)
     cudaError_t e;
     if (g_x == nullptr) {
-        e = launch_global_scale(Xh, M, K, ldx, gx_slot, st);
-        if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+        // amax partials -> quantize (reduces g_x into the slot) -> GEMM, each
+        // a programmatic dependent of the one before
+        e = launch_quantize_dynamic(Xh, M, K, ldx, partials, gx_slot, xq, xs, st);
         g_x = gx_slot;
+    } else {
+        e = launch_quantize(Xh, M, K, ldx, g_x, xq, xs, NVFP4_SF_MMA_128x4, st);
     }
-    // The fused mode shares the unfused launch sequence until its kernel lands.
-    e = launch_quantize(Xh, M, K, ldx, g_x, xq, xs, NVFP4_SF_MMA_128x4, st);
     if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (M <= kSkinnyMaxM) {
+        SkinnyArgs sa{Wq, Ws, g_w, xq, xs, nullptr, 0, g_x, M, N, K,
+                      static_cast<uint16_t *>(Y), ldy, 0};
+        return from_cuda(launch_gemm_skinny(sa, st));
+    }
     GemmArgs a{xq, xs, g_x, Wq, Ws, g_w, M, N, K, static_cast<uint16_t *>(Y), ldy};
     return from_cuda(launch_gemm(a, st));
 }

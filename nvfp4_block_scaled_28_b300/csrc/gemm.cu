@@ -192,6 +192,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (CM > 1) cluster_sync_all();  // peers' barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
+    // The set-up above overlaps the previous kernel when launched as a
+    // programmatic dependent; operands and scales are read only after it.
+    pdl_launch_dependents();
+    pdl_wait();
 
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
@@ -450,17 +454,18 @@ cudaError_t launch_cm(const CUtensorMap &tmA, const CUtensorMap &tmB, Params p, 
     p.num_ctiles = ((p.num_m_tiles + CM - 1) / CM) * p.num_n_tiles;
     const int clusters = p.num_ctiles < max_clusters ? p.num_ctiles : max_clusters;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CM;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();
     cfg.gridDim = dim3(CM * clusters, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = SMEM_ALLOC;
     cfg.stream = st;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, gemm_kernel<CM>, tmA, tmB, p);
 }
 

@@ -1,0 +1,487 @@
+// Skinny-M block-scaled FP4 GEMM (LLM decode: M = 1 .. 128 tokens against a
+// wide weight), computed as Y^T = W X^T so that the 128-row tensor-core M
+// dimension is filled with weight rows and the few activation rows become
+// the MMA's N dimension (64 or 128; the rows of X beyond the M that is
+// loaded give output columns that are never stored):
+//
+//   D[n, m] = sum_k e2m1(Wq[n,k]) e4m3(Ws[n,k/16]) e2m1(Xq[m,k]) e4m3(Xs[m,k/16])
+//   Y[m, n] = bf16(g_x * g_w * D[n, m])
+//
+// Same arithmetic as the large-M kernel (the "nvfp4-difusion" page's block-
+// scaled matmul, section 2); only the roles of the operands are swapped. The
+// regime is bound by streaming the weights from HBM once (N K / 2 bytes of
+// codes plus N K / 16 of scales), so each CTA owns 128 weight rows, streams
+// them through an 8-deep ring and keeps the whole of X's tile resident per
+// stage.
+//
+// FUSED (M <= 32): the producer loads bfloat16 X tiles instead of codes, and
+// four quantizer warps turn them into E2M1 codes and E4M3 scales in shared
+// memory with the same arithmetic as nvfp4_quantize (quant_math.cuh) before
+// the MMA reads them, so X's codes never travel through HBM. Every CTA
+// re-quantizes the same small X; for decode that costs far less than a
+// separate quantize launch.
+//
+// Warps: 0 TMA producer, 1 MMA issuer (scale copies to TMEM + MMAs, issued
+// from the converged warp through elect.sync), 2 TMEM allocator, 3-6
+// epilogue (one per 32-lane TMEM quarter), 7-10 quantizers (FUSED only).
+// All waits are bounded; a timeout is recorded and every role leaves.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "quant_math.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int SK_BM = 128;                 // weight rows per tile
+constexpr int SK_BK = 256;                 // K per stage
+constexpr int SK_SF_TILE = 512;
+constexpr unsigned kAllLanes = 0xFFFFFFFFu;
+
+// NX: MMA N (64 or 128); XR <= NX: rows of X loaded (and quantized);
+// CPS: CTAs resident per SM (each gets 1/CPS of shared memory and TMEM).
+template <int NX, int XR, bool FUSED, int CPS>
+struct SkCfg {
+    static constexpr int W_BYTES = SK_BM * SK_BK / 2;            // 16 KiB
+    static constexpr int X_BYTES = NX * SK_BK / 2;               // codes, NX rows
+    static constexpr int X_LOAD = XR * SK_BK / 2;                // bytes of codes loaded
+    static constexpr int SFW_BYTES = 2048;                       // 4 scale tiles of W
+    static constexpr int SFX_BYTES = 2048;                       // 4 scale tiles of X
+    static constexpr int XBF_BYTES = FUSED ? XR * SK_BK * 2 : 0;  // bfloat16 X tile
+    static constexpr int OFF_W = 0;
+    static constexpr int OFF_X = OFF_W + W_BYTES;
+    static constexpr int OFF_SFW = OFF_X + X_BYTES;
+    static constexpr int OFF_SFX = OFF_SFW + SFW_BYTES;
+    static constexpr int OFF_XBF = OFF_SFX + SFX_BYTES;
+    static constexpr int STAGE_RAW = OFF_XBF + XBF_BYTES;
+    static constexpr int STAGE = (STAGE_RAW + 1023) / 1024 * 1024;
+    static constexpr int BUDGET = (CPS == 1 ? 220 : 108) * 1024;
+    static constexpr int STAGES = BUDGET / STAGE < 8 ? BUDGET / STAGE : 8;
+    static constexpr int BAR_OFF = STAGES * STAGE;
+    static constexpr int SMEM = BAR_OFF + 512 + 1024;
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int Q_WARPS = FUSED ? 4 : 0;
+    static constexpr int THREADS = 32 * (3 + EPI_WARPS + Q_WARPS);
+    static constexpr uint32_t ACC_COL = 0;                       // NX columns
+    static constexpr uint32_t SF_COL = 128;                      // per stage 16 (W) + 16 (X)
+    static constexpr uint32_t SF_COLS = 32;
+    static constexpr uint32_t TMEM_COLS = CPS == 1 ? 512 : 256;
+    static_assert(SF_COL + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
+    static_assert(STAGES >= 3, "pipeline depth");
+    static_assert(SMEM * CPS <= 232448, "shared memory budget");
+    static_assert(OFF_X % 1024 == 0 && STAGE % 1024 == 0, "swizzled tiles need 1024-B alignment");
+};
+
+struct SkParams {
+    const uint8_t *Ws;   // weight scales, 128x4 tile layout
+    const uint8_t *Xs;   // activation scales, 128x4 tile layout (unfused)
+    const uint16_t *X;   // bfloat16 activation (fused; read for amax when g_x is null)
+    int64_t ldx;
+    const float *g_x;    // fused: null = compute amax(|X|) / (6 * 448) in the kernel
+    const float *g_w;
+    uint16_t *Y;
+    int64_t ldy;
+    int M, N, K;
+    int n_tiles;
+    int inject;
+    uint64_t timeout_ns;
+    unsigned int *err;
+};
+
+template <int STAGES>
+struct SkShared {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t qdone[STAGES];
+    uint64_t acc_full;
+    uint64_t acc_empty;
+    uint64_t drain;
+    uint32_t tmem_base;
+    volatile uint32_t abort_flag;
+    float g_x;                 // fused: activation global scale used by this CTA
+    uint32_t amax_part[4];     // fused: per-quantizer-warp amax (bfloat16 bits)
+};
+
+template <int STAGES>
+__device__ __forceinline__ bool sk_wait(uint64_t *bar, uint32_t parity, const SkParams &p,
+                                        SkShared<STAGES> &sh) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        const uint32_t a = smem_addr(bar);
+        if (!mbar_try_wait(a, parity)) {
+            const uint64_t t0 = global_timer_ns();
+            while (true) {
+                if (mbar_try_wait(a, parity)) break;
+                if (sh.abort_flag) {
+                    ok = 0;
+                    break;
+                }
+                if (global_timer_ns() - t0 > p.timeout_ns) {
+                    record_timeout(p.err);
+                    sh.abort_flag = 1;
+                    ok = 0;
+                    break;
+                }
+            }
+        }
+    }
+    return __shfl_sync(kAllLanes, ok, 0) != 0;
+}
+
+template <int NX, int XR, bool FUSED, int CPS>
+__global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, CPS>::THREADS, CPS)
+    skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                  const SkParams p) {
+    using C = SkCfg<NX, XR, FUSED, CPS>;
+    constexpr int S = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    SkShared<S> &sh = *reinterpret_cast<SkShared<S> *>(smem + C::BAR_OFF);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int num_k = p.K / SK_BK;
+    const int kb4 = p.K / 64;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&sh.full[s], 1);
+            mbar_init(&sh.empty[s], 1);
+            mbar_init(&sh.qdone[s], C::Q_WARPS > 0 ? C::Q_WARPS : 1);
+        }
+        mbar_init(&sh.acc_full, 1);
+        mbar_init(&sh.acc_empty, C::EPI_WARPS);
+        mbar_init(&sh.drain, 1);
+        sh.abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmX);
+    }
+    if (warp == 2) {
+        tmem_alloc(&sh.tmem_base, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+    // set-up overlaps the previous kernel (programmatic dependent launch)
+    pdl_launch_dependents();
+    pdl_wait();
+
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer
+        const uint64_t pol_w = policy_evict_first();  // weights stream through once
+        const uint64_t pol_x = policy_evict_last();   // X is re-read by every CTA
+        constexpr uint32_t tx = FUSED ? (C::W_BYTES + C::SFW_BYTES + C::XBF_BYTES)
+                                      : (C::W_BYTES + C::SFW_BYTES + C::X_LOAD + C::SFX_BYTES);
+        int g = 0;
+        bool ok = !p.inject;
+        for (int nt = blockIdx.x; ok && nt < p.n_tiles; nt += gridDim.x) {
+            for (int kt = 0; kt < num_k; ++kt, ++g) {
+                const int s = g % S;
+                if (!sk_wait<S>(&sh.empty[s], ((g / S) & 1) ^ 1, p, sh)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    uint8_t *st = smem + s * C::STAGE;
+                    mbar_arrive_expect_tx(&sh.full[s], tx);
+                    tma_load_2d(st + C::OFF_W, &tmW, &sh.full[s], kt * (SK_BK / 2), nt * SK_BM,
+                                pol_w);
+                    bulk_load(st + C::OFF_SFW,
+                              p.Ws + (static_cast<int64_t>(nt) * kb4 + kt * 4) * SK_SF_TILE,
+                              C::SFW_BYTES, &sh.full[s], pol_w);
+                    if (FUSED) {
+                        tma_load_2d(st + C::OFF_XBF, &tmX, &sh.full[s], kt * SK_BK, 0, pol_x);
+                    } else {
+                        tma_load_2d(st + C::OFF_X, &tmX, &sh.full[s], kt * (SK_BK / 2), 0, pol_x);
+                        bulk_load(st + C::OFF_SFX, p.Xs + static_cast<int64_t>(kt) * 4 * SK_SF_TILE,
+                                  C::SFX_BYTES, &sh.full[s], pol_x);
+                    }
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok && !p.inject && lane == 0) {
+            for (int s = 0; s < S && s < g; ++s) {
+                const int fills = (g - s + S - 1) / S;
+                mbar_wait(&sh.full[s], (fills - 1) & 1, p.timeout_ns);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = idesc_mxf4nvf4(SK_BM, NX);
+        int g = 0, it = 0;
+        bool ok = true;
+        for (int nt = blockIdx.x; ok && nt < p.n_tiles; nt += gridDim.x, ++it) {
+            if (!sk_wait<S>(&sh.acc_empty, (it & 1) ^ 1, p, sh)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int kt = 0; kt < num_k; ++kt, ++g) {
+                const int s = g % S;
+                uint64_t *ready = FUSED ? &sh.qdone[s] : &sh.full[s];
+                if (!sk_wait<S>(ready, (g / S) & 1, p, sh)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint8_t *st = smem + s * C::STAGE;
+                const uint32_t sf_w = tmem + C::SF_COL + s * C::SF_COLS;
+                const uint32_t sf_x = sf_w + 16;
+                const uint32_t sfw_smem = smem_addr(st + C::OFF_SFW);
+                const uint32_t sfx_smem = smem_addr(st + C::OFF_SFX);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    tmem_cp_32x128b_x4_elect(sf_w + j * 4, sdesc_sf(sfw_smem + j * SK_SF_TILE));
+                    tmem_cp_32x128b_x4_elect(sf_x + j * 4, sdesc_sf(sfx_smem + j * SK_SF_TILE));
+                }
+                const uint32_t w_smem = smem_addr(st + C::OFF_W);
+                const uint32_t x_smem = smem_addr(st + C::OFF_X);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    mma_mxf4nvf4_elect(tmem + C::ACC_COL, sdesc_sw128(w_smem + j * 32),
+                                       sdesc_sw128(x_smem + j * 32), idesc, sf_w + j * 4,
+                                       sf_x + j * 4, (kt | j) != 0);
+                tc_commit_elect(&sh.empty[s]);
+            }
+            if (ok) tc_commit_elect(&sh.acc_full);
+        }
+        if (!ok) {
+            tc_commit_elect(&sh.drain);
+            if (lane == 0) mbar_wait(&sh.drain, 0, p.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // TMEM allocator only
+    } else if (warp < 3 + C::EPI_WARPS) {
+        // -------------------------------------------------------- epilogue
+        const int quarter = warp & 3;
+        int it = 0;
+        for (int nt = blockIdx.x; nt < p.n_tiles; nt += gridDim.x, ++it) {
+            if (!sk_wait<S>(&sh.acc_full, it & 1, p, sh)) break;
+            tc_fence_after();
+            // fused: the quantizer warps published g_x in shared memory before
+            // the MMAs this accumulator completion follows
+            const float gx = FUSED ? sh.g_x : *p.g_x;
+            const float alpha = __fmul_rn(gx, *p.g_w);
+            const uint32_t t_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + C::ACC_COL;
+            // D[n, m]: lane = weight row n, column = activation row m
+            float acc[NX];
+#pragma unroll
+            for (int c = 0; c < NX / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_base + c * 32, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[c * 32 + i] = __uint_as_float(r[i]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.acc_empty);
+            const int n = nt * SK_BM + quarter * 32 + lane;
+            if (n < p.N) {
+#pragma unroll
+                for (int m = 0; m < XR; ++m) {
+                    if (m < p.M) {
+                        const __nv_bfloat16 v = __float2bfloat16_rn(acc[m] * alpha);
+                        p.Y[static_cast<int64_t>(m) * p.ldy + n] = *reinterpret_cast<const uint16_t *>(&v);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (FUSED) {
+        // ------------------------------------------------ X quantizer warps
+        const int qt = threadIdx.x - 32 * (3 + C::EPI_WARPS);  // 0 .. 127
+        const int qwarp = qt >> 5;
+        float gx;
+        if (p.g_x != nullptr) {
+            gx = *p.g_x;
+        } else {
+            // g_x = amax(|X|) / (6 * 448) (1 for an all-zero X), computed by every
+            // CTA with the same integer max and IEEE division as
+            // nvfp4_global_scale, so the bytes match the unfused path
+            const uint32_t vpr = static_cast<uint32_t>(p.K / 8);
+            const uint32_t total = static_cast<uint32_t>(p.M) * vpr;
+            const uint32_t m16 = 0x7FFF7FFFu;
+            uint32_t acc = 0;
+            for (uint32_t i = qt; i < total; i += 128) {
+                const uint32_t r = i / vpr, c = i - r * vpr;
+                const uint4 v = *reinterpret_cast<const uint4 *>(p.X + r * p.ldx + c * 8ull);
+                acc = max_u16x2(acc, max_u16x2(max_u16x2(v.x & m16, v.y & m16),
+                                               max_u16x2(v.z & m16, v.w & m16)));
+            }
+            uint32_t a = max(acc & 0xFFFFu, acc >> 16);
+            a = __reduce_max_sync(kAllLanes, a);
+            if (lane == 0) sh.amax_part[qwarp] = a;
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // the four quantizer warps
+            a = max(max(sh.amax_part[0], sh.amax_part[1]), max(sh.amax_part[2], sh.amax_part[3]));
+            const float amax = __uint_as_float(a << 16);
+            gx = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+        }
+        if (qt == 0) sh.g_x = gx;
+        const int mrows = p.M < XR ? p.M : XR;
+        int g = 0;
+        bool ok = true;
+        for (int nt = blockIdx.x; ok && nt < p.n_tiles; nt += gridDim.x) {
+            for (int kt = 0; kt < num_k; ++kt, ++g) {
+                const int s = g % S;
+                if (!sk_wait<S>(&sh.full[s], (g / S) & 1, p, sh)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *st = smem + s * C::STAGE;
+                const uint8_t *xbf = st + C::OFF_XBF;  // XR rows x 512 bytes, dense
+                uint8_t *xq = st + C::OFF_X;           // NX rows x 128 bytes, 128-byte swizzle
+                uint8_t *xsf = st + C::OFF_SFX;        // 4 scale tiles of 512 bytes
+                // the M rows present, 16 blocks of 16 elements each; rows
+                // M .. XR-1 only feed output columns that are never stored
+                for (int b = qt; b < mrows * 16; b += 128) {
+                    const int r = b >> 4, kb = b & 15;
+                    const uint4 *src = reinterpret_cast<const uint4 *>(xbf + r * 512 + kb * 32);
+                    const uint4 a = src[0], c = src[1];
+                    uint32_t lo, hi;
+                    const uint32_t Sb = quantize16(a, c, gx, lo, hi);
+                    const int chunk = kb >> 1;
+                    *reinterpret_cast<uint2 *>(xq + r * 128 + ((chunk ^ (r & 7)) << 4) +
+                                               (kb & 1) * 8) = make_uint2(lo, hi);
+                    xsf[(kb >> 2) * SK_SF_TILE + (r & 31) * 16 + (r >> 5) * 4 + (kb & 3)] =
+                        static_cast<uint8_t>(Sb);
+                }
+                fence_proxy_async_shared();  // generic-proxy writes -> tensor core reads
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.qdone[s]);
+            }
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn sk_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+bool sk_map(CUtensorMap *map, CUtensorMapDataType type, const void *ptr, uint64_t inner,
+            uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
+            CUtensorMapSwizzle swz) {
+    EncodeTiledFn enc = sk_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    return enc(map, type, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NX, int XR, bool FUSED, int CPS>
+cudaError_t launch_sk(const SkinnyArgs &a, cudaStream_t st) {
+    using C = SkCfg<NX, XR, FUSED, CPS>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(skinny_kernel<NX, XR, FUSED, CPS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    CUtensorMap tmW, tmX;
+    if (!sk_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wq, a.K / 2, a.N, a.K / 2, 128, SK_BM,
+                CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    if (FUSED) {
+        if (!sk_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.X, a.K, a.M, a.ldx * 2, SK_BK, XR,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    } else {
+        if (!sk_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Xq, a.K / 2, a.M, a.K / 2, 128, XR,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    SkParams p;
+    p.Ws = a.Ws;
+    p.Xs = a.Xs;
+    p.X = a.X;
+    p.ldx = a.ldx;
+    p.g_x = a.g_x;
+    p.g_w = a.g_w;
+    p.Y = a.Y;
+    p.ldy = a.ldy;
+    p.M = static_cast<int>(a.M);
+    p.N = static_cast<int>(a.N);
+    p.K = static_cast<int>(a.K);
+    p.n_tiles = static_cast<int>((a.N + SK_BM - 1) / SK_BM);
+    p.inject = debug_state().inject;
+    p.timeout_ns = debug_state().timeout_ns;
+    p.err = device_error_word();
+    if (p.err == nullptr) return cudaErrorInvalidSymbol;
+    const int slots = CPS * launch_cfg().num_sms;
+    const int grid = p.n_tiles < slots ? p.n_tiles : slots;
+    cudaLaunchAttribute pdl = pdl_attribute();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cfg.attrs = &pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, skinny_kernel<NX, XR, FUSED, CPS>, tmW, tmX, p);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_skinny(const SkinnyArgs &a, cudaStream_t st) {
+    if (a.M == 0 || a.N == 0) return cudaSuccess;
+    if (a.M > kSkinnyMaxM || (a.fused && a.M > kSkinnyFusedMaxM)) return cudaErrorInvalidValue;
+    static int cps = 0;
+    if (cps == 0) {
+        const char *env = getenv("NVFP4_SKINNY_CTAS_PER_SM");  // tuning knob: 1 or 2
+        cps = (env && env[0] == '2' && env[1] == 0) ? 2 : 1;
+    }
+    if (cps == 2) {
+        if (a.M <= 32)
+            return a.fused ? launch_sk<64, 32, true, 1>(a, st) : launch_sk<64, 32, false, 2>(a, st);
+        if (a.M <= 64) return launch_sk<64, 64, false, 2>(a, st);
+        return launch_sk<128, 128, false, 2>(a, st);
+    }
+    if (a.M <= 32)
+        return a.fused ? launch_sk<64, 32, true, 1>(a, st) : launch_sk<64, 32, false, 1>(a, st);
+    if (a.M <= 64) return launch_sk<64, 64, false, 1>(a, st);
+    return launch_sk<128, 128, false, 1>(a, st);
+}
+
+}  // namespace nvfp4

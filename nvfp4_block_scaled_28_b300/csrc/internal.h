@@ -42,6 +42,20 @@ cudaError_t launch_quantize(const uint16_t *X, int64_t rows, int64_t cols, int64
                             const float *g, uint8_t *q, uint8_t *sf, int layout,
                             cudaStream_t st);
 
+// Activation quantization with a dynamic global scale as two kernels chained
+// by programmatic dependent launch: per-CTA partial amax into `partials`
+// (kMaxAmaxPartials words), then a quantizer whose CTAs each reduce the
+// partials to g (written to *g_out by CTA 0) and quantize into the
+// tensor-core scale layout (padding rows zeroed). No memset, no finalize.
+constexpr int kMaxAmaxPartials = 2048;
+cudaError_t launch_quantize_dynamic(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
+                                    uint32_t *partials, float *g_out, uint8_t *q, uint8_t *sf,
+                                    cudaStream_t st);
+
+// Launch configuration for kernels that take part in programmatic
+// dependent launch chains.
+cudaLaunchAttribute pdl_attribute();
+
 cudaError_t launch_sf_to_mma(const uint8_t *sf_rm, int64_t rows, int64_t K, uint8_t *sf_mma,
                              cudaStream_t st);
 
@@ -56,6 +70,23 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st);
+
+// Skinny-M GEMM (Y^T = W X^T, weights as the 128-row MMA operand).
+constexpr int64_t kSkinnyMaxM = 128;       // activation rows it handles
+constexpr int64_t kSkinnyFusedMaxM = 32;   // ... with in-kernel quantization of X
+struct SkinnyArgs {
+    const uint8_t *Wq, *Ws;  // weights: codes (N x K/2), scales (128x4 tile layout)
+    const float *g_w;
+    const uint8_t *Xq, *Xs;  // unfused: activation codes (M x K/2), tile-layout scales
+    const uint16_t *X;       // fused: bfloat16 activation, leading dimension ldx
+    int64_t ldx;
+    const float *g_x;
+    int64_t M, N, K;
+    uint16_t *Y;
+    int64_t ldy;
+    int fused;
+};
+cudaError_t launch_gemm_skinny(const SkinnyArgs &a, cudaStream_t st);
 
 cudaError_t launch_mma_peak(int ctas, int iters, int variant, unsigned long long *cycles,
                             cudaStream_t st);

@@ -27,6 +27,21 @@ __device__ __forceinline__ uint32_t elect_lane0() {
     return (threadIdx.x & 31) == 0;
 }
 
+// ------------------------------------------- programmatic dependent launch
+
+// Wait until the grid this one depends on (the previous kernel in the
+// stream, when launched with programmatic stream serialization) has
+// completed and its writes are visible; a no-op otherwise.
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel in the stream to be scheduled (it still waits in
+// pdl_wait() for this grid to complete before touching its results).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {

@@ -1,0 +1,74 @@
+// The NVFP4 block quantizer's arithmetic, shared by the standalone
+// quantizer and the GEMM that quantizes activations in its producer, so both
+// produce the same bytes.
+//
+// Format ("nvfp4-gemma4" page, section 2; "nvfp4-difusion" page, section 2):
+// E2M1 codes two per byte (even element in the low nibble), one E4M3 scale
+// per 16 consecutive elements. Scale rule (absmax) with the decode-direction
+// global scale g:
+//   S = E4M3_rne_satfinite((amax_block / 6) / g)
+//   r = 1 / (e4m3(S) * g)   (0 when S == 0)
+//   code = E2M1_rne_satfinite(x * r), sign bit = sign bit of x.
+// Every float step is one IEEE binary32 operation (explicit _rn intrinsics,
+// never contracted).
+#pragma once
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace nvfp4 {
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Largest |x| of the 8 bfloat16 pairs as a bfloat16 magnitude bit pattern.
+// Non-negative floats order like their bit patterns, so this is exact.
+__device__ __forceinline__ uint32_t amax_bits16(uint4 a, uint4 b) {
+    const uint32_t m = 0x7FFF7FFFu;
+    uint32_t t0 = max_u16x2(a.x & m, a.y & m);
+    uint32_t t1 = max_u16x2(a.z & m, a.w & m);
+    uint32_t t2 = max_u16x2(b.x & m, b.y & m);
+    uint32_t t3 = max_u16x2(b.z & m, b.w & m);
+    uint32_t t = max_u16x2(max_u16x2(t0, t1), max_u16x2(t2, t3));
+    return max(t & 0xFFFFu, t >> 16);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Four E2M1 codes of the two bfloat16 pairs w0 (elements 0,1) and w1
+// (elements 2,3), packed little-end first.
+__device__ __forceinline__ uint32_t codes4(uint32_t w0, uint32_t w1, float r) {
+    uint32_t b0 = cvt_e2m1x2(__fmul_rn(bf16_lo(w0), r), __fmul_rn(bf16_hi(w0), r));
+    uint32_t b1 = cvt_e2m1x2(__fmul_rn(bf16_lo(w1), r), __fmul_rn(bf16_hi(w1), r));
+    return b0 | (b1 << 8);
+}
+
+// Quantize one 16-element block held in (a, b). Returns the scale byte and
+// writes the 8 code bytes into (lo, hi).
+__device__ __forceinline__ uint32_t quantize16(uint4 a, uint4 b, float g, uint32_t &lo,
+                                               uint32_t &hi) {
+    const float amax = __uint_as_float(amax_bits16(a, b) << 16);
+    const float v = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
+    const uint32_t S = cvt_e4m3_satfinite(v);
+    const float s = e4m3_to_f32(S);
+    const float denom = __fmul_rn(s, g);
+    const float r = denom > 0.0f ? __frcp_rn(denom) : 0.0f;
+    lo = codes4(a.x, a.y, r) | (codes4(a.z, a.w, r) << 16);
+    hi = codes4(b.x, b.y, r) | (codes4(b.z, b.w, r) << 16);
+    return S;
+}
+
+}  // namespace nvfp4

@@ -15,64 +15,13 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant_math.cuh"
 
 namespace nvfp4 {
 
 namespace {
 
 constexpr int kThreads = 256;
-
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-// Largest |x| of the 8 bfloat16 pairs as a bfloat16 magnitude bit pattern.
-// Non-negative floats order like their bit patterns, so this is exact.
-__device__ __forceinline__ uint32_t amax_bits16(uint4 a, uint4 b) {
-    const uint32_t m = 0x7FFF7FFFu;
-    uint32_t t0 = max_u16x2(a.x & m, a.y & m);
-    uint32_t t1 = max_u16x2(a.z & m, a.w & m);
-    uint32_t t2 = max_u16x2(b.x & m, b.y & m);
-    uint32_t t3 = max_u16x2(b.z & m, b.w & m);
-    uint32_t t = max_u16x2(max_u16x2(t0, t1), max_u16x2(t2, t3));
-    return max(t & 0xFFFFu, t >> 16);
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Four E2M1 codes of the two bfloat16 pairs w0 (elements 0,1) and w1
-// (elements 2,3), packed little-end first.
-__device__ __forceinline__ uint32_t codes4(uint32_t w0, uint32_t w1, float r) {
-    uint32_t b0 = cvt_e2m1x2(__fmul_rn(bf16_lo(w0), r), __fmul_rn(bf16_hi(w0), r));
-    uint32_t b1 = cvt_e2m1x2(__fmul_rn(bf16_lo(w1), r), __fmul_rn(bf16_hi(w1), r));
-    return b0 | (b1 << 8);
-}
-
-// Quantize one 16-element block held in (a, b). Returns the scale byte and
-// writes the 8 code bytes into (lo, hi).
-__device__ __forceinline__ uint32_t quantize16(uint4 a, uint4 b, float g, uint32_t &lo,
-                                               uint32_t &hi) {
-    const float amax = __uint_as_float(amax_bits16(a, b) << 16);
-    const float v = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
-    const uint32_t S = cvt_e4m3_satfinite(v);
-    const float s = e4m3_to_f32(S);
-    const float denom = __fmul_rn(s, g);
-    const float r = denom > 0.0f ? __frcp_rn(denom) : 0.0f;
-    lo = codes4(a.x, a.y, r) | (codes4(a.z, a.w, r) << 16);
-    hi = codes4(b.x, b.y, r) | (codes4(b.z, b.w, r) << 16);
-    return S;
-}
 
 // Byte offset of scale (row, kb) in the 128x4 tensor-core tile layout.
 __device__ __forceinline__ uint64_t sf_mma_offset(uint32_t row, uint32_t kb, uint32_t kb4) {
@@ -167,6 +116,95 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t *__restri
     }
 }
 
+// Per-CTA partial amax (bfloat16 magnitude bits) -> partials[blockIdx.x];
+// every CTA writes its slot, so nothing needs zeroing beforehand.
+__global__ void __launch_bounds__(kThreads) amax_partial_kernel(const uint16_t *__restrict__ X,
+                                                                uint32_t rows, uint32_t vpr,
+                                                                uint64_t ldx, FastDiv div_vpr,
+                                                                uint32_t *partials) {
+    pdl_launch_dependents();
+    pdl_wait();  // X may come from the previous kernel
+    const uint32_t total = rows * vpr;
+    const uint32_t stride = gridDim.x * blockDim.x;
+    const uint32_t m = 0x7FFF7FFFu;
+    uint32_t acc = 0;
+    uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < total; i += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t j = i + u * stride;
+            const uint32_t r = div_vpr.div(j), c = j - r * vpr;
+            v[u] = ld_stream(reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            acc = max_u16x2(acc, max_u16x2(max_u16x2(v[u].x & m, v[u].y & m),
+                                           max_u16x2(v[u].z & m, v[u].w & m)));
+    }
+    for (; i < total; i += stride) {
+        const uint32_t r = div_vpr.div(i), c = i - r * vpr;
+        const uint4 v = ld_stream(reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull));
+        acc = max_u16x2(acc, max_u16x2(max_u16x2(v.x & m, v.y & m), max_u16x2(v.z & m, v.w & m)));
+    }
+    uint32_t a = max(acc & 0xFFFFu, acc >> 16);
+    a = __reduce_max_sync(0xFFFFFFFFu, a);
+    __shared__ uint32_t warp_max[kThreads / 32];
+    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = a;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        uint32_t b = threadIdx.x < kThreads / 32 ? warp_max[threadIdx.x] : 0u;
+        b = __reduce_max_sync(0xFFFFFFFFu, b);
+        if (threadIdx.x == 0) partials[blockIdx.x] = b;
+    }
+}
+
+// Quantize into the tensor-core scale layout with g reduced from the amax
+// partials (same integer max and IEEE division as global_scale_finalize).
+__global__ void __launch_bounds__(kThreads) quantize_dynamic_kernel(
+    const uint16_t *__restrict__ X, uint32_t rows, uint32_t rows_pad, uint32_t kbpr, uint64_t ldx,
+    FastDiv div_kbpr, const uint32_t *__restrict__ partials, uint32_t n_partials, float *g_out,
+    uint8_t *__restrict__ q, uint8_t *__restrict__ sf) {
+    pdl_launch_dependents();
+    pdl_wait();  // the partials come from amax_partial_kernel
+    __shared__ float g_sh;
+    if (threadIdx.x < 32) {
+        uint32_t b = 0;
+        for (uint32_t i = threadIdx.x; i < n_partials; i += 32) b = max(b, partials[i]);
+        b = __reduce_max_sync(0xFFFFFFFFu, b);
+        if (threadIdx.x == 0) {
+            const float amax = __uint_as_float(b << 16);
+            g_sh = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+        }
+    }
+    __syncthreads();
+    const float g = g_sh;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+    const uint32_t total = rows * kbpr;
+    const uint32_t total_pad = rows_pad * kbpr;
+    const uint32_t stride = gridDim.x * blockDim.x;
+    const uint32_t kb4 = kbpr >> 2;
+    for (uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < total_pad; i0 += 2 * stride) {
+        const uint32_t i1 = i0 + stride;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const uint32_t i = u == 0 ? i0 : i1;
+            if (i >= total_pad) break;
+            const uint32_t row = div_kbpr.div(i), kb = i - row * kbpr;
+            if (i >= total) {  // padding rows of the last 128-row group read 0
+                sf[sf_mma_offset(row, kb, kb4)] = 0;
+                continue;
+            }
+            const uint4 *src = reinterpret_cast<const uint4 *>(X + row * ldx + kb * 16ull);
+            const uint4 a = ld_stream(src), b = ld_stream(src + 1);
+            uint32_t lo, hi;
+            const uint32_t S = quantize16(a, b, g, lo, hi);
+            *reinterpret_cast<uint2 *>(q + static_cast<uint64_t>(i) * 8) = make_uint2(lo, hi);
+            sf[sf_mma_offset(row, kb, kb4)] = static_cast<uint8_t>(S);
+        }
+    }
+}
+
 // g = amax / (6 * 448), or 1 for an all-zero tensor; in place over the cell.
 __global__ void global_scale_finalize(uint32_t *cell) {
     const float amax = __uint_as_float(*cell << 16);
@@ -241,6 +279,39 @@ cudaError_t launch_quantize(const uint16_t *X, int64_t rows, int64_t cols, int64
             X, static_cast<uint32_t>(rows), kbpr, static_cast<uint64_t>(ldx), FastDiv(kbpr), g, q,
             sf);
     return cudaGetLastError();
+}
+
+cudaLaunchAttribute pdl_attribute() {
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+    return a;
+}
+
+cudaError_t launch_quantize_dynamic(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
+                                    uint32_t *partials, float *g_out, uint8_t *q, uint8_t *sf,
+                                    cudaStream_t st) {
+    const uint32_t vpr = static_cast<uint32_t>(cols / 8);
+    const uint64_t total = static_cast<uint64_t>(rows) * vpr;
+    int n_partials = grid_for(total, 4);
+    if (n_partials > kMaxAmaxPartials) n_partials = kMaxAmaxPartials;
+    cudaLaunchAttribute attr = pdl_attribute();
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = st;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(n_partials, 1, 1);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, amax_partial_kernel, X, static_cast<uint32_t>(rows),
+                                       vpr, static_cast<uint64_t>(ldx), FastDiv(vpr), partials);
+    if (e != cudaSuccess) return e;
+    const uint32_t kbpr = static_cast<uint32_t>(cols / 16);
+    const uint32_t rows_pad = static_cast<uint32_t>((rows + 127) / 128 * 128);
+    cfg.gridDim = dim3(grid_for(static_cast<uint64_t>(rows_pad) * kbpr, 2), 1, 1);
+    return cudaLaunchKernelEx(&cfg, quantize_dynamic_kernel, X, static_cast<uint32_t>(rows),
+                              rows_pad, kbpr, static_cast<uint64_t>(ldx), FastDiv(kbpr),
+                              static_cast<const uint32_t *>(partials),
+                              static_cast<uint32_t>(n_partials), g_out, q, sf);
 }
 
 cudaError_t launch_sf_to_mma(const uint8_t *sf_rm, int64_t rows, int64_t K, uint8_t *sf_mma,

@@ -120,6 +120,36 @@ def test_gemm_zero_sized_is_noop(nv):
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("M", [1, 3, 17, 32])
+@pytest.mark.parametrize("N,K", [(8, 256), (200, 768), (1000, 512)])
+def test_fused_skinny_equals_unfused(nv, oracle_mod, M, N, K):
+    """M <= 32: the fused kernel quantizes X in shared memory; its output is
+    bitwise the unfused one's, and within tolerance of the oracle."""
+    x = workloads.make_x("outlier", M, K, seed=M * 131 + N)
+    w = workloads.make_w(N, K, seed=N * 7 + K)
+    y_unf, _ = _run_linear(nv, x, w, nv.LINEAR_UNFUSED)
+    y_fus, _ = _run_linear(nv, x, w, nv.LINEAR_FUSED)
+    assert torch.equal(y_unf.view(torch.int16), y_fus.view(torch.int16))
+    (xq, xs, gx), (wq, ws, gw) = _oracle_operands(oracle_mod, x, w)
+    check_gemm_tolerance(bf16_bits(y_fus), oracle_mod.gemm(xq, xs, gx, wq, ws, gw), "fused")
+    assert nv.nvfp4_device_error() == 0
+
+
+def test_fused_skinny_strided_x_and_given_scale(nv, oracle_mod):
+    M, N, K = 20, 384, 1024
+    big = workloads.make_x("outlier", M, K + 256, seed=3)
+    x = big[:, 128:128 + K]
+    w = workloads.make_w(N, K, seed=4)
+    (xq, xs, gx), (wq, ws, gw) = _oracle_operands(oracle_mod, x.contiguous(), w)
+    Wq, Ws, g_w = nv.nvfp4_quantize_weight(w.cuda(), nv.SF_MMA_128x4)
+    xd = big.cuda()[:, 128:128 + K]
+    g = torch.tensor([gx], dtype=torch.float32, device="cuda")
+    y_f = nv.nvfp4_linear(xd, Wq, Ws, g_w, g_x=g, mode=nv.LINEAR_FUSED)
+    y_u = nv.nvfp4_linear(xd, Wq, Ws, g_w, mode=nv.LINEAR_UNFUSED)
+    assert torch.equal(y_f.view(torch.int16), y_u.view(torch.int16))
+    check_gemm_tolerance(bf16_bits(y_f), oracle_mod.gemm(xq, xs, gx, wq, ws, gw), "strided")
+
+
 def _full_size_case(nv, oracle_mod, name, M, Nn, n_rows):
     w_ = workloads.WORKLOADS[name]
     x = workloads.make_x(w_.x_kind, M, w_.K, workloads.x_seed(w_))
@@ -133,6 +163,9 @@ def _full_size_case(nv, oracle_mod, name, M, Nn, n_rows):
     y_ref = oracle_mod.gemm_rows(xq, xs, gx, wq, ws, gw, rows)
     y_rows = y.index_select(0, torch.from_numpy(rows).cuda())
     max_rel, floor_only = check_gemm_tolerance(bf16_bits(y_rows), y_ref, name)
+    if M <= 32:  # the fused decode path, in the configuration the benchmark times
+        y_f, _ = _run_linear(nv, x, w, nv.LINEAR_FUSED)
+        assert torch.equal(y_f.view(torch.int16), y.view(torch.int16))
     print("%s M=%d N=%d: max_rel=%.3g floor_only=%d" % (name, M, Nn, max_rel, floor_only))
     assert np.array_equal(to_np_u8(Wq), wq)
     assert nv.nvfp4_device_error() == 0
