@@ -209,7 +209,8 @@ nvfp4_status nvfp4_gemm(const uint8_t *Aq, const uint8_t *As, const float *g_a, 
         return from_cuda(launch_gemm_skinny(sa, static_cast<cudaStream_t>(stream)));
     }
     GemmArgs a{Aq, As, g_a, Bq, Bs, g_b, M, N, K, static_cast<uint16_t *>(Y), ldy};
-    return from_cuda(launch_gemm(a, static_cast<cudaStream_t>(stream)));
+    return from_cuda(gemm_use_pair() ? launch_gemm_pair(a, static_cast<cudaStream_t>(stream))
+                                     : launch_gemm(a, static_cast<cudaStream_t>(stream)));
 }
 
 // nvfp4_linear workspace: [g_x | amax partials] header, X codes, X scales.
@@ -274,7 +275,7 @@ nvfp4_status nvfp4_linear(const void *X, int64_t M, int64_t K, int64_t ldx, cons
         return from_cuda(launch_gemm_skinny(sa, st));
     }
     GemmArgs a{xq, xs, g_x, Wq, Ws, g_w, M, N, K, static_cast<uint16_t *>(Y), ldy};
-    return from_cuda(launch_gemm(a, st));
+    return from_cuda(gemm_use_pair() ? launch_gemm_pair(a, st) : launch_gemm(a, st));
 }
 
 nvfp4_status nvfp4_device_error(int clear) {

@@ -1,0 +1,441 @@
+// Block-scaled FP4 GEMM on a CTA pair: the same product as gemm.cu,
+//
+//   Y[m, n] = bf16( g_a * g_b * sum_k e2m1(A[m,k]) e4m3(SA[m,k/16])
+//                                     e2m1(B[n,k]) e4m3(SB[n,k/16]) )
+//
+// (the "nvfp4-difusion" page's quantized matmul, section 2), computed with
+// the two-SM form of the tensor-core instruction (tcgen05 .cta_group::2).
+//
+// Why a pair: one 128 x 256 x 64 FP4 MMA takes 128 cycles, so a single SM
+// with a 128 x 256 tile must receive 48 KiB of A/B (+6 KiB of scales) every
+// 512 cycles, more than TMA delivers into one SM's shared memory when all
+// SMs stream at once. In a pair each CTA holds 128 rows of A and 128 rows
+// of B of a 256 x 256 tile and the instruction reads the partner's half of
+// B directly, so each SM receives 32 KiB of A/B per 512 MMA cycles.
+//
+// Persistent kernel, clusters of 2 CTAs (one per SM), 256 x 256 output
+// tiles per pair, K in stages of 256 (4 MMAs of K = 64). Warp roles, in
+// both CTAs unless noted:
+//   warp 0    TMA producer: this CTA's A rows, B rows, A scales and all 256
+//             B-row scales of the tile for stage g, into a STAGES-deep ring.
+//             Every load of both CTAs is counted on the full barrier of
+//             rank 0, which therefore sees the whole stage.
+//   warp 1    (rank 0) MMA issuer: per stage, 12 scale copies shared -> TMEM
+//             and 4 MMAs, each one instruction for both CTAs; the release
+//             of the stage and of the finished accumulator is multicast to
+//             both CTAs' barriers.
+//   warp 2    allocates and frees TMEM (jointly with the partner CTA).
+//   warps 3-10 epilogue over this CTA's 128 accumulator rows: tcgen05.ld,
+//             release to rank 0's accumulator barrier (16 arrivals: 8 warps
+//             x 2 CTAs), scale by g_a g_b, round to bfloat16, store.
+// Every mbarrier wait is bounded in time; a wait that runs out records a
+// timeout in the device error word and the roles of both CTAs leave.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tensor_map.h"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int PM = 256;                    // tile rows per pair
+constexpr int BM = 128;                    // ... per CTA
+constexpr int BN = 256;                    // tile columns
+constexpr int BNH = 128;                   // B rows loaded by each CTA
+constexpr int BK = 256;                    // FP4 elements per stage
+constexpr int STAGES = 5;
+constexpr int A_BYTES = BM * BK / 2;       // 16 KiB
+constexpr int B_BYTES = BNH * BK / 2;      // 16 KiB
+constexpr int SFA_BYTES = BM * BK / 16;    // 2 KiB: 4 tiles of 512 B
+constexpr int SFB_BYTES = BN * BK / 16;    // 4 KiB: 2 row groups x 4 tiles
+constexpr int SF_TILE = 512;
+constexpr int SF_ROW = 256;                // scale arrays as rows of 256 bytes
+constexpr int CTA_STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+constexpr uint32_t STAGE_TX = 2 * CTA_STAGE_BYTES;  // both CTAs, counted at rank 0
+constexpr int MMAS_PER_STAGE = BK / 64;    // 4
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_COL = 0;            // 256 FP32 columns
+constexpr uint32_t SF_COL = 256;           // per stage: 16 (SFA) + 32 (SFB)
+constexpr uint32_t SF_COLS_PER_STAGE = 48;
+constexpr int kEpiWarps = 8;
+constexpr int kFirstEpiWarp = 3;
+constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);  // 352
+constexpr int GROUP_M = 8;                 // raster: 8 pair rows (2048 rows) per sweep
+constexpr uint16_t kPairMask = 0x3;
+constexpr unsigned kAll = 0xFFFFFFFFu;
+
+constexpr int SMEM_A = 0;
+constexpr int SMEM_B = SMEM_A + STAGES * A_BYTES;
+constexpr int SMEM_SFA = SMEM_B + STAGES * B_BYTES;
+constexpr int SMEM_SFB = SMEM_SFA + STAGES * SFA_BYTES;
+constexpr int SMEM_BAR = SMEM_SFB + STAGES * SFB_BYTES;
+constexpr int SMEM_USED = SMEM_BAR + 256;
+constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // room to align the base to 1024
+
+static_assert(SF_COL + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
+static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+
+struct Params {
+    const float *g_a;
+    const float *g_b;
+    uint16_t *Y;
+    int64_t ldy;
+    int M, N, K;
+    int num_m_tiles;     // 256-row tiles
+    int num_n_tiles;     // 256-column tiles
+    int num_tiles;
+    int y_vec;           // rows of Y start 16-byte aligned: 16-byte stores
+    int inject;          // 1: the producers issue nothing (bounded-wait test)
+    uint64_t timeout_ns;
+    unsigned int *err;   // device error word
+};
+
+struct Shared {
+    uint64_t full[STAGES];   // (rank 0) both CTAs' loads of the stage landed
+    uint64_t empty[STAGES];  // MMAs of the stage done: its slot may be refilled
+    uint64_t acc_full;       // accumulator complete (both CTAs)
+    uint64_t acc_empty;      // (rank 0) both CTAs drained the accumulator
+    uint64_t drain_mma;      // teardown after an abort: MMAs issued have completed
+    uint32_t tmem_base;
+    volatile uint32_t abort_flag;
+};
+static_assert(sizeof(Shared) <= 256, "barrier area");
+
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int &mt, int &nt) {
+    const int per_group = GROUP_M * num_n;
+    const int group = t / per_group;
+    const int first_m = group * GROUP_M;
+    const int gsz = min(num_m - first_m, GROUP_M);
+    const int local = t - group * per_group;
+    mt = first_m + local % gsz;
+    nt = local / gsz;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Bounded wait by lane 0 of a converged warp, also giving up once another
+// role of this CTA has aborted; the verdict is broadcast to the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const Params &p,
+                                          Shared &sh) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        const uint32_t a = smem_addr(bar);
+        if (!mbar_try_wait(a, parity)) {
+            const uint64_t t0 = global_timer_ns();
+            while (true) {
+                if (mbar_try_wait(a, parity)) break;
+                if (sh.abort_flag) {
+                    ok = 0;
+                    break;
+                }
+                if (global_timer_ns() - t0 > p.timeout_ns) {
+                    record_timeout(p.err);
+                    sh.abort_flag = 1;
+                    ok = 0;
+                    break;
+                }
+            }
+        }
+    }
+    return __shfl_sync(kAll, ok, 0) != 0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmSA,
+                     const __grid_constant__ CUtensorMap tmSB, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Shared &sh = *reinterpret_cast<Shared *>(smem + SMEM_BAR);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+    const int num_pairs = gridDim.x >> 1;
+    const int my_tiles =
+        pair < p.num_tiles ? (p.num_tiles - pair + num_pairs - 1) / num_pairs : 0;
+    const int num_k = p.K / BK;
+    const int kb4 = p.K / 64;  // 512-byte scale tiles per 128-row group
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&sh.full[s], 1);
+            mbar_init(&sh.empty[s], 1);
+        }
+        mbar_init(&sh.acc_full, 1);
+        mbar_init(&sh.acc_empty, 2 * kEpiWarps);
+        mbar_init(&sh.drain_mma, 1);
+        sh.abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmSA);
+        tma_prefetch_desc(&tmSB);
+    }
+    if (warp == 2) {
+        tmem_alloc_pair(&sh.tmem_base, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // both CTAs' barriers and TMEM exist before any remote use
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+    pdl_launch_dependents();
+    pdl_wait();
+
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer
+        const uint64_t pol = policy_evict_last();
+        const uint32_t full0 = mapa_shared(smem_addr(&sh.full[0]), 0);
+        int g = 0;
+        bool ok = !p.inject;
+        for (int t = 0; ok && t < my_tiles; ++t) {
+            int mt, nt;
+            tile_coords(pair + t * num_pairs, p.num_m_tiles, p.num_n_tiles, mt, nt);
+            const int arow = mt * PM + static_cast<int>(rank) * BM;
+            const int brow = nt * BN + static_cast<int>(rank) * BNH;
+            const int sfa_grp = mt * 2 + static_cast<int>(rank);
+            for (int kt = 0; kt < num_k; ++kt, ++g) {
+                const int s = g % STAGES;
+                if (!warp_wait(&sh.empty[s], ((g / STAGES) & 1) ^ 1, p, sh)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    if (leader) mbar_arrive_expect_tx(&sh.full[s], STAGE_TX);
+                    const uint32_t bar = full0 + static_cast<uint32_t>(s) * 8u;
+                    tma_load_2d_pair(smem + SMEM_A + s * A_BYTES, &tmA, bar, kt * (BK / 2), arow,
+                                     pol);
+                    tma_load_2d_pair(smem + SMEM_B + s * B_BYTES, &tmB, bar, kt * (BK / 2), brow,
+                                     pol);
+                    // scale rows of 256 B: group grp, stage kt starts at row
+                    // (grp * kb4 + 4 kt) * 2; groups past the array read as 0
+                    tma_load_2d_pair(smem + SMEM_SFA + s * SFA_BYTES, &tmSA, bar, 0,
+                                     (sfa_grp * kb4 + kt * 4) * 2, pol);
+                    tma_load_2d_pair(smem + SMEM_SFB + s * SFB_BYTES, &tmSB, bar, 0,
+                                     (nt * 2 * kb4 + kt * 4) * 2, pol);
+                    tma_load_2d_pair(smem + SMEM_SFB + s * SFB_BYTES + SFB_BYTES / 2, &tmSB, bar,
+                                     0, ((nt * 2 + 1) * kb4 + kt * 4) * 2, pol);
+                }
+                __syncwarp();
+            }
+        }
+        if (ok) {
+            // the last releases multicast to this CTA land before it exits
+            for (int s = 0; s < STAGES && s < g; ++s) {
+                const int fills = (g - s + STAGES - 1) / STAGES;
+                if (!warp_wait(&sh.empty[s], (fills - 1) & 1, p, sh)) break;
+            }
+        }
+        if (!ok && !p.inject && leader && lane == 0) {
+            // let loads already issued land before the CTA exits
+            for (int s = 0; s < STAGES && s < g; ++s) {
+                const int fills = (g - s + STAGES - 1) / STAGES;
+                mbar_wait(&sh.full[s], (fills - 1) & 1, p.timeout_ns);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1 && leader) {
+        // ------------------------------------------- MMA issuer (rank 0)
+        constexpr uint32_t idesc = idesc_mxf4nvf4(PM, BN);
+        int g = 0, it = 0;
+        bool ok = true;
+        for (int t = 0; ok && t < my_tiles; ++t, ++it) {
+            if (!warp_wait(&sh.acc_empty, (it & 1) ^ 1, p, sh)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int kt = 0; kt < num_k; ++kt, ++g) {
+                const int s = g % STAGES;
+                if (!warp_wait(&sh.full[s], (g / STAGES) & 1, p, sh)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // scales shared -> TMEM (both CTAs), ordered before the MMAs
+                // that read them by issue order from this thread
+                const uint32_t sf_a = tmem + SF_COL + s * SF_COLS_PER_STAGE;
+                const uint32_t sf_b = sf_a + 16;
+                const uint32_t sfa_smem = smem_addr(smem + SMEM_SFA + s * SFA_BYTES);
+                const uint32_t sfb_smem = smem_addr(smem + SMEM_SFB + s * SFB_BYTES);
+#pragma unroll
+                for (int j = 0; j < MMAS_PER_STAGE; ++j)
+                    sf_copy3_pair_elect(sf_a + j * 4, sf_b + j * 8, sdesc_sf(sfa_smem + j * SF_TILE),
+                                        sdesc_sf(sfb_smem + j * SF_TILE),
+                                        sdesc_sf(sfb_smem + SFB_BYTES / 2 + j * SF_TILE));
+                const uint32_t a_smem = smem_addr(smem + SMEM_A + s * A_BYTES);
+                const uint32_t b_smem = smem_addr(smem + SMEM_B + s * B_BYTES);
+#pragma unroll
+                for (int j = 0; j < MMAS_PER_STAGE; ++j)
+                    mma_mxf4nvf4_pair_elect(tmem + ACC_COL, sdesc_sw128(a_smem + j * 32),
+                                            sdesc_sw128(b_smem + j * 32), idesc, sf_a + j * 4,
+                                            sf_b + j * 8, (kt | j) != 0);
+                tc_commit_pair_mc_elect(&sh.empty[s], kPairMask);
+            }
+            if (ok) tc_commit_pair_mc_elect(&sh.acc_full, kPairMask);
+        }
+        if (!ok) {
+            // MMAs already issued must complete before TMEM is released
+            tc_commit_pair_mc_elect(&sh.drain_mma, 0x1);
+            if (lane == 0) mbar_wait(&sh.drain_mma, 0, p.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp >= kFirstEpiWarp) {
+        // -------------------------------------------------------- epilogue
+        const int quarter = warp & 3;
+        const int half = (warp - kFirstEpiWarp) >> 2;  // which 128 columns
+        const float alpha = __fmul_rn(*p.g_a, *p.g_b);
+        const uint32_t acc_empty0 = mapa_shared(smem_addr(&sh.acc_empty), 0);
+        int it = 0;
+        for (int t = 0; t < my_tiles; ++t, ++it) {
+            if (!warp_wait(&sh.acc_full, it & 1, p, sh)) break;
+            tc_fence_after();
+            int mt, nt;
+            tile_coords(pair + t * num_pairs, p.num_m_tiles, p.num_n_tiles, mt, nt);
+            const uint32_t t_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + ACC_COL +
+                                    static_cast<uint32_t>(half * 128);
+            uint32_t packed[64];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_base + c * 32, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    packed[c * 16 + i] = pack_bf16x2(__uint_as_float(r[2 * i]) * alpha,
+                                                     __uint_as_float(r[2 * i + 1]) * alpha);
+            }
+            // accumulator drained into registers: release it to rank 0
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_empty0);
+
+            const int row = mt * PM + static_cast<int>(rank) * BM + quarter * 32 + lane;
+            const int n0 = nt * BN + half * 128;
+            if (row < p.M) {
+                uint16_t *yrow = p.Y + static_cast<int64_t>(row) * p.ldy;
+                if (p.y_vec && n0 + 128 <= p.N) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(yrow + n0);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                            packed[4 * i + 3]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) {
+                        const int n = n0 + 2 * i;
+                        if (n < p.N) yrow[n] = static_cast<uint16_t>(packed[i] & 0xFFFFu);
+                        if (n + 1 < p.N) yrow[n + 1] = static_cast<uint16_t>(packed[i] >> 16);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // neither CTA leaves while the other may address it
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+int gemm_use_pair() {
+    static int use = -1;
+    if (use < 0) {
+        const char *env = getenv("NVFP4_GEMM_PAIR");
+        use = (env && env[0] == '0' && env[1] == 0) ? 0 : 1;
+    }
+    return use;
+}
+
+cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
+    if (a.M == 0 || a.N == 0) return cudaSuccess;
+    static int max_clusters = -1;
+    if (max_clusters < 0) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
+        max_clusters = launch_cfg().num_sms / 2;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * max_clusters, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = SMEM_ALLOC;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel, &cfg) == cudaSuccess && n > 0 &&
+            n < max_clusters)
+            max_clusters = n;
+    }
+    const int64_t sf_rows_a = (a.M + 127) / 128 * (a.K / 16) * 128 / SF_ROW;
+    const int64_t sf_rows_b = (a.N + 127) / 128 * (a.K / 16) * 128 / SF_ROW;
+    CUtensorMap tmA, tmB, tmSA, tmSB;
+    if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Aq, a.K / 2, a.M, a.K / 2, 128u, BM,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Bq, a.K / 2, a.N, a.K / 2, 128u, BNH,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_2d(&tmSA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.As, SF_ROW, sf_rows_a, SF_ROW,
+                     SF_ROW, SFA_BYTES / SF_ROW, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map_2d(&tmSB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Bs, SF_ROW, sf_rows_b, SF_ROW,
+                     SF_ROW, (SFB_BYTES / 2) / SF_ROW, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    Params p;
+    p.g_a = a.g_a;
+    p.g_b = a.g_b;
+    p.Y = a.Y;
+    p.ldy = a.ldy;
+    p.M = static_cast<int>(a.M);
+    p.N = static_cast<int>(a.N);
+    p.K = static_cast<int>(a.K);
+    p.num_m_tiles = static_cast<int>((a.M + PM - 1) / PM);
+    p.num_n_tiles = static_cast<int>((a.N + BN - 1) / BN);
+    p.num_tiles = p.num_m_tiles * p.num_n_tiles;
+    p.y_vec = (a.ldy % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.Y) & 15) == 0);
+    p.inject = debug_state().inject;
+    p.timeout_ns = debug_state().timeout_ns;
+    p.err = device_error_word();
+    if (p.err == nullptr) return cudaErrorInvalidSymbol;
+    const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_ALLOC;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_pair_kernel, tmA, tmB, tmSA, tmSB, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -32,6 +32,7 @@
 #include <cstring>
 
 #include "internal.h"
+#include "tensor_map.h"
 #include "ptx.cuh"
 #include "quant_math.cuh"
 
@@ -375,40 +376,6 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, CPS>::THREADS, CPS)
     }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn sk_encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
-bool sk_map(CUtensorMap *map, CUtensorMapDataType type, const void *ptr, uint64_t inner,
-            uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
-            CUtensorMapSwizzle swz) {
-    EncodeTiledFn enc = sk_encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {box_inner, box_rows};
-    cuuint32_t estr[2] = {1u, 1u};
-    return enc(map, type, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int NX, int XR, bool FUSED, int CPS>
 cudaError_t launch_sk(const SkinnyArgs &a, cudaStream_t st) {
     using C = SkCfg<NX, XR, FUSED, CPS>;
@@ -420,15 +387,15 @@ cudaError_t launch_sk(const SkinnyArgs &a, cudaStream_t st) {
         attr = true;
     }
     CUtensorMap tmW, tmX;
-    if (!sk_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wq, a.K / 2, a.N, a.K / 2, 128, SK_BM,
+    if (!make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wq, a.K / 2, a.N, a.K / 2, 128, SK_BM,
                 CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     if (FUSED) {
-        if (!sk_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.X, a.K, a.M, a.ldx * 2, SK_BK, XR,
+        if (!make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.X, a.K, a.M, a.ldx * 2, SK_BK, XR,
                     CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     } else {
-        if (!sk_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Xq, a.K / 2, a.M, a.K / 2, 128, XR,
+        if (!make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Xq, a.K / 2, a.M, a.K / 2, 128, XR,
                     CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }

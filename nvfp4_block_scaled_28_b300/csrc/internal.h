@@ -70,6 +70,11 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st);
+// The same GEMM on CTA pairs (tcgen05 cta_group::2), 256 x 256 tiles.
+cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st);
+// Kernel for M > 128: 1 = CTA pairs (default), 0 = single-CTA tiles
+// (NVFP4_GEMM_PAIR=0 selects it, for comparison).
+int gemm_use_pair();
 
 // Skinny-M GEMM (Y^T = W X^T, weights as the 128-row MMA operand).
 constexpr int64_t kSkinnyMaxM = 128;       // activation rows it handles

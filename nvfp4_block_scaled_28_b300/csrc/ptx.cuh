@@ -398,6 +398,22 @@ __device__ __forceinline__ void mma_bf16_elect(uint32_t d_tmem, uint64_t adesc, 
         : "memory");
 }
 
+// One MMA's scales under a single elect: the A tile to columns
+// [sfa, sfa + 4), the two 128-row B tiles to [sfb, sfb + 4) and
+// [sfb + 4, sfb + 8), each a 32x128b.warpx4 copy.
+__device__ __forceinline__ void sf_copy3_elect(uint32_t sfa, uint32_t sfb, uint64_t da,
+                                               uint64_t db0, uint64_t db1) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .b32 t;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "add.u32 t, %1, 4;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %2;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%1], %3;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [t], %4;\n\t}" ::"r"(sfa),
+        "r"(sfb), "l"(da), "l"(db0), "l"(db1)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_cp_32x128b_x4_elect(uint32_t taddr, uint64_t sdesc) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
@@ -450,6 +466,99 @@ __device__ __forceinline__ void tc_commit_elect(uint64_t *bar) {
         : "memory");
 }
 
+// ------------------------------------------------ CTA pair (cta_group::2)
+// The two CTAs of a cluster of 2 act as one tensor-core unit: rank 0 issues
+// the MMAs and scale copies for both, each CTA holds its half of A (rows),
+// of B (columns) and of the accumulator (rows) at the same shared / TMEM
+// offsets.
+
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// Arrive on an mbarrier of any CTA of the cluster (shared::cluster address).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                     cluster_addr)
+                 : "memory");
+}
+
+// 2-D tiled load into this CTA's shared memory whose bytes are counted on an
+// mbarrier of either CTA of the pair (shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".cta_group::2.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+// TMEM allocation for both CTAs of the pair: one warp of each CTA executes it.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// One MMA's scales for both CTAs (each copies from its own shared memory at
+// the same offsets): A tile -> [sfa, sfa + 4), B row groups -> [sfb, sfb + 4)
+// and [sfb + 4, sfb + 8).
+__device__ __forceinline__ void sf_copy3_pair_elect(uint32_t sfa, uint32_t sfb, uint64_t da,
+                                                    uint64_t db0, uint64_t db1) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .b32 t;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "add.u32 t, %1, 4;\n\t"
+        "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %2;\n\t"
+        "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%1], %3;\n\t"
+        "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], %4;\n\t}" ::"r"(sfa),
+        "r"(sfb), "l"(da), "l"(db0), "l"(db1)
+        : "memory");
+}
+
+// D (+)= A x B^T over the pair: M = 256 (128 rows per CTA), N up to 256
+// (N / 2 rows of B in each CTA), K = 64, block scales from TMEM.
+__device__ __forceinline__ void mma_mxf4nvf4_pair_elect(uint32_t d_tmem, uint64_t adesc,
+                                                        uint64_t bdesc, uint32_t idesc,
+                                                        uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
+// Arrive (once) on the mbarrier at `bar`'s offset in each CTA of `mask` when
+// every tcgen05 operation this thread issued before has completed.
+__device__ __forceinline__ void tc_commit_pair_mc_elect(uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;\n\t}" ::"r"(smem_addr(bar)),
+        "h"(mask)
+        : "memory");
+}
+
 // Copy a 32-row x 16-byte shared tile to TMEM, replicated into all four
 // 32-lane quarters (4 columns of 32 bits).
 __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
@@ -478,6 +587,15 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
           "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// 32 lanes x 64 consecutive 32-bit columns: thread i gets lane (base + i).
+__device__ __forceinline__ void tmem_ld_32x32b_x64(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
         : "r"(taddr)
         : "memory");
 }
