@@ -16,18 +16,24 @@
 // Persistent kernel, clusters of 2 CTAs (one per SM), 256 x 256 output
 // tiles per pair, K in stages of 256 (4 MMAs of K = 64). Warp roles, in
 // both CTAs unless noted:
-//   warp 0    TMA producer: this CTA's A rows, B rows, A scales and all 256
-//             B-row scales of the tile for stage g, into a STAGES-deep ring.
-//             Every load of both CTAs is counted on the full barrier of
-//             rank 0, which therefore sees the whole stage.
-//   warp 1    (rank 0) MMA issuer: per stage, 12 scale copies shared -> TMEM
-//             and 4 MMAs, each one instruction for both CTAs; the release
-//             of the stage and of the finished accumulator is multicast to
-//             both CTAs' barriers.
-//   warp 2    allocates and frees TMEM (jointly with the partner CTA).
+//   warp 0    TMA producer of this CTA's 128 A rows and 128 B rows of stage g
+//             into a STAGES-deep ring;
+//   warp 2    allocates / frees TMEM (jointly with the partner CTA), and is
+//             the TMA producer of the stage's scales: this CTA's A scales
+//             and all 256 B-row scales of the tile (one 3-D box). Every load
+//             of both CTAs is counted on the full barrier of rank 0;
+//   warp 1    (rank 0) MMA issuer: per stage and K = 64 step, 3 scale
+//             copies shared -> TMEM and 1 MMA, each one instruction for both
+//             CTAs; the release of the stage and of the finished
+//             accumulator is multicast to both CTAs' barriers;
 //   warps 3-10 epilogue over this CTA's 128 accumulator rows: tcgen05.ld,
 //             release to rank 0's accumulator barrier (16 arrivals: 8 warps
 //             x 2 CTAs), scale by g_a g_b, round to bfloat16, store.
+// The copies stay in the MMA thread: a separate copy warp synchronised by
+// tcgen05.commit let the partner SM's MMA read a scale replica before its
+// copy had landed (wrong products in one TMEM lane quarter); from one
+// thread, copy and MMA reach both SMs in issue order. Two producer warps
+// halve the TMA issue work per warp.
 // Every mbarrier wait is bounded in time; a wait that runs out records a
 // timeout in the device error word and the roles of both CTAs leave.
 #include <cuda.h>
@@ -153,6 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSA,
                      const __grid_constant__ CUtensorMap tmSB, const Params p) {
+    // tmSA: A scales as rows of 256 B (8 rows per stage); tmSB: B scales as
+    // {256 B, rows of a 128-row group, group} (8 rows x 2 groups per stage)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -196,8 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_launch_dependents();
     pdl_wait();
 
-    if (warp == 0) {
-        // ---------------------------------------------------- TMA producer
+    if (warp == 0 || warp == 2) {
+        // --------------------------------------- TMA producers (A/B; scales)
+        const bool scales = warp == 2;
         const uint64_t pol = policy_evict_last();
         const uint32_t full0 = mapa_shared(smem_addr(&sh.full[0]), 0);
         int g = 0;
@@ -207,7 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tile_coords(pair + t * num_pairs, p.num_m_tiles, p.num_n_tiles, mt, nt);
             const int arow = mt * PM + static_cast<int>(rank) * BM;
             const int brow = nt * BN + static_cast<int>(rank) * BNH;
-            const int sfa_grp = mt * 2 + static_cast<int>(rank);
+            // scale rows of 256 B: group grp, stage kt starts at row
+            // (grp * kb4 + 4 kt) * 2; groups past the array read as 0
+            const int sfa_row = (mt * 2 + static_cast<int>(rank)) * kb4 * 2;
             for (int kt = 0; kt < num_k; ++kt, ++g) {
                 const int s = g % STAGES;
                 if (!warp_wait(&sh.empty[s], ((g / STAGES) & 1) ^ 1, p, sh)) {
@@ -215,20 +226,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 if (lane == 0) {
-                    if (leader) mbar_arrive_expect_tx(&sh.full[s], STAGE_TX);
                     const uint32_t bar = full0 + static_cast<uint32_t>(s) * 8u;
-                    tma_load_2d_pair(smem + SMEM_A + s * A_BYTES, &tmA, bar, kt * (BK / 2), arow,
-                                     pol);
-                    tma_load_2d_pair(smem + SMEM_B + s * B_BYTES, &tmB, bar, kt * (BK / 2), brow,
-                                     pol);
-                    // scale rows of 256 B: group grp, stage kt starts at row
-                    // (grp * kb4 + 4 kt) * 2; groups past the array read as 0
-                    tma_load_2d_pair(smem + SMEM_SFA + s * SFA_BYTES, &tmSA, bar, 0,
-                                     (sfa_grp * kb4 + kt * 4) * 2, pol);
-                    tma_load_2d_pair(smem + SMEM_SFB + s * SFB_BYTES, &tmSB, bar, 0,
-                                     (nt * 2 * kb4 + kt * 4) * 2, pol);
-                    tma_load_2d_pair(smem + SMEM_SFB + s * SFB_BYTES + SFB_BYTES / 2, &tmSB, bar,
-                                     0, ((nt * 2 + 1) * kb4 + kt * 4) * 2, pol);
+                    if (!scales) {
+                        if (leader) mbar_arrive_expect_tx(&sh.full[s], STAGE_TX);
+                        tma_load_2d_pair(smem + SMEM_A + s * A_BYTES, &tmA, bar, kt * (BK / 2),
+                                         arow, pol);
+                        tma_load_2d_pair(smem + SMEM_B + s * B_BYTES, &tmB, bar, kt * (BK / 2),
+                                         brow, pol);
+                    } else {
+                        tma_load_2d_pair(smem + SMEM_SFA + s * SFA_BYTES, &tmSA, bar, 0,
+                                         sfa_row + kt * 8, pol);
+                        tma_load_3d_pair(smem + SMEM_SFB + s * SFB_BYTES, &tmSB, bar, 0, kt * 8,
+                                         nt * 2, pol);
+                    }
                 }
                 __syncwarp();
             }
@@ -240,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!warp_wait(&sh.empty[s], (fills - 1) & 1, p, sh)) break;
             }
         }
-        if (!ok && !p.inject && leader && lane == 0) {
+        if (!ok && !p.inject && leader && lane == 0 && !scales) {
             // let loads already issued land before the CTA exits
             for (int s = 0; s < STAGES && s < g; ++s) {
                 const int fills = (g - s + STAGES - 1) / STAGES;
@@ -266,24 +276,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                // scales shared -> TMEM (both CTAs), ordered before the MMAs
-                // that read them by issue order from this thread
+                // per K = 64 step: the step's scales shared -> TMEM for both
+                // CTAs, then the MMA that reads them, in issue order
                 const uint32_t sf_a = tmem + SF_COL + s * SF_COLS_PER_STAGE;
                 const uint32_t sf_b = sf_a + 16;
                 const uint32_t sfa_smem = smem_addr(smem + SMEM_SFA + s * SFA_BYTES);
                 const uint32_t sfb_smem = smem_addr(smem + SMEM_SFB + s * SFB_BYTES);
-#pragma unroll
-                for (int j = 0; j < MMAS_PER_STAGE; ++j)
-                    sf_copy3_pair_elect(sf_a + j * 4, sf_b + j * 8, sdesc_sf(sfa_smem + j * SF_TILE),
-                                        sdesc_sf(sfb_smem + j * SF_TILE),
-                                        sdesc_sf(sfb_smem + SFB_BYTES / 2 + j * SF_TILE));
                 const uint32_t a_smem = smem_addr(smem + SMEM_A + s * A_BYTES);
                 const uint32_t b_smem = smem_addr(smem + SMEM_B + s * B_BYTES);
 #pragma unroll
                 for (int j = 0; j < MMAS_PER_STAGE; ++j)
-                    mma_mxf4nvf4_pair_elect(tmem + ACC_COL, sdesc_sw128(a_smem + j * 32),
+                    sf_copy3_mma_pair_elect(tmem + ACC_COL, sdesc_sw128(a_smem + j * 32),
                                             sdesc_sw128(b_smem + j * 32), idesc, sf_a + j * 4,
-                                            sf_b + j * 8, (kt | j) != 0);
+                                            sf_b + j * 8, (kt | j) != 0,
+                                            sdesc_sf(sfa_smem + j * SF_TILE),
+                                            sdesc_sf(sfb_smem + j * SF_TILE),
+                                            sdesc_sf(sfb_smem + SFB_BYTES / 2 + j * SF_TILE));
                 tc_commit_pair_mc_elect(&sh.empty[s], kPairMask);
             }
             if (ok) tc_commit_pair_mc_elect(&sh.acc_full, kPairMask);
@@ -391,8 +399,9 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
             n < max_clusters)
             max_clusters = n;
     }
-    const int64_t sf_rows_a = (a.M + 127) / 128 * (a.K / 16) * 128 / SF_ROW;
-    const int64_t sf_rows_b = (a.N + 127) / 128 * (a.K / 16) * 128 / SF_ROW;
+    const int64_t kb4 = a.K / 64;
+    const int64_t sf_rows_a = (a.M + 127) / 128 * kb4 * 2;  // 256-byte rows
+    const int64_t groups_b = (a.N + 127) / 128;
     CUtensorMap tmA, tmB, tmSA, tmSB;
     if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Aq, a.K / 2, a.M, a.K / 2, 128u, BM,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -400,8 +409,8 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map_2d(&tmSA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.As, SF_ROW, sf_rows_a, SF_ROW,
                      SF_ROW, SFA_BYTES / SF_ROW, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map_2d(&tmSB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Bs, SF_ROW, sf_rows_b, SF_ROW,
-                     SF_ROW, (SFB_BYTES / 2) / SF_ROW, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !make_map_3d(&tmSB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Bs, SF_ROW, kb4 * 2, groups_b, SF_ROW,
+                     kb4 * SF_TILE, SF_ROW, (SFB_BYTES / 2) / SF_ROW, 2))
         return cudaErrorInvalidValue;
     Params p;
     p.g_a = a.g_a;

@@ -498,6 +498,19 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m
         : "memory");
 }
 
+// 3-D tiled load into this CTA's shared memory, bytes counted on an mbarrier
+// of either CTA of the pair.
+__device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y,
+                                                 int32_t z, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".cta_group::2.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z),
+        "l"(policy)
+        : "memory");
+}
+
 // TMEM allocation for both CTAs of the pair: one warp of each CTA executes it.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -544,6 +557,41 @@ __device__ __forceinline__ void mma_mxf4nvf4_pair_elect(uint32_t d_tmem, uint64_
         "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
         " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
+// One K = 64 step of the pair MMA with its scales, under a single elect:
+// the three scale copies (as sf_copy3_pair_elect) then the MMA reading
+// them. Copies and MMA from one thread reach both SMs' tensor cores in
+// issue order.
+__device__ __forceinline__ void sf_copy3_mma_pair_elect(uint32_t d_tmem, uint64_t adesc,
+                                                        uint64_t bdesc, uint32_t idesc,
+                                                        uint32_t sfa, uint32_t sfb,
+                                                        uint32_t accumulate, uint64_t da,
+                                                        uint64_t db0, uint64_t db1) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 t;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "add.u32 t, %6, 4;\n\t"
+        "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%5], %7;\n\t"
+        "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%6], %8;\n\t"
+        "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], %9;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb), "l"(da),
+        "l"(db0), "l"(db1)
+        : "memory");
+}
+
+// Arrive (once) on this CTA's mbarrier when every tcgen05 operation this
+// thread issued before has completed (pair form).
+__device__ __forceinline__ void tc_commit_pair_elect(uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            smem_addr(bar))
         : "memory");
 }
 

@@ -44,4 +44,19 @@ bool make_map_2d(CUtensorMap *map, CUtensorMapDataType type, const void *ptr, ui
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_map_3d(CUtensorMap *map, CUtensorMapDataType type, const void *ptr, uint64_t inner,
+                 uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2, uint32_t box_inner,
+                 uint32_t box1, uint32_t box2) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {inner, d1, d2};
+    cuuint64_t strides[2] = {s1, s2};
+    cuuint32_t box[3] = {box_inner, box1, box2};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(map, type, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 }  // namespace nvfp4
