@@ -40,6 +40,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdlib>
+#include <cstring>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -79,12 +80,16 @@ constexpr int SMEM_A = 0;
 constexpr int SMEM_B = SMEM_A + STAGES * A_BYTES;
 constexpr int SMEM_SFA = SMEM_B + STAGES * B_BYTES;
 constexpr int SMEM_SFB = SMEM_SFA + STAGES * SFA_BYTES;
-constexpr int SMEM_BAR = SMEM_SFB + STAGES * SFB_BYTES;
+constexpr int EPI_CHUNK = 64;              // output columns per TMA store (128 B rows)
+constexpr int EPI_BYTES = 32 * EPI_CHUNK * 2;  // one warp's 32 rows x 64 columns of bfloat16
+constexpr int SMEM_EPI = SMEM_SFB + STAGES * SFB_BYTES;  // 1024-aligned staging, one per warp
+constexpr int SMEM_BAR = SMEM_EPI + kEpiWarps * EPI_BYTES;
 constexpr int SMEM_USED = SMEM_BAR + 256;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // room to align the base to 1024
 
 static_assert(SF_COL + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+static_assert(SMEM_EPI % 1024 == 0 && EPI_BYTES % 1024 == 0, "128-byte swizzle atoms");
 
 struct Params {
     const float *g_a;
@@ -96,6 +101,7 @@ struct Params {
     int num_n_tiles;     // 256-column tiles
     int num_tiles;
     int y_vec;           // rows of Y start 16-byte aligned: 16-byte stores
+    int y_tma;           // Y written by TMA stores (rows 16-byte aligned, map valid)
     int inject;          // 1: the producers issue nothing (bounded-wait test)
     uint64_t timeout_ns;
     unsigned int *err;   // device error word
@@ -158,7 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSA,
-                     const __grid_constant__ CUtensorMap tmSB, const Params p) {
+                     const __grid_constant__ CUtensorMap tmSB,
+                     const __grid_constant__ CUtensorMap tmY, const Params p) {
     // tmSA: A scales as rows of 256 B (8 rows per stage); tmSB: B scales as
     // {256 B, rows of a 128-row group, group} (8 rows x 2 groups per stage)
     extern __shared__ uint8_t smem_raw[];
@@ -191,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmSA);
         tma_prefetch_desc(&tmSB);
+        if (p.y_tma) tma_prefetch_desc(&tmY);
     }
     if (warp == 2) {
         tmem_alloc_pair(&sh.tmem_base, TMEM_COLS);
@@ -332,9 +340,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(acc_empty0);
 
-            const int row = mt * PM + static_cast<int>(rank) * BM + quarter * 32 + lane;
+            const int row0 = mt * PM + static_cast<int>(rank) * BM + quarter * 32;
+            const int row = row0 + lane;
             const int n0 = nt * BN + half * 128;
-            if (row < p.M) {
+            if (p.y_tma) {
+                // 64-column chunks through this warp's staging tile (128-byte
+                // swizzle: 16-byte piece k of row r sits at piece k ^ (r % 8)),
+                // written out by one TMA store each; rows >= M and columns
+                // >= N are clipped by the tensor map
+                uint8_t *stage = smem + SMEM_EPI + (warp - kFirstEpiWarp) * EPI_BYTES;
+#pragma unroll
+                for (int c = 0; c < 128 / EPI_CHUNK; ++c) {
+                    if (lane == 0) bulk_wait_read_all();  // previous store has read the tile
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        *reinterpret_cast<uint4 *>(stage + lane * 128 + ((k ^ (lane & 7)) * 16)) =
+                            make_uint4(packed[c * 32 + 4 * k], packed[c * 32 + 4 * k + 1],
+                                       packed[c * 32 + 4 * k + 2], packed[c * 32 + 4 * k + 3]);
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmY, stage, n0 + c * EPI_CHUNK, row0);
+                        bulk_commit_group();
+                    }
+                }
+            } else if (row < p.M) {
                 uint16_t *yrow = p.Y + static_cast<int64_t>(row) * p.ldy;
                 if (p.y_vec && n0 + 128 <= p.N) {
                     uint4 *dst = reinterpret_cast<uint4 *>(yrow + n0);
@@ -352,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        if (p.y_tma && lane == 0) bulk_wait_all();
         __syncwarp();
     }
 
@@ -412,6 +444,11 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
         !make_map_3d(&tmSB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Bs, SF_ROW, kb4 * 2, groups_b, SF_ROW,
                      kb4 * SF_TILE, SF_ROW, (SFB_BYTES / 2) / SF_ROW, 2))
         return cudaErrorInvalidValue;
+    CUtensorMap tmY;
+    const bool y_vec = (a.ldy % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.Y) & 15) == 0);
+    const bool y_tma = y_vec && make_map_2d(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.Y, a.N, a.M,
+                                            a.ldy * 2, EPI_CHUNK, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!y_tma) memset(&tmY, 0, sizeof(tmY));
     Params p;
     p.g_a = a.g_a;
     p.g_b = a.g_b;
@@ -423,7 +460,8 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     p.num_m_tiles = static_cast<int>((a.M + PM - 1) / PM);
     p.num_n_tiles = static_cast<int>((a.N + BN - 1) / BN);
     p.num_tiles = p.num_m_tiles * p.num_n_tiles;
-    p.y_vec = (a.ldy % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.Y) & 15) == 0);
+    p.y_vec = y_vec;
+    p.y_tma = y_tma;
     p.inject = debug_state().inject;
     p.timeout_ns = debug_state().timeout_ns;
     p.err = device_error_word();
@@ -442,7 +480,7 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_pair_kernel, tmA, tmB, tmSA, tmSB, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_pair_kernel, tmA, tmB, tmSA, tmSB, tmY, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
