@@ -213,7 +213,8 @@ nvfp4_status nvfp4_gemm(const uint8_t *Aq, const uint8_t *As, const float *g_a, 
                                      : launch_gemm(a, static_cast<cudaStream_t>(stream)));
 }
 
-// nvfp4_linear workspace: [g_x | amax partials] header, X codes, X scales.
+// nvfp4_linear workspace: [g_x, barrier counter | amax partials] header,
+// X codes, X scales.
 constexpr size_t kLinearHeader = 256 + sizeof(uint32_t) * kMaxAmaxPartials;
 
 size_t nvfp4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int mode) {
@@ -261,9 +262,10 @@ nvfp4_status nvfp4_linear(const void *X, int64_t M, int64_t K, int64_t ldx, cons
     // every N-tile's producer would cost more than one quantize pass)
     cudaError_t e;
     if (g_x == nullptr) {
-        // amax partials -> quantize (reduces g_x into the slot) -> GEMM, each
-        // a programmatic dependent of the one before
-        e = launch_quantize_dynamic(Xh, M, K, ldx, partials, gx_slot, xq, xs, st);
+        // amax partials, grid barrier and quantization in one launch (g_x
+        // into the slot), then the GEMM as its programmatic dependent
+        unsigned int *counter = reinterpret_cast<unsigned int *>(ws + 64);
+        e = launch_quantize_fused(Xh, M, K, ldx, partials, counter, gx_slot, xq, xs, st);
         g_x = gx_slot;
     } else {
         e = launch_quantize(Xh, M, K, ldx, g_x, xq, xs, NVFP4_SF_MMA_128x4, st);

@@ -52,6 +52,13 @@ cudaError_t launch_quantize_dynamic(const uint16_t *X, int64_t rows, int64_t col
                                     uint32_t *partials, float *g_out, uint8_t *q, uint8_t *sf,
                                     cudaStream_t st);
 
+// The same in one cooperative launch: amax partials, a grid-wide barrier on
+// `counter` (zeroed by the launcher), then quantization; the second read
+// of X comes from L2 when X fits there.
+cudaError_t launch_quantize_fused(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
+                                  uint32_t *partials, unsigned int *counter, float *g_out,
+                                  uint8_t *q, uint8_t *sf, cudaStream_t st);
+
 // Launch configuration for kernels that take part in programmatic
 // dependent launch chains.
 cudaLaunchAttribute pdl_attribute();

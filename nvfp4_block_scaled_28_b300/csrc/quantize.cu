@@ -205,6 +205,125 @@ __global__ void __launch_bounds__(kThreads) quantize_dynamic_kernel(
     }
 }
 
+// Dynamic activation quantization in one launch: every CTA reduces the amax
+// of its share of X into partials[blockIdx.x], the grid meets at a barrier
+// (all CTAs are co-resident: cooperative launch), then every CTA reduces
+// the same partials to the same g (integer max, one IEEE division) and
+// quantizes into the tensor-core scale layout. The second read of X hits L2
+// when X fits there. `counter` is zero at launch. The barrier wait is
+// bounded: on timeout the CTA records it in the error word and goes on.
+__global__ void __launch_bounds__(kThreads) quantize_fused_kernel(
+    const uint16_t *__restrict__ X, uint32_t rows, uint32_t rows_pad, uint32_t kbpr, uint64_t ldx,
+    FastDiv div_kbpr, uint32_t vpr, FastDiv div_vpr, uint32_t *partials, unsigned int *counter,
+    float *g_out, uint8_t *__restrict__ q, uint8_t *__restrict__ sf, uint64_t timeout_ns,
+    unsigned int *err) {
+    pdl_launch_dependents();
+    pdl_wait();  // X may come from the previous kernel
+    // ---- amax of this CTA's share (16-byte vectors, 4 in flight)
+    {
+        const uint32_t total = rows * vpr;
+        const uint32_t stride = gridDim.x * blockDim.x;
+        const uint32_t m = 0x7FFF7FFFu;
+        uint32_t acc = 0;
+        uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+        for (; i + 7 * stride < total; i += 8 * stride) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t j = i + u * stride;
+                const uint32_t r = div_vpr.div(j), c = j - r * vpr;
+                v[u] = ld_stream(reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull));
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                acc = max_u16x2(acc, max_u16x2(max_u16x2(v[u].x & m, v[u].y & m),
+                                               max_u16x2(v[u].z & m, v[u].w & m)));
+        }
+        for (; i < total; i += stride) {
+            const uint32_t r = div_vpr.div(i), c = i - r * vpr;
+            const uint4 v = ld_stream(reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull));
+            acc = max_u16x2(acc,
+                            max_u16x2(max_u16x2(v.x & m, v.y & m), max_u16x2(v.z & m, v.w & m)));
+        }
+        uint32_t a = max(acc & 0xFFFFu, acc >> 16);
+        a = __reduce_max_sync(0xFFFFFFFFu, a);
+        __shared__ uint32_t warp_max[kThreads / 32];
+        if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = a;
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            uint32_t b = threadIdx.x < kThreads / 32 ? warp_max[threadIdx.x] : 0u;
+            b = __reduce_max_sync(0xFFFFFFFFu, b);
+            if (threadIdx.x == 0) {
+                partials[blockIdx.x] = b;
+                __threadfence();
+                atomicAdd(counter, 1u);
+                // wait for every CTA's partial
+                const uint64_t t0 = global_timer_ns();
+                while (atomicAdd(counter, 0u) < gridDim.x) {
+                    if (global_timer_ns() - t0 > timeout_ns) {
+                        record_timeout(err);
+                        break;
+                    }
+                }
+                __threadfence();
+            }
+        }
+        __syncthreads();
+    }
+    // ---- g from all partials (the same value in every CTA)
+    __shared__ float g_sh;
+    if (threadIdx.x < 32) {
+        uint32_t b = 0;
+        for (uint32_t i = threadIdx.x; i < gridDim.x; i += 32)
+            b = max(b, *reinterpret_cast<volatile uint32_t *>(partials + i));
+        b = __reduce_max_sync(0xFFFFFFFFu, b);
+        if (threadIdx.x == 0) {
+            const float amax = __uint_as_float(b << 16);
+            g_sh = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+        }
+    }
+    __syncthreads();
+    const float g = g_sh;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+    // ---- quantize (padding rows of the last 128-row group get scale 0)
+    const uint32_t total = rows * kbpr;
+    const uint32_t total_pad = rows_pad * kbpr;
+    const uint32_t stride = gridDim.x * blockDim.x;
+    const uint32_t kb4 = kbpr >> 2;
+    // four blocks per thread per round, all loads issued before the math
+    constexpr int U = 4;
+    for (uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < total_pad; i0 += U * stride) {
+        uint4 va[U], vb[U];
+        uint32_t row[U], kb[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t i = i0 + u * stride;
+            row[u] = div_kbpr.div(i);
+            kb[u] = i - row[u] * kbpr;
+            va[u] = make_uint4(0, 0, 0, 0);
+            vb[u] = va[u];
+            if (i < total) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(X + row[u] * ldx + kb[u] * 16ull);
+                va[u] = ld_stream(src);
+                vb[u] = ld_stream(src + 1);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t i = i0 + u * stride;
+            if (i >= total_pad) break;
+            if (i >= total) {  // padding rows of the last 128-row group read 0
+                sf[sf_mma_offset(row[u], kb[u], kb4)] = 0;
+                continue;
+            }
+            uint32_t lo, hi;
+            const uint32_t S = quantize16(va[u], vb[u], g, lo, hi);
+            *reinterpret_cast<uint2 *>(q + static_cast<uint64_t>(i) * 8) = make_uint2(lo, hi);
+            sf[sf_mma_offset(row[u], kb[u], kb4)] = static_cast<uint8_t>(S);
+        }
+    }
+}
+
 // g = amax / (6 * 448), or 1 for an all-zero tensor; in place over the cell.
 __global__ void global_scale_finalize(uint32_t *cell) {
     const float amax = __uint_as_float(*cell << 16);
@@ -312,6 +431,43 @@ cudaError_t launch_quantize_dynamic(const uint16_t *X, int64_t rows, int64_t col
                               rows_pad, kbpr, static_cast<uint64_t>(ldx), FastDiv(kbpr),
                               static_cast<const uint32_t *>(partials),
                               static_cast<uint32_t>(n_partials), g_out, q, sf);
+}
+
+cudaError_t launch_quantize_fused(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
+                                  uint32_t *partials, unsigned int *counter, float *g_out,
+                                  uint8_t *q, uint8_t *sf, cudaStream_t st) {
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        int n = 0;
+        cudaError_t e =
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_fused_kernel, kThreads, 0);
+        if (e != cudaSuccess) return e;
+        per_sm = n < 1 ? 1 : (n > 8 ? 8 : n);
+    }
+    const uint32_t vpr = static_cast<uint32_t>(cols / 8);
+    const uint32_t kbpr = static_cast<uint32_t>(cols / 16);
+    const uint32_t rows_pad = static_cast<uint32_t>((rows + 127) / 128 * 128);
+    int grid = launch_cfg().num_sms * per_sm;
+    const int need = grid_for(static_cast<uint64_t>(rows_pad) * kbpr, 4);
+    if (need < grid) grid = need;
+    if (grid > kMaxAmaxPartials) grid = kMaxAmaxPartials;
+    cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(unsigned int), st);
+    if (e != cudaSuccess) return e;
+    unsigned int *err = device_error_word();
+    if (err == nullptr) return cudaErrorInvalidSymbol;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quantize_fused_kernel, X, static_cast<uint32_t>(rows),
+                              rows_pad, kbpr, static_cast<uint64_t>(ldx), FastDiv(kbpr), vpr,
+                              FastDiv(vpr), partials, counter, g_out, q, sf,
+                              debug_state().timeout_ns, err);
 }
 
 cudaError_t launch_sf_to_mma(const uint8_t *sf_rm, int64_t rows, int64_t K, uint8_t *sf_mma,
