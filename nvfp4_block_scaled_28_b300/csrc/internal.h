@@ -42,17 +42,11 @@ cudaError_t launch_quantize(const uint16_t *X, int64_t rows, int64_t cols, int64
                             const float *g, uint8_t *q, uint8_t *sf, int layout,
                             cudaStream_t st);
 
-// Activation quantization with a dynamic global scale as two kernels chained
-// by programmatic dependent launch: per-CTA partial amax into `partials`
-// (kMaxAmaxPartials words), then a quantizer whose CTAs each reduce the
-// partials to g (written to *g_out by CTA 0) and quantize into the
-// tensor-core scale layout (padding rows zeroed). No memset, no finalize.
+// Largest grid of the fused dynamic quantizer (one amax partial per CTA).
 constexpr int kMaxAmaxPartials = 2048;
-cudaError_t launch_quantize_dynamic(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
-                                    uint32_t *partials, float *g_out, uint8_t *q, uint8_t *sf,
-                                    cudaStream_t st);
 
-// The same in one cooperative launch: amax partials, a grid-wide barrier on
+// Activation quantization with a dynamic global scale g = amax / (6 * 448)
+// in one cooperative launch: amax partials, a grid-wide barrier on
 // `counter` (zeroed by the launcher), then quantization; the second read
 // of X comes from L2 when X fits there.
 cudaError_t launch_quantize_fused(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,

@@ -9,8 +9,8 @@
 //   S = E4M3_rne_satfinite((amax_block / 6) / g)
 //   r = 1 / (e4m3(S) * g)   (0 when S == 0)
 //   code = E2M1_rne_satfinite(x * r), sign bit = sign bit of x.
-// Every float step is one IEEE binary32 operation (explicit _rn intrinsics,
-// never contracted).
+// Every float step is one IEEE binary32 operation (explicit _rn intrinsics
+// or .rn instructions, never contracted).
 #pragma once
 
 #include <cstdint>
@@ -48,12 +48,29 @@ __device__ __forceinline__ uint32_t amax_bits16(uint4 a, uint4 b) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Two E2M1 codes (one byte, low element in the low nibble) of the bfloat16
+// pair w scaled by r: both products in one packed IEEE binary32 multiply
+// (mul.rn.f32x2: two round-to-nearest products, no flush), then one
+// round-to-nearest-even saturating conversion.
+__device__ __forceinline__ uint32_t codes2(uint32_t w, uint64_t rr) {
+    uint32_t out;
+    asm("{\n\t.reg .b32 l, h;\n\t.reg .b64 p, q;\n\t.reg .f32 x, y;\n\t.reg .b8 b;\n\t"
+        "shl.b32 l, %1, 16;\n\t"
+        "and.b32 h, %1, 0xFFFF0000;\n\t"
+        "mov.b64 p, {l, h};\n\t"
+        "mul.rn.f32x2 q, p, %2;\n\t"
+        "mov.b64 {x, y}, q;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b, y, x;\n\t"
+        "cvt.u32.u8 %0, b;\n\t}"
+        : "=r"(out)
+        : "r"(w), "l"(rr));
+    return out;
+}
+
 // Four E2M1 codes of the two bfloat16 pairs w0 (elements 0,1) and w1
 // (elements 2,3), packed little-end first.
-__device__ __forceinline__ uint32_t codes4(uint32_t w0, uint32_t w1, float r) {
-    uint32_t b0 = cvt_e2m1x2(__fmul_rn(bf16_lo(w0), r), __fmul_rn(bf16_hi(w0), r));
-    uint32_t b1 = cvt_e2m1x2(__fmul_rn(bf16_lo(w1), r), __fmul_rn(bf16_hi(w1), r));
-    return b0 | (b1 << 8);
+__device__ __forceinline__ uint32_t codes4(uint32_t w0, uint32_t w1, uint64_t rr) {
+    return codes2(w0, rr) | (codes2(w1, rr) << 8);
 }
 
 // Quantize one 16-element block held in (a, b). Returns the scale byte and
@@ -66,8 +83,9 @@ __device__ __forceinline__ uint32_t quantize16(uint4 a, uint4 b, float g, uint32
     const float s = e4m3_to_f32(S);
     const float denom = __fmul_rn(s, g);
     const float r = denom > 0.0f ? __frcp_rn(denom) : 0.0f;
-    lo = codes4(a.x, a.y, r) | (codes4(a.z, a.w, r) << 16);
-    hi = codes4(b.x, b.y, r) | (codes4(b.z, b.w, r) << 16);
+    const uint64_t rr = (static_cast<uint64_t>(__float_as_uint(r)) << 32) | __float_as_uint(r);
+    lo = codes4(a.x, a.y, rr) | (codes4(a.z, a.w, rr) << 16);
+    hi = codes4(b.x, b.y, rr) | (codes4(b.z, b.w, rr) << 16);
     return S;
 }
 

@@ -30,7 +30,74 @@ __device__ __forceinline__ uint64_t sf_mma_offset(uint32_t row, uint32_t kb, uin
            ((r >> 5) << 2) + (kb & 3u);
 }
 
-// One thread per 16-element block, two blocks in flight per thread.
+// One warp-uniform round of U blocks per lane: blocks i = base + lane +
+// u * stride (stride a multiple of 32, base of the warp's lane 0). All loads
+// are issued before the math. The four scale bytes of blocks 4j..4j+3 are
+// consecutive in both layouts (K / 16 is a multiple of 4 in the tile
+// layout), so lane 4j gathers them by shuffle and stores one 32-bit word
+// where it is aligned and whole (kGather; fewer store transactions for
+// HBM-bound runs); otherwise each lane stores its byte.
+// Blocks in [total, total_pad) are padding rows of the tile layout: scale 0.
+template <int kLayout, int U, bool kGather>
+__device__ __forceinline__ void quantize_round(const uint16_t *__restrict__ X, uint32_t base,
+                                               uint32_t stride, uint32_t total,
+                                               uint32_t total_pad, uint32_t kbpr, uint64_t ldx,
+                                               FastDiv div_kbpr, float g, uint8_t *__restrict__ q,
+                                               uint8_t *__restrict__ sf) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t kb4 = kbpr >> 2;
+    uint4 va[U], vb[U];
+    uint32_t row[U], kb[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const uint32_t i = base + lane + u * stride;
+        row[u] = div_kbpr.div(i);
+        kb[u] = i - row[u] * kbpr;
+        va[u] = make_uint4(0, 0, 0, 0);
+        vb[u] = va[u];
+        if (i < total) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(X + row[u] * ldx + kb[u] * 16ull);
+            va[u] = ld_stream(src);
+            vb[u] = ld_stream(src + 1);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const uint32_t i = base + lane + u * stride;
+        uint32_t S = 0, lo, hi;
+        if (i < total) {
+            S = quantize16(va[u], vb[u], g, lo, hi);
+            *reinterpret_cast<uint2 *>(q + static_cast<uint64_t>(i) * 8) = make_uint2(lo, hi);
+        }
+        const uint32_t end = kLayout == NVFP4_SF_ROW_MAJOR ? total : total_pad;
+        const uint64_t off = kLayout == NVFP4_SF_ROW_MAJOR
+                                 ? static_cast<uint64_t>(i)
+                                 : ((static_cast<uint64_t>(row[u] >> 7) * kb4 + (kb[u] >> 2)) << 9) +
+                                       ((row[u] & 31u) << 4) + (((row[u] & 127u) >> 5) << 2) +
+                                       (kb[u] & 3u);
+        if (!kGather) {
+            if (i < end) sf[off] = static_cast<uint8_t>(S);
+            continue;
+        }
+        const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, S, 1);
+        const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, S, 2);
+        const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, S, 3);
+        const bool whole = (i & 3u) == 0 && i + 3 < end &&
+                           ((reinterpret_cast<uintptr_t>(sf) + off) & 3u) == 0;
+        if (whole) {
+            *reinterpret_cast<uint32_t *>(sf + off) = S | (s1 << 8) | (s2 << 16) | (s3 << 24);
+        } else if (i < end) {
+            // the lane leading a whole group stored this byte already
+            const uint32_t lead = i & ~3u;
+            const uint64_t lead_off = off - (i - lead);
+            const bool lead_whole = lead + 3 < end &&
+                                    ((reinterpret_cast<uintptr_t>(sf) + lead_off) & 3u) == 0;
+            if (!lead_whole || (i & 3u) == 0) sf[off] = static_cast<uint8_t>(S);
+        }
+    }
+}
+
+// Warp-uniform rounds of 4 blocks per lane over all blocks.
 template <int kLayout>
 __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t *__restrict__ X,
                                                             uint32_t rows, uint32_t kbpr,
@@ -41,37 +108,11 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t *__re
     const float g = *g_ptr;
     const uint32_t total = rows * kbpr;
     const uint32_t stride = gridDim.x * blockDim.x;
-    const uint32_t kb4 = kbpr >> 2;
-    for (uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += 2 * stride) {
-        const uint32_t i1 = i0 + stride;
-        const bool has1 = i1 < total;
-        const uint32_t row0 = div_kbpr.div(i0), kb0 = i0 - row0 * kbpr;
-        const uint32_t row1 = has1 ? div_kbpr.div(i1) : row0;
-        const uint32_t kb1 = has1 ? i1 - row1 * kbpr : kb0;
-        const uint4 *p0 = reinterpret_cast<const uint4 *>(X + row0 * ldx + kb0 * 16ull);
-        const uint4 *p1 = reinterpret_cast<const uint4 *>(X + row1 * ldx + kb1 * 16ull);
-        const uint4 a0 = ld_stream(p0), b0 = ld_stream(p0 + 1);
-        uint4 a1 = make_uint4(0, 0, 0, 0), b1 = a1;
-        if (has1) {
-            a1 = ld_stream(p1);
-            b1 = ld_stream(p1 + 1);
-        }
-        uint32_t lo, hi;
-        uint32_t S = quantize16(a0, b0, g, lo, hi);
-        *reinterpret_cast<uint2 *>(q + static_cast<uint64_t>(i0) * 8) = make_uint2(lo, hi);
-        if (kLayout == NVFP4_SF_ROW_MAJOR)
-            sf[i0] = static_cast<uint8_t>(S);
-        else
-            sf[sf_mma_offset(row0, kb0, kb4)] = static_cast<uint8_t>(S);
-        if (has1) {
-            S = quantize16(a1, b1, g, lo, hi);
-            *reinterpret_cast<uint2 *>(q + static_cast<uint64_t>(i1) * 8) = make_uint2(lo, hi);
-            if (kLayout == NVFP4_SF_ROW_MAJOR)
-                sf[i1] = static_cast<uint8_t>(S);
-            else
-                sf[sf_mma_offset(row1, kb1, kb4)] = static_cast<uint8_t>(S);
-        }
-    }
+    constexpr int U = 4;
+    for (uint32_t base = blockIdx.x * blockDim.x + (threadIdx.x & ~31u); base < total;
+         base += U * stride)
+        quantize_round<kLayout, U, true>(X, base, stride, total, total, kbpr, ldx, div_kbpr, g, q,
+                                         sf);
 }
 
 // amax(|X|) over 16-byte vectors as a bfloat16 magnitude bit pattern,
@@ -113,95 +154,6 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t *__restri
         uint32_t b = threadIdx.x < kThreads / 32 ? warp_max[threadIdx.x] : 0u;
         b = __reduce_max_sync(0xFFFFFFFFu, b);
         if (threadIdx.x == 0 && b != 0) atomicMax(cell, b);
-    }
-}
-
-// Per-CTA partial amax (bfloat16 magnitude bits) -> partials[blockIdx.x];
-// every CTA writes its slot, so nothing needs zeroing beforehand.
-__global__ void __launch_bounds__(kThreads) amax_partial_kernel(const uint16_t *__restrict__ X,
-                                                                uint32_t rows, uint32_t vpr,
-                                                                uint64_t ldx, FastDiv div_vpr,
-                                                                uint32_t *partials) {
-    pdl_launch_dependents();
-    pdl_wait();  // X may come from the previous kernel
-    const uint32_t total = rows * vpr;
-    const uint32_t stride = gridDim.x * blockDim.x;
-    const uint32_t m = 0x7FFF7FFFu;
-    uint32_t acc = 0;
-    uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
-    for (; i + 3 * stride < total; i += 4 * stride) {
-        uint4 v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const uint32_t j = i + u * stride;
-            const uint32_t r = div_vpr.div(j), c = j - r * vpr;
-            v[u] = ld_stream(reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull));
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            acc = max_u16x2(acc, max_u16x2(max_u16x2(v[u].x & m, v[u].y & m),
-                                           max_u16x2(v[u].z & m, v[u].w & m)));
-    }
-    for (; i < total; i += stride) {
-        const uint32_t r = div_vpr.div(i), c = i - r * vpr;
-        const uint4 v = ld_stream(reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull));
-        acc = max_u16x2(acc, max_u16x2(max_u16x2(v.x & m, v.y & m), max_u16x2(v.z & m, v.w & m)));
-    }
-    uint32_t a = max(acc & 0xFFFFu, acc >> 16);
-    a = __reduce_max_sync(0xFFFFFFFFu, a);
-    __shared__ uint32_t warp_max[kThreads / 32];
-    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = a;
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        uint32_t b = threadIdx.x < kThreads / 32 ? warp_max[threadIdx.x] : 0u;
-        b = __reduce_max_sync(0xFFFFFFFFu, b);
-        if (threadIdx.x == 0) partials[blockIdx.x] = b;
-    }
-}
-
-// Quantize into the tensor-core scale layout with g reduced from the amax
-// partials (same integer max and IEEE division as global_scale_finalize).
-__global__ void __launch_bounds__(kThreads) quantize_dynamic_kernel(
-    const uint16_t *__restrict__ X, uint32_t rows, uint32_t rows_pad, uint32_t kbpr, uint64_t ldx,
-    FastDiv div_kbpr, const uint32_t *__restrict__ partials, uint32_t n_partials, float *g_out,
-    uint8_t *__restrict__ q, uint8_t *__restrict__ sf) {
-    pdl_launch_dependents();
-    pdl_wait();  // the partials come from amax_partial_kernel
-    __shared__ float g_sh;
-    if (threadIdx.x < 32) {
-        uint32_t b = 0;
-        for (uint32_t i = threadIdx.x; i < n_partials; i += 32) b = max(b, partials[i]);
-        b = __reduce_max_sync(0xFFFFFFFFu, b);
-        if (threadIdx.x == 0) {
-            const float amax = __uint_as_float(b << 16);
-            g_sh = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
-        }
-    }
-    __syncthreads();
-    const float g = g_sh;
-    if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
-    const uint32_t total = rows * kbpr;
-    const uint32_t total_pad = rows_pad * kbpr;
-    const uint32_t stride = gridDim.x * blockDim.x;
-    const uint32_t kb4 = kbpr >> 2;
-    for (uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < total_pad; i0 += 2 * stride) {
-        const uint32_t i1 = i0 + stride;
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const uint32_t i = u == 0 ? i0 : i1;
-            if (i >= total_pad) break;
-            const uint32_t row = div_kbpr.div(i), kb = i - row * kbpr;
-            if (i >= total) {  // padding rows of the last 128-row group read 0
-                sf[sf_mma_offset(row, kb, kb4)] = 0;
-                continue;
-            }
-            const uint4 *src = reinterpret_cast<const uint4 *>(X + row * ldx + kb * 16ull);
-            const uint4 a = ld_stream(src), b = ld_stream(src + 1);
-            uint32_t lo, hi;
-            const uint32_t S = quantize16(a, b, g, lo, hi);
-            *reinterpret_cast<uint2 *>(q + static_cast<uint64_t>(i) * 8) = make_uint2(lo, hi);
-            sf[sf_mma_offset(row, kb, kb4)] = static_cast<uint8_t>(S);
-        }
     }
 }
 
@@ -289,39 +241,11 @@ __global__ void __launch_bounds__(kThreads) quantize_fused_kernel(
     const uint32_t total = rows * kbpr;
     const uint32_t total_pad = rows_pad * kbpr;
     const uint32_t stride = gridDim.x * blockDim.x;
-    const uint32_t kb4 = kbpr >> 2;
-    // four blocks per thread per round, all loads issued before the math
     constexpr int U = 4;
-    for (uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < total_pad; i0 += U * stride) {
-        uint4 va[U], vb[U];
-        uint32_t row[U], kb[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t i = i0 + u * stride;
-            row[u] = div_kbpr.div(i);
-            kb[u] = i - row[u] * kbpr;
-            va[u] = make_uint4(0, 0, 0, 0);
-            vb[u] = va[u];
-            if (i < total) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(X + row[u] * ldx + kb[u] * 16ull);
-                va[u] = ld_stream(src);
-                vb[u] = ld_stream(src + 1);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t i = i0 + u * stride;
-            if (i >= total_pad) break;
-            if (i >= total) {  // padding rows of the last 128-row group read 0
-                sf[sf_mma_offset(row[u], kb[u], kb4)] = 0;
-                continue;
-            }
-            uint32_t lo, hi;
-            const uint32_t S = quantize16(va[u], vb[u], g, lo, hi);
-            *reinterpret_cast<uint2 *>(q + static_cast<uint64_t>(i) * 8) = make_uint2(lo, hi);
-            sf[sf_mma_offset(row[u], kb[u], kb4)] = static_cast<uint8_t>(S);
-        }
-    }
+    for (uint32_t base = blockIdx.x * blockDim.x + (threadIdx.x & ~31u); base < total_pad;
+         base += U * stride)
+        quantize_round<NVFP4_SF_MMA_128x4, U, false>(X, base, stride, total, total_pad, kbpr, ldx,
+                                                     div_kbpr, g, q, sf);
 }
 
 // g = amax / (6 * 448), or 1 for an all-zero tensor; in place over the cell.
@@ -388,7 +312,7 @@ cudaError_t launch_quantize(const uint16_t *X, int64_t rows, int64_t cols, int64
         if (e != cudaSuccess) return e;
     }
     if (total == 0) return cudaSuccess;
-    const int grid = grid_for(total, 2);
+    const int grid = grid_for(total, 4);
     if (layout == NVFP4_SF_ROW_MAJOR)
         quantize_kernel<NVFP4_SF_ROW_MAJOR><<<grid, kThreads, 0, st>>>(
             X, static_cast<uint32_t>(rows), kbpr, static_cast<uint64_t>(ldx), FastDiv(kbpr), g, q,
@@ -405,32 +329,6 @@ cudaLaunchAttribute pdl_attribute() {
     a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     a.val.programmaticStreamSerializationAllowed = 1;
     return a;
-}
-
-cudaError_t launch_quantize_dynamic(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
-                                    uint32_t *partials, float *g_out, uint8_t *q, uint8_t *sf,
-                                    cudaStream_t st) {
-    const uint32_t vpr = static_cast<uint32_t>(cols / 8);
-    const uint64_t total = static_cast<uint64_t>(rows) * vpr;
-    int n_partials = grid_for(total, 4);
-    if (n_partials > kMaxAmaxPartials) n_partials = kMaxAmaxPartials;
-    cudaLaunchAttribute attr = pdl_attribute();
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.stream = st;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    cfg.gridDim = dim3(n_partials, 1, 1);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, amax_partial_kernel, X, static_cast<uint32_t>(rows),
-                                       vpr, static_cast<uint64_t>(ldx), FastDiv(vpr), partials);
-    if (e != cudaSuccess) return e;
-    const uint32_t kbpr = static_cast<uint32_t>(cols / 16);
-    const uint32_t rows_pad = static_cast<uint32_t>((rows + 127) / 128 * 128);
-    cfg.gridDim = dim3(grid_for(static_cast<uint64_t>(rows_pad) * kbpr, 2), 1, 1);
-    return cudaLaunchKernelEx(&cfg, quantize_dynamic_kernel, X, static_cast<uint32_t>(rows),
-                              rows_pad, kbpr, static_cast<uint64_t>(ldx), FastDiv(kbpr),
-                              static_cast<const uint32_t *>(partials),
-                              static_cast<uint32_t>(n_partials), g_out, q, sf);
 }
 
 cudaError_t launch_quantize_fused(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
