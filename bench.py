@@ -39,6 +39,10 @@ L2_BYTES = 126 * 1024 * 1024
 FP4_OVER_BF16 = 13.5 / 2.25
 
 
+# sources of the GEMM kernel the benchmark step runs (CTA-pair kernel)
+GEMM_SOURCES = ("gemm_pair.cu", "ptx.cuh", "tensor_map.cu")
+
+
 def gemm_traffic_per_launch():
     """DRAM bytes per GEMM launch of the benchmark step from the committed
     ncu capture, valid only while the kernel source is the one captured."""
@@ -47,7 +51,7 @@ def gemm_traffic_per_launch():
         with open(os.path.join(ROOT, "profiles", "gemm_prefill_traffic.json")) as f:
             rec = json.load(f)
         h = hashlib.sha256()
-        for name in ("gemm.cu", "ptx.cuh"):
+        for name in GEMM_SOURCES:
             with open(os.path.join(ROOT, "nvfp4_block_scaled_28_b300", "csrc", name), "rb") as f:
                 h.update(f.read())
         if h.hexdigest() == rec["source_sha256"]:
@@ -307,7 +311,8 @@ def run_native(args):
     peak_sust = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
     peak_burst = peaks["bf16_tflops"] * FP4_OVER_BF16
     achieved = flops / (gemm_ms * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "kernel": "gemm_kernel (tcgen05 kind::mxf4nvf4)",
+    roofline = {"bound": "tensor",
+                "kernel": "gemm_pair_kernel (tcgen05 cta_group::2 kind::mxf4nvf4)",
                 "achieved": achieved, "peak": peak_sust, "unit": "TFLOP/s",
                 "frac": achieved / peak_sust, "frac_of_burst_peak": achieved / peak_burst,
                 "peak_note": "%s bf16 %s x %.0f (fp4:bf16 nominal 13.5:2.25), sustained"
@@ -503,7 +508,9 @@ def run_single_op(args):
         iters = args.iters
         cyc = torch.zeros(1, dtype=torch.int64, device="cuda")
         v = args.variant
-        n_mma = {0: 256, 1: 128, 2: 192}[v & 3]
+        if v == 7:
+            ctas &= ~1
+        n_mma = 128 if v in (1, 2) else 256
         fn = lambda i: _ok(lib.nvfp4_mma_peak_probe(ctas, iters, v, cyc.data_ptr(), D.stream),
                            "peak")
         for i in range(max(1, args.warmup)):
@@ -512,16 +519,20 @@ def run_single_op(args):
         sampler.start()
         ms = time_region(torch, fn, args.steps)
         clocks = sampler.stop()
-        k_mma = 16 if (v >> 6) & 1 else 64
+        k_mma = 16 if v == 6 else 64
         fl = ctas * iters * 2.0 * 128 * n_mma * k_mma
         c = int(cyc.item())
-        print(json.dumps({"op": "mma_peak", "variant": v, "N": n_mma, "K": k_mma,
-                          "two_issuers": (v >> 5) & 1,
-                          "accumulators": 1 << ((v >> 2) & 3), "sf_copies": (v >> 4) & 1,
-                          "ctas": ctas, "iters": iters, "ms": ms,
+        names = {0: "fp4 128x256x64", 1: "fp4 128x128x64", 2: "fp4 128x128x64, two warps",
+                 3: "fp4 + 3 scale copies per MMA, same thread",
+                 4: "fp4 + 3 scale copies per MMA, second warp",
+                 5: "fp4 + commit/poll/fence per 4 MMAs", 6: "bf16 128x256x16",
+                 7: "fp4 CTA pair 256x256x64 (per SM 128x256x64)"}
+        print(json.dumps({"op": "mma_peak", "variant": v, "what": names[v], "N": n_mma,
+                          "K": k_mma, "ctas": ctas, "iters": iters, "ms": ms,
                           "TFLOP/s": fl / ms / 1e9, "cycles_cta0": c,
-                          "cycles_per_mma": c / iters,
-                          "flop_per_cycle_per_sm": 2.0 * 128 * n_mma * k_mma * iters / c,
+                          "cycles_per_mma": c / (iters // 2 if v == 2 else iters),
+                          "flop_per_cycle_per_sm": 2.0 * 128 * n_mma * k_mma * iters / c
+                          if c else None,
                           "clocks": clocks}))
         return
     M, Nn, K = (int(v) for v in args.shape.split(","))

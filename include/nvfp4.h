@@ -240,24 +240,26 @@ NVFP4_API nvfp4_status nvfp4_device_error(int clear);
 /*
  * Dense FP4 tensor-core peak probe (measurement, not part of the linear
  * layer): `ctas` CTAs each issue `iters` back-to-back tcgen05.mma
- * kind::mxf4nvf4 instructions of 128 x N x 64 on shared-memory-resident
- * operands. variant bits 0-1 select N (0: 256, 1: 128, 2: 192), bits 2-3
- * the number of TMEM accumulators the MMAs rotate through (1, 2, 4; N times
- * that count at most 448), bit 4 adds before every MMA the three
- * shared->TMEM scale copies (tcgen05.cp) the GEMM issues per MMA, bit 5
- * splits the MMAs over two issuing warps with one accumulator each (needs
- * one accumulator and 2 N <= 448), bit 6 issues kind::f16 BF16 MMAs of
- * 128 x N x 16 instead (calibration against the BF16 rate), bit 7 issues the
- * three scale copies per MMA from a second warp concurrently (not with bits
- * 4 or 5); bits 8-10 add after every 4 MMAs a tcgen05.commit (8), a
- * tcgen05.fence::after_thread_sync (9), a warp-wide mbarrier poll by lane 0
- * (10); bit 11 issues five 128x256b scale copies in front of every 4 MMAs
- * from the MMA warp; bit 12 polls the mbarrier with all lanes; bits 13-15
- * stall the issuing warp with value * 32 dependent integer multiply-adds
- * after every 4 MMAs.
- * FLOPs = ctas * iters * 2 * 128 * N * K (K = 64, or 16 for BF16); time it
- * with events on `stream`.
- * CTA 0 writes its SM clock cycles to *cycles (device pointer).
+ * kind::mxf4nvf4 instructions on shared-memory-resident operands, from a
+ * loop specialised per variant (so the issuing warp's own work does not
+ * set the rate):
+ *   0  128 x 256 x 64 into one TMEM accumulator
+ *   1  128 x 128 x 64
+ *   2  128 x 128 x 64 from two warps, one accumulator each (iters / 2 each)
+ *   3  variant 0 with the GEMM's three shared->TMEM scale copies
+ *      (tcgen05.cp 32x128b.warpx4) in front of every MMA, same thread
+ *   4  variant 0 with those copies issued by a second warp concurrently
+ *   5  variant 0 with a GEMM stage's bookkeeping after every 4 MMAs:
+ *      tcgen05.commit, an mbarrier poll (lane 0 + shuffle), a fence
+ *   6  kind::f16 BF16 128 x 256 x 16 (calibration against the BF16 rate)
+ *   7  CTA pairs (clusters of 2, tcgen05 cta_group::2): rank 0 issues
+ *      256 x 256 x 64 MMAs computed half on each SM (ctas rounded down
+ *      to even, at least 2)
+ * iters must be a multiple of 4 (of 8 for variant 2).
+ * FLOPs = ctas * iters * 2 * 128 * N * K (N = 128 for variants 1 and 2,
+ * else 256; K = 16 for variant 6, else 64; for variant 7 per CTA of the
+ * even count); time it with events on
+ * `stream`. CTA 0 writes its SM clock cycles to *cycles (device pointer).
  * Errors: INVALID_ARG, MISALIGNED, CUDA.
  */
 NVFP4_API nvfp4_status nvfp4_mma_peak_probe(int ctas, int iters, int variant,

@@ -296,16 +296,10 @@ nvfp4_status nvfp4_device_error(int clear) {
 nvfp4_status nvfp4_mma_peak_probe(int ctas, int iters, int variant, unsigned long long *cycles,
                                   void *stream) {
     if (ctas <= 0 || iters <= 0 || cycles == nullptr) return NVFP4_ERR_INVALID_ARG;
-    // N (256, 128, 192) times the accumulator count must leave the scale
-    // columns 448..511 free
-    const int n_sel = variant & 3, accs = 1 << ((variant >> 2) & 3);
-    const int N = n_sel == 0 ? 256 : (n_sel == 1 ? 128 : 192);
-    const bool two_issuers = (variant >> 5) & 1;
-    const bool copy_warp = (variant >> 7) & 1;
-    if (variant < 0 || variant > 65535 || n_sel == 3 || ((variant >> 2) & 3) == 3 ||
-        N * accs > 448 || (two_issuers && (N * 2 > 448 || accs != 1)) ||
-        (copy_warp && (two_issuers || ((variant >> 4) & 1))))
-        return NVFP4_ERR_INVALID_ARG;
+    if (variant < 0 || variant > 7) return NVFP4_ERR_INVALID_ARG;
+    if (variant == 7 && ctas < 2) return NVFP4_ERR_INVALID_ARG;  // clusters of 2
+    // unrolled by 4 MMAs per warp; variant 2 splits them over two warps
+    if (iters % (variant == 2 ? 8 : 4) != 0) return NVFP4_ERR_INVALID_ARG;
     if (!aligned(cycles, 8)) return NVFP4_ERR_MISALIGNED;
     return from_cuda(launch_mma_peak(ctas, iters, variant, cycles,
                                      static_cast<cudaStream_t>(stream)));

@@ -125,3 +125,15 @@ def test_python_binding_rejects_packed_fp4_as_bf16():
     with pytest.raises(ValueError, match="scale bytes"):
         nv.nvfp4_linear(X, torch.zeros(128, 256, dtype=torch.uint8),
                         torch.zeros(128, 16, dtype=torch.uint8), g)
+
+
+def test_mma_peak_probe_argument_checks(lib):
+    p = lib.nvfp4_mma_peak_probe
+    assert p(1, 8, 8, A16, None) == N.ERR_INVALID_ARG   # no such variant
+    assert p(1, 8, 7, A16, None) == N.ERR_INVALID_ARG   # pair variant needs 2 CTAs
+    assert p(1, 8, -1, A16, None) == N.ERR_INVALID_ARG
+    assert p(1, 6, 0, A16, None) == N.ERR_INVALID_ARG   # iters not a multiple of 4
+    assert p(1, 12, 2, A16, None) == N.ERR_INVALID_ARG  # two warps: multiple of 8
+    assert p(0, 8, 0, A16, None) == N.ERR_INVALID_ARG
+    assert p(1, 8, 0, None, None) == N.ERR_INVALID_ARG
+    assert p(1, 8, 0, A16 + 4, None) == N.ERR_MISALIGNED
