@@ -159,6 +159,7 @@ class Direct:
     def __init__(self, lib, stream):
         self.lib = lib
         self.stream = stream
+        self._ws = {}
 
     def global_scale(self, X, g):
         return self.lib.nvfp4_global_scale(X.data_ptr(), X.shape[0], X.shape[1], X.stride(0),
@@ -170,9 +171,19 @@ class Direct:
                                        self.stream)
 
     def gemm(self, Aq, As, ga, Bq, Bs, gb, M, N, K, Y):
+        # scratch of nvfp4_gemm_workspace_bytes, allocated once per shape
+        need = int(self.lib.nvfp4_gemm_workspace_bytes(M, N, K))
+        ws = None
+        if need:
+            import torch
+            key = (M, N, K)
+            if key not in self._ws:
+                self._ws[key] = torch.empty(need, dtype=torch.uint8, device="cuda")
+            ws = self._ws[key]
         return self.lib.nvfp4_gemm(Aq.data_ptr(), As.data_ptr(), ga.data_ptr(), Bq.data_ptr(),
                                    Bs.data_ptr(), gb.data_ptr(), M, N, K, Y.data_ptr(),
-                                   Y.stride(0), None, 0, self.stream)
+                                   Y.stride(0), None if ws is None else ws.data_ptr(), need,
+                                   self.stream)
 
     def linear(self, X, Wq, Ws, gw, Y, gx, mode, ws):
         M, K = X.shape

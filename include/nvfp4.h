@@ -149,8 +149,8 @@ NVFP4_API nvfp4_status nvfp4_sf_to_mma_layout(const uint8_t *sf_row_major, int64
  * M <= 128 (decode) runs a weight-streaming kernel that computes Y^T = W X^T
  * with the weights as the 128-row MMA operand; larger M runs the 128 x 256
  * tile kernel.
- * workspace / workspace_bytes: scratch for the skinny-M split-K path; query
- * nvfp4_gemm_workspace_bytes(). May be NULL when that returns 0.
+ * workspace / workspace_bytes: scratch; query nvfp4_gemm_workspace_bytes()
+ * (0 for every shape in this version). May be NULL when that returns 0.
  * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_SHAPE,
  * WORKSPACE_TOO_SMALL, CUDA.
  */

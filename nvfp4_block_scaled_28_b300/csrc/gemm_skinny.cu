@@ -10,9 +10,9 @@
 // Same arithmetic as the large-M kernel (the "nvfp4-difusion" page's block-
 // scaled matmul, section 2); only the roles of the operands are swapped. The
 // regime is bound by streaming the weights from HBM once (N K / 2 bytes of
-// codes plus N K / 16 of scales), so each CTA owns 128 weight rows, streams
-// them through an 8-deep ring and keeps the whole of X's tile resident per
-// stage.
+// codes plus N K / 16 of scales), so each CTA owns 128 weight rows and
+// streams them through a ring of stages (two 256-deep K chunks per stage
+// when K allows; 3 to 8 stages, as many as fit), X's chunk riding along.
 //
 // FUSED (M <= 32): the producer loads bfloat16 X tiles instead of codes, and
 // four quantizer warps turn them into E2M1 codes and E4M3 scales in shared
@@ -21,8 +21,8 @@
 // re-quantizes the same small X; for decode that costs far less than a
 // separate quantize launch.
 //
-// Warps: 0 TMA producer, 1 MMA issuer (scale copies to TMEM + MMAs, issued
-// from the converged warp through elect.sync), 2 TMEM allocator, 3-6
+// Warps: 0 TMA producer, 1 MMA issuer (per K = 64 step its two scale copies
+// to TMEM and the MMA under one elect.sync), 2 TMEM allocator, 3-6
 // epilogue (one per 32-lane TMEM quarter), 7-10 quantizers (FUSED only).
 // All waits are bounded; a timeout is recorded and every role leaves.
 #include <cuda.h>
@@ -46,14 +46,22 @@ constexpr int SK_SF_TILE = 512;
 constexpr unsigned kAllLanes = 0xFFFFFFFFu;
 
 // NX: MMA N (64 or 128); XR <= NX: rows of X loaded (and quantized);
-// CPS: CTAs resident per SM (each gets 1/CPS of shared memory and TMEM).
-template <int NX, int XR, bool FUSED, int CPS>
+// KC: 256-deep K chunks per pipeline stage (2 for the unfused path when
+// K % 512 == 0: two weight boxes per stage halve the per-stage costs of
+// the ring, which bound the weight stream with one box per stage).
+template <int NX, int XR, bool FUSED, int KC>
 struct SkCfg {
-    static constexpr int W_BYTES = SK_BM * SK_BK / 2;            // 16 KiB
-    static constexpr int X_BYTES = NX * SK_BK / 2;               // codes, NX rows
-    static constexpr int X_LOAD = XR * SK_BK / 2;                // bytes of codes loaded
-    static constexpr int SFW_BYTES = 2048;                       // 4 scale tiles of W
-    static constexpr int SFX_BYTES = 2048;                       // 4 scale tiles of X
+    static constexpr int W_CHUNK = SK_BM * SK_BK / 2;             // 16 KiB per K chunk
+    // X chunks sit XR rows apart; the MMA reads NX >= XR rows from each, so
+    // rows XR .. NX-1 of a chunk are the next chunk's (or the scales') bytes
+    // and only feed output columns that are never stored (unfused path; the
+    // fused quantizer writes whole NX-row chunks)
+    static constexpr int X_CHUNK = (FUSED ? NX : XR) * SK_BK / 2;
+    static constexpr int W_BYTES = KC * W_CHUNK;
+    static constexpr int X_BYTES = KC * X_CHUNK;
+    static constexpr int X_LOAD = KC * XR * SK_BK / 2;            // bytes of codes loaded
+    static constexpr int SFW_BYTES = KC * 2048;                   // 4 scale tiles of W per chunk
+    static constexpr int SFX_BYTES = KC * 2048;                   // 4 scale tiles of X per chunk
     static constexpr int XBF_BYTES = FUSED ? XR * SK_BK * 2 : 0;  // bfloat16 X tile
     static constexpr int OFF_W = 0;
     static constexpr int OFF_X = OFF_W + W_BYTES;
@@ -62,21 +70,23 @@ struct SkCfg {
     static constexpr int OFF_XBF = OFF_SFX + SFX_BYTES;
     static constexpr int STAGE_RAW = OFF_XBF + XBF_BYTES;
     static constexpr int STAGE = (STAGE_RAW + 1023) / 1024 * 1024;
-    static constexpr int BUDGET = (CPS == 1 ? 220 : 108) * 1024;
+    static constexpr int BUDGET = 220 * 1024;
     static constexpr int STAGES = BUDGET / STAGE < 8 ? BUDGET / STAGE : 8;
     static constexpr int BAR_OFF = STAGES * STAGE;
     static constexpr int SMEM = BAR_OFF + 512 + 1024;
     static constexpr int EPI_WARPS = 4;
     static constexpr int Q_WARPS = FUSED ? 4 : 0;
     static constexpr int THREADS = 32 * (3 + EPI_WARPS + Q_WARPS);
-    static constexpr uint32_t ACC_COL = 0;                       // NX columns
-    static constexpr uint32_t SF_COL = 128;                      // per stage 16 (W) + 16 (X)
-    static constexpr uint32_t SF_COLS = 32;
-    static constexpr uint32_t TMEM_COLS = CPS == 1 ? 512 : 256;
+    static constexpr uint32_t ACC_COL = 0;                        // NX columns
+    static constexpr uint32_t SF_COL = 128;                       // per stage 16 KC (W) + 16 KC (X)
+    static constexpr uint32_t SF_COLS = 32 * KC;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(!FUSED || KC == 1, "the fused quantizer works on 256-deep stages");
     static_assert(SF_COL + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
     static_assert(STAGES >= 3, "pipeline depth");
-    static_assert(SMEM * CPS <= 232448, "shared memory budget");
-    static_assert(OFF_X % 1024 == 0 && STAGE % 1024 == 0, "swizzled tiles need 1024-B alignment");
+    static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(OFF_X % 1024 == 0 && X_CHUNK % 1024 == 0 && STAGE % 1024 == 0,
+                  "swizzled tiles need 1024-B alignment");
 };
 
 struct SkParams {
@@ -135,11 +145,11 @@ __device__ __forceinline__ bool sk_wait(uint64_t *bar, uint32_t parity, const Sk
     return __shfl_sync(kAllLanes, ok, 0) != 0;
 }
 
-template <int NX, int XR, bool FUSED, int CPS>
-__global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, CPS>::THREADS, CPS)
+template <int NX, int XR, bool FUSED, int KC>
+__global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
     skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                   const SkParams p) {
-    using C = SkCfg<NX, XR, FUSED, CPS>;
+    using C = SkCfg<NX, XR, FUSED, KC>;
     constexpr int S = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -148,7 +158,7 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, CPS>::THREADS, CPS)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int num_k = p.K / SK_BK;
+    const int num_k = p.K / (SK_BK * KC);  // pipeline stages per tile
     const int kb4 = p.K / 64;
 
     if (threadIdx.x == 0) {
@@ -194,17 +204,23 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, CPS>::THREADS, CPS)
                 }
                 if (lane == 0) {
                     uint8_t *st = smem + s * C::STAGE;
+                    const int k0 = kt * KC;  // first 256-deep chunk of the stage
                     mbar_arrive_expect_tx(&sh.full[s], tx);
-                    tma_load_2d(st + C::OFF_W, &tmW, &sh.full[s], kt * (SK_BK / 2), nt * SK_BM,
-                                pol_w);
+#pragma unroll
+                    for (int c = 0; c < KC; ++c)
+                        tma_load_2d(st + C::OFF_W + c * C::W_CHUNK, &tmW, &sh.full[s],
+                                    (k0 + c) * (SK_BK / 2), nt * SK_BM, pol_w);
                     bulk_load(st + C::OFF_SFW,
-                              p.Ws + (static_cast<int64_t>(nt) * kb4 + kt * 4) * SK_SF_TILE,
+                              p.Ws + (static_cast<int64_t>(nt) * kb4 + k0 * 4) * SK_SF_TILE,
                               C::SFW_BYTES, &sh.full[s], pol_w);
                     if (FUSED) {
                         tma_load_2d(st + C::OFF_XBF, &tmX, &sh.full[s], kt * SK_BK, 0, pol_x);
                     } else {
-                        tma_load_2d(st + C::OFF_X, &tmX, &sh.full[s], kt * (SK_BK / 2), 0, pol_x);
-                        bulk_load(st + C::OFF_SFX, p.Xs + static_cast<int64_t>(kt) * 4 * SK_SF_TILE,
+#pragma unroll
+                        for (int c = 0; c < KC; ++c)
+                            tma_load_2d(st + C::OFF_X + c * C::X_CHUNK, &tmX, &sh.full[s],
+                                        (k0 + c) * (SK_BK / 2), 0, pol_x);
+                        bulk_load(st + C::OFF_SFX, p.Xs + static_cast<int64_t>(k0) * 4 * SK_SF_TILE,
                                   C::SFX_BYTES, &sh.full[s], pol_x);
                     }
                 }
@@ -239,21 +255,22 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, CPS>::THREADS, CPS)
                 tc_fence_after();
                 uint8_t *st = smem + s * C::STAGE;
                 const uint32_t sf_w = tmem + C::SF_COL + s * C::SF_COLS;
-                const uint32_t sf_x = sf_w + 16;
+                const uint32_t sf_x = sf_w + 16 * KC;
                 const uint32_t sfw_smem = smem_addr(st + C::OFF_SFW);
                 const uint32_t sfx_smem = smem_addr(st + C::OFF_SFX);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    tmem_cp_32x128b_x4_elect(sf_w + j * 4, sdesc_sf(sfw_smem + j * SK_SF_TILE));
-                    tmem_cp_32x128b_x4_elect(sf_x + j * 4, sdesc_sf(sfx_smem + j * SK_SF_TILE));
-                }
                 const uint32_t w_smem = smem_addr(st + C::OFF_W);
                 const uint32_t x_smem = smem_addr(st + C::OFF_X);
+                // per K = 64 step: its two scale tiles, then the MMA, one elect
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    mma_mxf4nvf4_elect(tmem + C::ACC_COL, sdesc_sw128(w_smem + j * 32),
-                                       sdesc_sw128(x_smem + j * 32), idesc, sf_w + j * 4,
-                                       sf_x + j * 4, (kt | j) != 0);
+                for (int q = 0; q < 4 * KC; ++q) {
+                    const int c = q >> 2, j = q & 3;  // chunk, K = 64 step within it
+                    sf_copy2_mma_elect(tmem + C::ACC_COL,
+                                       sdesc_sw128(w_smem + c * C::W_CHUNK + j * 32),
+                                       sdesc_sw128(x_smem + c * C::X_CHUNK + j * 32), idesc,
+                                       sf_w + q * 4, sf_x + q * 4, (kt | q) != 0,
+                                       sdesc_sf(sfw_smem + q * SK_SF_TILE),
+                                       sdesc_sf(sfx_smem + q * SK_SF_TILE));
+                }
                 tc_commit_elect(&sh.empty[s]);
             }
             if (ok) tc_commit_elect(&sh.acc_full);
@@ -376,12 +393,12 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, CPS>::THREADS, CPS)
     }
 }
 
-template <int NX, int XR, bool FUSED, int CPS>
+template <int NX, int XR, bool FUSED, int KC>
 cudaError_t launch_sk(const SkinnyArgs &a, cudaStream_t st) {
-    using C = SkCfg<NX, XR, FUSED, CPS>;
+    using C = SkCfg<NX, XR, FUSED, KC>;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(skinny_kernel<NX, XR, FUSED, CPS>,
+        cudaError_t e = cudaFuncSetAttribute(skinny_kernel<NX, XR, FUSED, KC>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         attr = true;
@@ -416,7 +433,7 @@ cudaError_t launch_sk(const SkinnyArgs &a, cudaStream_t st) {
     p.timeout_ns = debug_state().timeout_ns;
     p.err = device_error_word();
     if (p.err == nullptr) return cudaErrorInvalidSymbol;
-    const int slots = CPS * launch_cfg().num_sms;
+    const int slots = launch_cfg().num_sms;
     const int grid = p.n_tiles < slots ? p.n_tiles : slots;
     cudaLaunchAttribute pdl = pdl_attribute();
     cudaLaunchConfig_t cfg = {};
@@ -426,7 +443,7 @@ cudaError_t launch_sk(const SkinnyArgs &a, cudaStream_t st) {
     cfg.stream = st;
     cfg.attrs = &pdl;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, skinny_kernel<NX, XR, FUSED, CPS>, tmW, tmX, p);
+    return cudaLaunchKernelEx(&cfg, skinny_kernel<NX, XR, FUSED, KC>, tmW, tmX, p);
 }
 
 }  // namespace
@@ -434,19 +451,13 @@ cudaError_t launch_sk(const SkinnyArgs &a, cudaStream_t st) {
 cudaError_t launch_gemm_skinny(const SkinnyArgs &a, cudaStream_t st) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
     if (a.M > kSkinnyMaxM || (a.fused && a.M > kSkinnyFusedMaxM)) return cudaErrorInvalidValue;
-    static int cps = 0;
-    if (cps == 0) {
-        const char *env = getenv("NVFP4_SKINNY_CTAS_PER_SM");  // tuning knob: 1 or 2
-        cps = (env && env[0] == '2' && env[1] == 0) ? 2 : 1;
-    }
-    if (cps == 2) {
-        if (a.M <= 32)
-            return a.fused ? launch_sk<64, 32, true, 1>(a, st) : launch_sk<64, 32, false, 2>(a, st);
+    if (a.fused) return launch_sk<64, 32, true, 1>(a, st);
+    if (a.K % 512 == 0) {
+        if (a.M <= 32) return launch_sk<64, 32, false, 2>(a, st);
         if (a.M <= 64) return launch_sk<64, 64, false, 2>(a, st);
         return launch_sk<128, 128, false, 2>(a, st);
     }
-    if (a.M <= 32)
-        return a.fused ? launch_sk<64, 32, true, 1>(a, st) : launch_sk<64, 32, false, 1>(a, st);
+    if (a.M <= 32) return launch_sk<64, 32, false, 1>(a, st);
     if (a.M <= 64) return launch_sk<64, 64, false, 1>(a, st);
     return launch_sk<128, 128, false, 1>(a, st);
 }

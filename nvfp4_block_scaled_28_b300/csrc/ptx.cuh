@@ -466,6 +466,25 @@ __device__ __forceinline__ void tc_commit_elect(uint64_t *bar) {
         : "memory");
 }
 
+// One K = 64 step under a single elect: the A and B scale tiles shared ->
+// TMEM (32x128b.warpx4 each, to [sfa, sfa + 4) and [sfb, sfb + 4)), then
+// the MMA that reads them; one thread's copies and MMA reach the tensor
+// core in issue order.
+__device__ __forceinline__ void sf_copy2_mma_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                   uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                                   uint32_t accumulate, uint64_t da, uint64_t db) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%5], %7;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%6], %8;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb), "l"(da), "l"(db)
+        : "memory");
+}
+
 // ------------------------------------------------ CTA pair (cta_group::2)
 // The two CTAs of a cluster of 2 act as one tensor-core unit: rank 0 issues
 // the MMAs and scale copies for both, each CTA holds its half of A (rows),
