@@ -251,15 +251,15 @@ nvfp4_status nvfp4_linear(const void *X, int64_t M, int64_t K, int64_t ldx, cons
     uint8_t *xq = ws + kLinearHeader;
     uint8_t *xs = xq + round_up(static_cast<size_t>(M) * static_cast<size_t>(K / 2), 256);
     const uint16_t *Xh = static_cast<const uint16_t *>(X);
-    if (mode == NVFP4_LINEAR_FUSED && M <= kSkinnyFusedMaxM) {
+    if (mode == NVFP4_LINEAR_FUSED && M <= kSkinnyFusedMaxM && K <= kSkinnyFusedMaxK) {
         // one launch: the GEMM computes g_x (when not given) and quantizes X
         // tiles in shared memory; no codes in HBM
         SkinnyArgs sa{Wq, Ws, g_w, nullptr, nullptr, Xh, ldx, g_x, M, N, K,
                       static_cast<uint16_t *>(Y), ldy, 1};
         return from_cuda(launch_gemm_skinny(sa, st));
     }
-    // unfused (and fused with more than 32 rows, where re-quantizing X in
-    // every N-tile's producer would cost more than one quantize pass)
+    // unfused (and fused beyond 8 rows or K = 6144, where every CTA
+    // re-quantizing X would cost more than one quantize pass)
     cudaError_t e;
     if (g_x == nullptr) {
         // amax partials, grid barrier and quantization in one launch (g_x

@@ -14,12 +14,14 @@
 // streams them through a ring of stages (two 256-deep K chunks per stage
 // when K allows; 3 to 8 stages, as many as fit), X's chunk riding along.
 //
-// FUSED (M <= 32): the producer loads bfloat16 X tiles instead of codes, and
-// four quantizer warps turn them into E2M1 codes and E4M3 scales in shared
-// memory with the same arithmetic as nvfp4_quantize (quant_math.cuh) before
-// the MMA reads them, so X's codes never travel through HBM. Every CTA
-// re-quantizes the same small X; for decode that costs far less than a
-// separate quantize launch.
+// FUSED (M <= 8, K <= kSkinnyFusedMaxK): no codes of X ever reach HBM. At the
+// start, four quantizer warps read the bfloat16 X, compute g_x when it is not
+// given (the same integer amax and IEEE division as nvfp4_global_scale) and
+// quantize all of X (quant_math.cuh, the bytes of nvfp4_quantize) into a
+// resident shared-memory copy: E2M1 codes in 128-byte-swizzled chunks and
+// E4M3 scales in the tensor-core tile layout. The ring then streams only
+// weights. Every CTA quantizes the same small X (M K / 16 blocks, a few
+// thousand), which overlaps the weight ring filling up.
 //
 // Warps: 0 TMA producer, 1 MMA issuer (per K = 64 step its two scale copies
 // to TMEM and the MMA under one elect.sync), 2 TMEM allocator, 3-6
@@ -45,34 +47,37 @@ constexpr int SK_BK = 256;                 // K per stage
 constexpr int SK_SF_TILE = 512;
 constexpr unsigned kAllLanes = 0xFFFFFFFFu;
 
-// NX: MMA N (64 or 128); XR <= NX: rows of X loaded (and quantized);
-// KC: 256-deep K chunks per pipeline stage (2 for the unfused path when
-// K % 512 == 0: two weight boxes per stage halve the per-stage costs of
-// the ring, which bound the weight stream with one box per stage).
+// NX: MMA N (64 or 128); XR <= NX: rows of X loaded (or quantized);
+// KC: 256-deep K chunks per pipeline stage (2 when K % 512 == 0: two weight
+// boxes per stage halve the per-stage costs of the ring).
 template <int NX, int XR, bool FUSED, int KC>
 struct SkCfg {
     static constexpr int W_CHUNK = SK_BM * SK_BK / 2;             // 16 KiB per K chunk
     // X chunks sit XR rows apart; the MMA reads NX >= XR rows from each, so
     // rows XR .. NX-1 of a chunk are the next chunk's (or the scales') bytes
-    // and only feed output columns that are never stored (unfused path; the
-    // fused quantizer writes whole NX-row chunks)
-    static constexpr int X_CHUNK = (FUSED ? NX : XR) * SK_BK / 2;
+    // and only feed output columns that are never stored
+    static constexpr int X_CHUNK = XR * SK_BK / 2;
+    // FUSED: resident X for K up to kSkinnyFusedMaxK
+    static constexpr int RES_CHUNKS = FUSED ? static_cast<int>(kSkinnyFusedMaxK / SK_BK) : 0;
+    static constexpr int XRES_BYTES = RES_CHUNKS * X_CHUNK;
+    static constexpr int SFXRES_BYTES = RES_CHUNKS * 2048;       // 4 scale tiles per chunk
+    static constexpr int RING = XRES_BYTES + SFXRES_BYTES;        // ring after the resident X
+    // one stage: weights (KC chunks) and their scales; unfused: X's chunks
+    // and scales too
     static constexpr int W_BYTES = KC * W_CHUNK;
-    static constexpr int X_BYTES = KC * X_CHUNK;
-    static constexpr int X_LOAD = KC * XR * SK_BK / 2;            // bytes of codes loaded
-    static constexpr int SFW_BYTES = KC * 2048;                   // 4 scale tiles of W per chunk
-    static constexpr int SFX_BYTES = KC * 2048;                   // 4 scale tiles of X per chunk
-    static constexpr int XBF_BYTES = FUSED ? XR * SK_BK * 2 : 0;  // bfloat16 X tile
+    static constexpr int X_BYTES = FUSED ? 0 : KC * X_CHUNK;
+    static constexpr int X_LOAD = X_BYTES;                        // bytes of codes loaded
+    static constexpr int SFW_BYTES = KC * 2048;
+    static constexpr int SFX_BYTES = FUSED ? 0 : KC * 2048;
     static constexpr int OFF_W = 0;
     static constexpr int OFF_X = OFF_W + W_BYTES;
     static constexpr int OFF_SFW = OFF_X + X_BYTES;
     static constexpr int OFF_SFX = OFF_SFW + SFW_BYTES;
-    static constexpr int OFF_XBF = OFF_SFX + SFX_BYTES;
-    static constexpr int STAGE_RAW = OFF_XBF + XBF_BYTES;
+    static constexpr int STAGE_RAW = OFF_SFX + SFX_BYTES;
     static constexpr int STAGE = (STAGE_RAW + 1023) / 1024 * 1024;
     static constexpr int BUDGET = 220 * 1024;
-    static constexpr int STAGES = BUDGET / STAGE < 8 ? BUDGET / STAGE : 8;
-    static constexpr int BAR_OFF = STAGES * STAGE;
+    static constexpr int STAGES = (BUDGET - RING) / STAGE < 8 ? (BUDGET - RING) / STAGE : 8;
+    static constexpr int BAR_OFF = RING + STAGES * STAGE;
     static constexpr int SMEM = BAR_OFF + 512 + 1024;
     static constexpr int EPI_WARPS = 4;
     static constexpr int Q_WARPS = FUSED ? 4 : 0;
@@ -81,11 +86,12 @@ struct SkCfg {
     static constexpr uint32_t SF_COL = 128;                       // per stage 16 KC (W) + 16 KC (X)
     static constexpr uint32_t SF_COLS = 32 * KC;
     static constexpr uint32_t TMEM_COLS = 512;
-    static_assert(!FUSED || KC == 1, "the fused quantizer works on 256-deep stages");
+    static_assert(!FUSED || XR == 8, "the resident X holds 8 rows");
     static_assert(SF_COL + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
     static_assert(STAGES >= 3, "pipeline depth");
     static_assert(SMEM <= 232448, "shared memory budget");
-    static_assert(OFF_X % 1024 == 0 && X_CHUNK % 1024 == 0 && STAGE % 1024 == 0,
+    static_assert(RING % 1024 == 0 && OFF_X % 1024 == 0 && X_CHUNK % 1024 == 0 &&
+                      STAGE % 1024 == 0,
                   "swizzled tiles need 1024-B alignment");
 };
 
@@ -109,14 +115,14 @@ template <int STAGES>
 struct SkShared {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
-    uint64_t qdone[STAGES];
+    uint64_t xready;           // fused: the resident X is quantized
     uint64_t acc_full;
     uint64_t acc_empty;
     uint64_t drain;
     uint32_t tmem_base;
     volatile uint32_t abort_flag;
     float g_x;                 // fused: activation global scale used by this CTA
-    uint32_t amax_part[4];     // fused: per-quantizer-warp amax (bfloat16 bits)
+    uint32_t amax_part[8];     // fused: per-warp amax of X (bfloat16 bits)
 };
 
 template <int STAGES>
@@ -145,6 +151,64 @@ __device__ __forceinline__ bool sk_wait(uint64_t *bar, uint32_t parity, const Sk
     return __shfl_sync(kAllLanes, ok, 0) != 0;
 }
 
+// Fused path, run by the epilogue and quantizer warps (warps 3 .. 3 + 8,
+// 256 threads): g_x (when not given: the same integer amax and IEEE
+// division as nvfp4_global_scale, so the bytes match the unfused path),
+// then all of X (rows < M; rows M .. XR-1 only feed unstored columns)
+// quantized into the resident copy. Block (row r, 16-element block kb):
+// codes in 256-deep chunk kb / 16 (128-byte swizzle: 16-byte piece k of
+// row r at k ^ (r % 8)), scale at the tile layout's byte.
+template <class C, int S>
+__device__ __forceinline__ void quantize_x_resident(const SkParams &p, SkShared<S> &sh,
+                                                    uint8_t *xres, uint8_t *sfxres) {
+    constexpr int kWarps = C::EPI_WARPS + C::Q_WARPS;
+    constexpr int kThr = 32 * kWarps;
+    const int qt = threadIdx.x - 32 * 3;  // 0 .. kThr - 1
+    const int lane = threadIdx.x & 31;
+    float gx;
+    if (p.g_x != nullptr) {
+        gx = *p.g_x;
+    } else {
+        const uint32_t vpr = static_cast<uint32_t>(p.K / 8);
+        const uint32_t total = static_cast<uint32_t>(p.M) * vpr;
+        const uint32_t m16 = 0x7FFF7FFFu;
+        uint32_t acc = 0;
+        for (uint32_t i = qt; i < total; i += kThr) {
+            const uint32_t r = i / vpr, c = i - r * vpr;
+            const uint4 v = *reinterpret_cast<const uint4 *>(p.X + r * p.ldx + c * 8ull);
+            acc = max_u16x2(acc, max_u16x2(max_u16x2(v.x & m16, v.y & m16),
+                                           max_u16x2(v.z & m16, v.w & m16)));
+        }
+        uint32_t a = max(acc & 0xFFFFu, acc >> 16);
+        a = __reduce_max_sync(kAllLanes, a);
+        if (lane == 0) sh.amax_part[qt >> 5] = a;
+        asm volatile("bar.sync 1, %0;" ::"n"(kThr) : "memory");
+        a = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) a = max(a, sh.amax_part[w]);
+        const float amax = __uint_as_float(a << 16);
+        gx = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+    }
+    if (qt == 0) sh.g_x = gx;
+    const int kbpr = p.K / 16;
+    for (int b = qt; b < p.M * kbpr; b += kThr) {
+        const int r = b / kbpr, kb = b - r * kbpr;
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.X + r * p.ldx + kb * 16ll);
+        const uint4 v0 = src[0], v1 = src[1];
+        uint32_t lo, hi;
+        const uint32_t Sb = quantize16(v0, v1, gx, lo, hi);
+        const int chunk = kb >> 4, kbc = kb & 15, piece = kbc >> 1;
+        *reinterpret_cast<uint2 *>(xres + chunk * C::X_CHUNK + r * 128 + ((piece ^ (r & 7)) << 4) +
+                                   (kbc & 1) * 8) = make_uint2(lo, hi);
+        sfxres[(kb >> 2) * SK_SF_TILE + (r & 31) * 16 + (r >> 5) * 4 + (kb & 3)] =
+            static_cast<uint8_t>(Sb);
+    }
+    fence_proxy_async_shared();  // generic-proxy writes -> tensor core reads
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.xready);
+    __syncwarp();
+}
+
 template <int NX, int XR, bool FUSED, int KC>
 __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
     skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -152,9 +216,12 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
     using C = SkCfg<NX, XR, FUSED, KC>;
     constexpr int S = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
+    uint8_t *smem_base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    SkShared<S> &sh = *reinterpret_cast<SkShared<S> *>(smem + C::BAR_OFF);
+    uint8_t *smem = smem_base + C::RING;      // the stage ring
+    uint8_t *xres = smem_base;                // fused: resident X codes
+    uint8_t *sfxres = smem_base + C::XRES_BYTES;  // fused: resident X scales
+    SkShared<S> &sh = *reinterpret_cast<SkShared<S> *>(smem_base + C::BAR_OFF);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -165,15 +232,15 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
         for (int s = 0; s < S; ++s) {
             mbar_init(&sh.full[s], 1);
             mbar_init(&sh.empty[s], 1);
-            mbar_init(&sh.qdone[s], C::Q_WARPS > 0 ? C::Q_WARPS : 1);
         }
+        mbar_init(&sh.xready, C::Q_WARPS > 0 ? C::Q_WARPS + C::EPI_WARPS : 1);
         mbar_init(&sh.acc_full, 1);
         mbar_init(&sh.acc_empty, C::EPI_WARPS);
         mbar_init(&sh.drain, 1);
         sh.abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmW);
-        tma_prefetch_desc(&tmX);
+        if (!FUSED) tma_prefetch_desc(&tmX);
     }
     if (warp == 2) {
         tmem_alloc(&sh.tmem_base, C::TMEM_COLS);
@@ -191,8 +258,7 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
         // ---------------------------------------------------- TMA producer
         const uint64_t pol_w = policy_evict_first();  // weights stream through once
         const uint64_t pol_x = policy_evict_last();   // X is re-read by every CTA
-        constexpr uint32_t tx = FUSED ? (C::W_BYTES + C::SFW_BYTES + C::XBF_BYTES)
-                                      : (C::W_BYTES + C::SFW_BYTES + C::X_LOAD + C::SFX_BYTES);
+        constexpr uint32_t tx = C::W_BYTES + C::SFW_BYTES + C::X_LOAD + C::SFX_BYTES;
         int g = 0;
         bool ok = !p.inject;
         for (int nt = blockIdx.x; ok && nt < p.n_tiles; nt += gridDim.x) {
@@ -213,9 +279,7 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
                     bulk_load(st + C::OFF_SFW,
                               p.Ws + (static_cast<int64_t>(nt) * kb4 + k0 * 4) * SK_SF_TILE,
                               C::SFW_BYTES, &sh.full[s], pol_w);
-                    if (FUSED) {
-                        tma_load_2d(st + C::OFF_XBF, &tmX, &sh.full[s], kt * SK_BK, 0, pol_x);
-                    } else {
+                    if (!FUSED) {
 #pragma unroll
                         for (int c = 0; c < KC; ++c)
                             tma_load_2d(st + C::OFF_X + c * C::X_CHUNK, &tmX, &sh.full[s],
@@ -238,7 +302,7 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
         // ------------------------------------------------------ MMA issuer
         constexpr uint32_t idesc = idesc_mxf4nvf4(SK_BM, NX);
         int g = 0, it = 0;
-        bool ok = true;
+        bool ok = !FUSED || sk_wait<S>(&sh.xready, 0, p, sh);
         for (int nt = blockIdx.x; ok && nt < p.n_tiles; nt += gridDim.x, ++it) {
             if (!sk_wait<S>(&sh.acc_empty, (it & 1) ^ 1, p, sh)) {
                 ok = false;
@@ -247,8 +311,7 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
             tc_fence_after();
             for (int kt = 0; kt < num_k; ++kt, ++g) {
                 const int s = g % S;
-                uint64_t *ready = FUSED ? &sh.qdone[s] : &sh.full[s];
-                if (!sk_wait<S>(ready, (g / S) & 1, p, sh)) {
+                if (!sk_wait<S>(&sh.full[s], (g / S) & 1, p, sh)) {
                     ok = false;
                     break;
                 }
@@ -257,9 +320,13 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
                 const uint32_t sf_w = tmem + C::SF_COL + s * C::SF_COLS;
                 const uint32_t sf_x = sf_w + 16 * KC;
                 const uint32_t sfw_smem = smem_addr(st + C::OFF_SFW);
-                const uint32_t sfx_smem = smem_addr(st + C::OFF_SFX);
                 const uint32_t w_smem = smem_addr(st + C::OFF_W);
-                const uint32_t x_smem = smem_addr(st + C::OFF_X);
+                // X and its scales: this stage's chunks, or (fused) the
+                // resident chunks kt * KC ..
+                const uint32_t x_smem = FUSED ? smem_addr(xres + kt * KC * C::X_CHUNK)
+                                              : smem_addr(st + C::OFF_X);
+                const uint32_t sfx_smem = FUSED ? smem_addr(sfxres + kt * KC * 2048)
+                                                : smem_addr(st + C::OFF_SFX);
                 // per K = 64 step: its two scale tiles, then the MMA, one elect
 #pragma unroll
                 for (int q = 0; q < 4 * KC; ++q) {
@@ -283,6 +350,9 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
     } else if (warp == 2) {
         // TMEM allocator only
     } else if (warp < 3 + C::EPI_WARPS) {
+        // fused: the epilogue warps first help quantize X (idle until the
+        // first accumulator is complete anyway)
+        if (FUSED) quantize_x_resident<C, S>(p, sh, xres, sfxres);
         // -------------------------------------------------------- epilogue
         const int quarter = warp & 3;
         int it = 0;
@@ -320,69 +390,7 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
         }
         __syncwarp();
     } else if (FUSED) {
-        // ------------------------------------------------ X quantizer warps
-        const int qt = threadIdx.x - 32 * (3 + C::EPI_WARPS);  // 0 .. 127
-        const int qwarp = qt >> 5;
-        float gx;
-        if (p.g_x != nullptr) {
-            gx = *p.g_x;
-        } else {
-            // g_x = amax(|X|) / (6 * 448) (1 for an all-zero X), computed by every
-            // CTA with the same integer max and IEEE division as
-            // nvfp4_global_scale, so the bytes match the unfused path
-            const uint32_t vpr = static_cast<uint32_t>(p.K / 8);
-            const uint32_t total = static_cast<uint32_t>(p.M) * vpr;
-            const uint32_t m16 = 0x7FFF7FFFu;
-            uint32_t acc = 0;
-            for (uint32_t i = qt; i < total; i += 128) {
-                const uint32_t r = i / vpr, c = i - r * vpr;
-                const uint4 v = *reinterpret_cast<const uint4 *>(p.X + r * p.ldx + c * 8ull);
-                acc = max_u16x2(acc, max_u16x2(max_u16x2(v.x & m16, v.y & m16),
-                                               max_u16x2(v.z & m16, v.w & m16)));
-            }
-            uint32_t a = max(acc & 0xFFFFu, acc >> 16);
-            a = __reduce_max_sync(kAllLanes, a);
-            if (lane == 0) sh.amax_part[qwarp] = a;
-            asm volatile("bar.sync 1, 128;" ::: "memory");  // the four quantizer warps
-            a = max(max(sh.amax_part[0], sh.amax_part[1]), max(sh.amax_part[2], sh.amax_part[3]));
-            const float amax = __uint_as_float(a << 16);
-            gx = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
-        }
-        if (qt == 0) sh.g_x = gx;
-        const int mrows = p.M < XR ? p.M : XR;
-        int g = 0;
-        bool ok = true;
-        for (int nt = blockIdx.x; ok && nt < p.n_tiles; nt += gridDim.x) {
-            for (int kt = 0; kt < num_k; ++kt, ++g) {
-                const int s = g % S;
-                if (!sk_wait<S>(&sh.full[s], (g / S) & 1, p, sh)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t *st = smem + s * C::STAGE;
-                const uint8_t *xbf = st + C::OFF_XBF;  // XR rows x 512 bytes, dense
-                uint8_t *xq = st + C::OFF_X;           // NX rows x 128 bytes, 128-byte swizzle
-                uint8_t *xsf = st + C::OFF_SFX;        // 4 scale tiles of 512 bytes
-                // the M rows present, 16 blocks of 16 elements each; rows
-                // M .. XR-1 only feed output columns that are never stored
-                for (int b = qt; b < mrows * 16; b += 128) {
-                    const int r = b >> 4, kb = b & 15;
-                    const uint4 *src = reinterpret_cast<const uint4 *>(xbf + r * 512 + kb * 32);
-                    const uint4 a = src[0], c = src[1];
-                    uint32_t lo, hi;
-                    const uint32_t Sb = quantize16(a, c, gx, lo, hi);
-                    const int chunk = kb >> 1;
-                    *reinterpret_cast<uint2 *>(xq + r * 128 + ((chunk ^ (r & 7)) << 4) +
-                                               (kb & 1) * 8) = make_uint2(lo, hi);
-                    xsf[(kb >> 2) * SK_SF_TILE + (r & 31) * 16 + (r >> 5) * 4 + (kb & 3)] =
-                        static_cast<uint8_t>(Sb);
-                }
-                fence_proxy_async_shared();  // generic-proxy writes -> tensor core reads
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.qdone[s]);
-            }
-        }
-        __syncwarp();
+        quantize_x_resident<C, S>(p, sh, xres, sfxres);
     }
 
     tc_fence_before();
@@ -408,9 +416,7 @@ cudaError_t launch_sk(const SkinnyArgs &a, cudaStream_t st) {
                 CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     if (FUSED) {
-        if (!make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.X, a.K, a.M, a.ldx * 2, SK_BK, XR,
-                    CU_TENSOR_MAP_SWIZZLE_NONE))
-            return cudaErrorInvalidValue;
+        memset(&tmX, 0, sizeof(tmX));  // X is read by the quantizer warps directly
     } else {
         if (!make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Xq, a.K / 2, a.M, a.K / 2, 128, XR,
                     CU_TENSOR_MAP_SWIZZLE_128B))
@@ -450,8 +456,11 @@ cudaError_t launch_sk(const SkinnyArgs &a, cudaStream_t st) {
 
 cudaError_t launch_gemm_skinny(const SkinnyArgs &a, cudaStream_t st) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
-    if (a.M > kSkinnyMaxM || (a.fused && a.M > kSkinnyFusedMaxM)) return cudaErrorInvalidValue;
-    if (a.fused) return launch_sk<64, 32, true, 1>(a, st);
+    if (a.M > kSkinnyMaxM) return cudaErrorInvalidValue;
+    if (a.fused) {
+        if (a.M > kSkinnyFusedMaxM || a.K > kSkinnyFusedMaxK) return cudaErrorInvalidValue;
+        return a.K % 512 == 0 ? launch_sk<64, 8, true, 2>(a, st) : launch_sk<64, 8, true, 1>(a, st);
+    }
     if (a.K % 512 == 0) {
         if (a.M <= 32) return launch_sk<64, 32, false, 2>(a, st);
         if (a.M <= 64) return launch_sk<64, 64, false, 2>(a, st);

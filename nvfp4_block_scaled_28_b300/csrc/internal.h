@@ -79,7 +79,8 @@ int gemm_use_pair();
 
 // Skinny-M GEMM (Y^T = W X^T, weights as the 128-row MMA operand).
 constexpr int64_t kSkinnyMaxM = 128;       // activation rows it handles
-constexpr int64_t kSkinnyFusedMaxM = 32;   // ... with in-kernel quantization of X
+constexpr int64_t kSkinnyFusedMaxM = 8;    // ... with in-kernel quantization of X
+constexpr int64_t kSkinnyFusedMaxK = 6144; // ... held resident in shared memory
 struct SkinnyArgs {
     const uint8_t *Wq, *Ws;  // weights: codes (N x K/2), scales (128x4 tile layout)
     const float *g_w;

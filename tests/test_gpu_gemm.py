@@ -120,11 +120,12 @@ def test_gemm_zero_sized_is_noop(nv):
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("M", [1, 3, 17, 32])
-@pytest.mark.parametrize("N,K", [(8, 256), (200, 768), (1000, 512)])
+@pytest.mark.parametrize("M", [1, 3, 8, 17, 32])
+@pytest.mark.parametrize("N,K", [(8, 256), (200, 768), (1000, 512), (300, 6144), (130, 6400)])
 def test_fused_skinny_equals_unfused(nv, oracle_mod, M, N, K):
-    """M <= 32: the fused kernel quantizes X in shared memory; its output is
-    bitwise the unfused one's, and within tolerance of the oracle."""
+    """M <= 8, K <= 6144: the fused kernel quantizes X into shared memory;
+    its output is bitwise the unfused one's (beyond those limits the fused
+    mode runs the unfused sequence), and within tolerance of the oracle."""
     x = workloads.make_x("outlier", M, K, seed=M * 131 + N)
     w = workloads.make_w(N, K, seed=N * 7 + K)
     y_unf, _ = _run_linear(nv, x, w, nv.LINEAR_UNFUSED)
@@ -136,7 +137,7 @@ def test_fused_skinny_equals_unfused(nv, oracle_mod, M, N, K):
 
 
 def test_fused_skinny_strided_x_and_given_scale(nv, oracle_mod):
-    M, N, K = 20, 384, 1024
+    M, N, K = 6, 384, 1024
     big = workloads.make_x("outlier", M, K + 256, seed=3)
     x = big[:, 128:128 + K]
     w = workloads.make_w(N, K, seed=4)
@@ -163,7 +164,7 @@ def _full_size_case(nv, oracle_mod, name, M, Nn, n_rows):
     y_ref = oracle_mod.gemm_rows(xq, xs, gx, wq, ws, gw, rows)
     y_rows = y.index_select(0, torch.from_numpy(rows).cuda())
     max_rel, floor_only = check_gemm_tolerance(bf16_bits(y_rows), y_ref, name)
-    if M <= 32:  # the fused decode path, in the configuration the benchmark times
+    if M <= 32:  # the fused mode, in the configurations the benchmark times
         y_f, _ = _run_linear(nv, x, w, nv.LINEAR_FUSED)
         assert torch.equal(y_f.view(torch.int16), y.view(torch.int16))
     print("%s M=%d N=%d: max_rel=%.3g floor_only=%d" % (name, M, Nn, max_rel, floor_only))
