@@ -166,7 +166,7 @@ NVFP4_API size_t nvfp4_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 typedef enum nvfp4_linear_mode {
     /* nvfp4_quantize into the workspace, then nvfp4_gemm. */
     NVFP4_LINEAR_UNFUSED = 0,
-    /* For M <= 8 and K <= 6144 one kernel does it all: every CTA reads the
+    /* For M <= 4 and K <= 6144 one kernel does it all: every CTA reads the
      * bfloat16 X, computes g_x when it is not given, and quantizes X once
      * into shared memory (same arithmetic, bit-identical output), so X's
      * codes never travel through HBM and no separate quantize launch is

@@ -258,14 +258,17 @@ nvfp4_status nvfp4_linear(const void *X, int64_t M, int64_t K, int64_t ldx, cons
                       static_cast<uint16_t *>(Y), ldy, 1};
         return from_cuda(launch_gemm_skinny(sa, st));
     }
-    // unfused (and fused beyond 8 rows or K = 6144, where every CTA
-    // re-quantizing X would cost more than one quantize pass)
+    // unfused (and fused beyond 4 rows or K = 6144, where every CTA
+    // re-quantizing X costs more than one quantize pass)
     cudaError_t e;
     if (g_x == nullptr) {
-        // amax partials, grid barrier and quantization in one launch (g_x
-        // into the slot), then the GEMM as its programmatic dependent
+        // one launch that also computes g_x into the slot (a small X: every
+        // CTA reduces the amax itself; else amax partials, a grid barrier,
+        // quantization), then the GEMM as its programmatic dependent
         unsigned int *counter = reinterpret_cast<unsigned int *>(ws + 64);
-        e = launch_quantize_fused(Xh, M, K, ldx, partials, counter, gx_slot, xq, xs, st);
+        e = M * K <= kQuantizeSmallElems
+                ? launch_quantize_small(Xh, M, K, ldx, gx_slot, xq, xs, st)
+                : launch_quantize_fused(Xh, M, K, ldx, partials, counter, gx_slot, xq, xs, st);
         g_x = gx_slot;
     } else {
         e = launch_quantize(Xh, M, K, ldx, g_x, xq, xs, NVFP4_SF_MMA_128x4, st);

@@ -14,14 +14,17 @@
 // streams them through a ring of stages (two 256-deep K chunks per stage
 // when K allows; 3 to 8 stages, as many as fit), X's chunk riding along.
 //
-// FUSED (M <= 8, K <= kSkinnyFusedMaxK): no codes of X ever reach HBM. At the
+// FUSED (M <= kSkinnyFusedMaxM, K <= kSkinnyFusedMaxK): no codes of X ever reach
+// HBM. At the
 // start, four quantizer warps read the bfloat16 X, compute g_x when it is not
 // given (the same integer amax and IEEE division as nvfp4_global_scale) and
 // quantize all of X (quant_math.cuh, the bytes of nvfp4_quantize) into a
 // resident shared-memory copy: E2M1 codes in 128-byte-swizzled chunks and
 // E4M3 scales in the tensor-core tile layout. The ring then streams only
-// weights. Every CTA quantizes the same small X (M K / 16 blocks, a few
-// thousand), which overlaps the weight ring filling up.
+// weights. Every CTA quantizes the same small X (M K / 16 blocks), which
+// overlaps the weight ring filling up while M is a few rows; at M = 8 the
+// 148 CTAs reading and quantizing the same rows already cost more than one
+// small quantize launch, hence the row limit.
 //
 // Warps: 0 TMA producer, 1 MMA issuer (per K = 64 step its two scale copies
 // to TMEM and the MMA under one elect.sync), 2 TMEM allocator, 3-6
@@ -173,7 +176,21 @@ __device__ __forceinline__ void quantize_x_resident(const SkParams &p, SkShared<
         const uint32_t total = static_cast<uint32_t>(p.M) * vpr;
         const uint32_t m16 = 0x7FFF7FFFu;
         uint32_t acc = 0;
-        for (uint32_t i = qt; i < total; i += kThr) {
+        uint32_t i = qt;
+        for (; i + 7 * kThr < total; i += 8 * kThr) {  // eight loads in flight
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t j = i + u * kThr;
+                const uint32_t r = j / vpr, c = j - r * vpr;
+                v[u] = *reinterpret_cast<const uint4 *>(p.X + r * p.ldx + c * 8ull);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                acc = max_u16x2(acc, max_u16x2(max_u16x2(v[u].x & m16, v[u].y & m16),
+                                               max_u16x2(v[u].z & m16, v[u].w & m16)));
+        }
+        for (; i < total; i += kThr) {
             const uint32_t r = i / vpr, c = i - r * vpr;
             const uint4 v = *reinterpret_cast<const uint4 *>(p.X + r * p.ldx + c * 8ull);
             acc = max_u16x2(acc, max_u16x2(max_u16x2(v.x & m16, v.y & m16),
@@ -191,17 +208,36 @@ __device__ __forceinline__ void quantize_x_resident(const SkParams &p, SkShared<
     }
     if (qt == 0) sh.g_x = gx;
     const int kbpr = p.K / 16;
-    for (int b = qt; b < p.M * kbpr; b += kThr) {
-        const int r = b / kbpr, kb = b - r * kbpr;
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.X + r * p.ldx + kb * 16ll);
-        const uint4 v0 = src[0], v1 = src[1];
-        uint32_t lo, hi;
-        const uint32_t Sb = quantize16(v0, v1, gx, lo, hi);
-        const int chunk = kb >> 4, kbc = kb & 15, piece = kbc >> 1;
-        *reinterpret_cast<uint2 *>(xres + chunk * C::X_CHUNK + r * 128 + ((piece ^ (r & 7)) << 4) +
-                                   (kbc & 1) * 8) = make_uint2(lo, hi);
-        sfxres[(kb >> 2) * SK_SF_TILE + (r & 31) * 16 + (r >> 5) * 4 + (kb & 3)] =
-            static_cast<uint8_t>(Sb);
+    const int nblk = p.M * kbpr;
+    constexpr int U = 4;  // blocks per thread per round, loads issued first
+    for (int b0 = qt; b0 < nblk; b0 += U * kThr) {
+        uint4 v0[U], v1[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int b = b0 + u * kThr;
+            v0[u] = make_uint4(0, 0, 0, 0);
+            v1[u] = v0[u];
+            if (b < nblk) {
+                const int r = b / kbpr, kb = b - r * kbpr;
+                const uint4 *src = reinterpret_cast<const uint4 *>(p.X + r * p.ldx + kb * 16ll);
+                v0[u] = src[0];
+                v1[u] = src[1];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int b = b0 + u * kThr;
+            if (b >= nblk) break;
+            const int r = b / kbpr, kb = b - r * kbpr;
+            uint32_t lo, hi;
+            const uint32_t Sb = quantize16(v0[u], v1[u], gx, lo, hi);
+            const int chunk = kb >> 4, kbc = kb & 15, piece = kbc >> 1;
+            *reinterpret_cast<uint2 *>(xres + chunk * C::X_CHUNK + r * 128 +
+                                       ((piece ^ (r & 7)) << 4) + (kbc & 1) * 8) =
+                make_uint2(lo, hi);
+            sfxres[(kb >> 2) * SK_SF_TILE + (r & 31) * 16 + (r >> 5) * 4 + (kb & 3)] =
+                static_cast<uint8_t>(Sb);
+        }
     }
     fence_proxy_async_shared();  // generic-proxy writes -> tensor core reads
     __syncwarp();

@@ -53,6 +53,12 @@ cudaError_t launch_quantize_fused(const uint16_t *X, int64_t rows, int64_t cols,
                                   uint32_t *partials, unsigned int *counter, float *g_out,
                                   uint8_t *q, uint8_t *sf, cudaStream_t st);
 
+// The same for a small X (at most kQuantizeSmallElems elements) in one
+// plain launch of a few CTAs that each reduce the amax of all of X.
+constexpr int64_t kQuantizeSmallElems = 64 * 1024;
+cudaError_t launch_quantize_small(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
+                                  float *g_out, uint8_t *q, uint8_t *sf, cudaStream_t st);
+
 // Launch configuration for kernels that take part in programmatic
 // dependent launch chains.
 cudaLaunchAttribute pdl_attribute();
@@ -79,7 +85,7 @@ int gemm_use_pair();
 
 // Skinny-M GEMM (Y^T = W X^T, weights as the 128-row MMA operand).
 constexpr int64_t kSkinnyMaxM = 128;       // activation rows it handles
-constexpr int64_t kSkinnyFusedMaxM = 8;    // ... with in-kernel quantization of X
+constexpr int64_t kSkinnyFusedMaxM = 4;    // ... with in-kernel quantization of X
 constexpr int64_t kSkinnyFusedMaxK = 6144; // ... held resident in shared memory
 struct SkinnyArgs {
     const uint8_t *Wq, *Ws;  // weights: codes (N x K/2), scales (128x4 tile layout)

@@ -248,6 +248,70 @@ __global__ void __launch_bounds__(kThreads) quantize_fused_kernel(
                                                      div_kbpr, g, q, sf);
 }
 
+// Dynamic quantization of a small activation (decode rows) in one plain
+// launch: every CTA reduces the amax of all of X itself (a few hundred KB
+// from L2), so all CTAs hold the same g (integer max, one IEEE division)
+// without a grid barrier; CTA 0 stores it; each CTA then quantizes its
+// share into the tensor-core scale layout.
+__global__ void __launch_bounds__(kThreads) quantize_small_kernel(
+    const uint16_t *__restrict__ X, uint32_t rows, uint32_t rows_pad, uint32_t kbpr, uint64_t ldx,
+    FastDiv div_kbpr, uint32_t vpr, FastDiv div_vpr, float *g_out, uint8_t *__restrict__ q,
+    uint8_t *__restrict__ sf) {
+    pdl_launch_dependents();
+    pdl_wait();  // X may come from the previous kernel
+    __shared__ float g_sh;
+    {
+        const uint32_t total = rows * vpr;
+        const uint32_t m = 0x7FFF7FFFu;
+        uint32_t acc = 0;
+        // eight 16-byte loads in flight per thread
+        uint32_t i = threadIdx.x;
+        for (; i + 7 * blockDim.x < total; i += 8 * blockDim.x) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t j = i + u * blockDim.x;
+                const uint32_t r = div_vpr.div(j), c = j - r * vpr;
+                v[u] = *reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                acc = max_u16x2(acc, max_u16x2(max_u16x2(v[u].x & m, v[u].y & m),
+                                               max_u16x2(v[u].z & m, v[u].w & m)));
+        }
+        for (; i < total; i += blockDim.x) {
+            const uint32_t r = div_vpr.div(i), c = i - r * vpr;
+            const uint4 v = *reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull);
+            acc = max_u16x2(acc,
+                            max_u16x2(max_u16x2(v.x & m, v.y & m), max_u16x2(v.z & m, v.w & m)));
+        }
+        uint32_t a = max(acc & 0xFFFFu, acc >> 16);
+        a = __reduce_max_sync(0xFFFFFFFFu, a);
+        __shared__ uint32_t warp_max[kThreads / 32];
+        if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = a;
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            uint32_t b = threadIdx.x < kThreads / 32 ? warp_max[threadIdx.x] : 0u;
+            b = __reduce_max_sync(0xFFFFFFFFu, b);
+            if (threadIdx.x == 0) {
+                const float amax = __uint_as_float(b << 16);
+                g_sh = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+            }
+        }
+        __syncthreads();
+    }
+    const float g = g_sh;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+    const uint32_t total = rows * kbpr;
+    const uint32_t total_pad = rows_pad * kbpr;
+    const uint32_t stride = gridDim.x * blockDim.x;
+    constexpr int U = 4;
+    for (uint32_t base = blockIdx.x * blockDim.x + (threadIdx.x & ~31u); base < total_pad;
+         base += U * stride)
+        quantize_round<NVFP4_SF_MMA_128x4, U, false>(X, base, stride, total, total_pad, kbpr, ldx,
+                                                     div_kbpr, g, q, sf);
+}
+
 // g = amax / (6 * 448), or 1 for an all-zero tensor; in place over the cell.
 __global__ void global_scale_finalize(uint32_t *cell) {
     const float amax = __uint_as_float(*cell << 16);
@@ -329,6 +393,25 @@ cudaLaunchAttribute pdl_attribute() {
     a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     a.val.programmaticStreamSerializationAllowed = 1;
     return a;
+}
+
+cudaError_t launch_quantize_small(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
+                                  float *g_out, uint8_t *q, uint8_t *sf, cudaStream_t st) {
+    const uint32_t vpr = static_cast<uint32_t>(cols / 8);
+    const uint32_t kbpr = static_cast<uint32_t>(cols / 16);
+    const uint32_t rows_pad = static_cast<uint32_t>((rows + 127) / 128 * 128);
+    int grid = grid_for(static_cast<uint64_t>(rows_pad) * kbpr, 4);
+    if (grid > 32) grid = 32;  // each CTA reads all of X for the amax
+    cudaLaunchAttribute attr = pdl_attribute();
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.stream = st;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quantize_small_kernel, X, static_cast<uint32_t>(rows),
+                              rows_pad, kbpr, static_cast<uint64_t>(ldx), FastDiv(kbpr), vpr,
+                              FastDiv(vpr), g_out, q, sf);
 }
 
 cudaError_t launch_quantize_fused(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
