@@ -324,21 +324,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             tile_coords(pair + t * num_pairs, p.num_m_tiles, p.num_n_tiles, mt, nt);
             const uint32_t t_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + ACC_COL +
                                     static_cast<uint32_t>(half * 128);
-            uint32_t packed[64];
+            // all four 32-column loads in flight, one wait, release the
+            // accumulator to rank 0, then scale and round
+            uint32_t r[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_base + c * 32, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    packed[c * 16 + i] = pack_bf16x2(__uint_as_float(r[2 * i]) * alpha,
-                                                     __uint_as_float(r[2 * i + 1]) * alpha);
-            }
-            // accumulator drained into registers: release it to rank 0
+            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(t_base + c * 32, r[c]);
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(acc_empty0);
+            uint32_t packed[64];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    packed[c * 16 + i] = pack_bf16x2(__uint_as_float(r[c][2 * i]) * alpha,
+                                                     __uint_as_float(r[c][2 * i + 1]) * alpha);
 
             const int row0 = mt * PM + static_cast<int>(rank) * BM + quarter * 32;
             const int row = row0 + lane;
