@@ -193,6 +193,17 @@ class Direct:
                                      ws.data_ptr(), ws.numel(), self.stream)
 
 
+    def linear_bias_requant(self, X, Wq, Ws, gw, bias, Y, gy, Yq, Ys, ws):
+        M, K = X.shape
+        n = Wq.shape[0]
+        return self.lib.nvfp4_linear_bias_requant(
+            X.data_ptr(), M, K, X.stride(0), Wq.data_ptr(), Ws.data_ptr(), gw.data_ptr(), n,
+            None if bias is None else bias.data_ptr(), None if Y is None else Y.data_ptr(),
+            n if Y is None else Y.stride(0), None if gy is None else gy.data_ptr(),
+            None if Yq is None else Yq.data_ptr(), None if Ys is None else Ys.data_ptr(), None,
+            ws.data_ptr(), ws.numel(), self.stream)
+
+
 def _ok(status, what):
     if status != 0:
         raise RuntimeError("%s failed with status %d" % (what, status))
@@ -405,6 +416,41 @@ def extra_rows(torch, nv, D, workloads, peaks):
         out["dit_linear_4096x3072x%d" % n] = {"ms": ms,
                                                "TFLOP/s": 2.0 * dit.M[0] * n * dit.K / ms / 1e9}
     del Xd
+    # F1: prefill layer with the bias add and the output's NVFP4
+    # re-quantization in the GEMM epilogue, against the same layer followed
+    # by a separate quantize pass over Y
+    pf = workloads.WORKLOADS["prefill"]
+    M, n, K = pf.M[0], pf.N[0], pf.K
+    Xp = workloads.make_x(pf.x_kind, M, K, workloads.x_seed(pf), device="cuda")
+    W = workloads.make_w(n, K, workloads.w_seed(pf), device="cuda")
+    Wq, Ws, gw = nv.nvfp4_quantize_weight(W, nv.SF_MMA_128x4)
+    del W
+    bias = workloads.make_bias(n, seed=77, device="cuda")
+    Y = torch.empty((M, n), dtype=torch.bfloat16, device="cuda")
+    Yq = torch.empty((M, n // 2), dtype=torch.uint8, device="cuda")
+    Ys = torch.empty(nv.sf_shape(M, n, nv.SF_MMA_128x4), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(nv.linear_workspace_bytes(M, n, K), dtype=torch.uint8, device="cuda")
+    _ok(D.linear(Xp, Wq, Ws, gw, Y, None, 0, ws), "lin")
+    gy = nv.nvfp4_global_scale(Y)
+    fl = 2.0 * M * n * K
+    ms_lin = time_region(torch, lambda i: _ok(D.linear(Xp, Wq, Ws, gw, Y, None, 0, ws), "lin"), 20)
+    ms_seq = time_region(torch, lambda i: (_ok(D.linear(Xp, Wq, Ws, gw, Y, None, 0, ws), "lin"),
+                                           _ok(D.quantize(Y, gy, Yq, Ys, nv.SF_MMA_128x4), "q")),
+                         20)
+    ms_epi = time_region(torch, lambda i: _ok(D.linear_bias_requant(Xp, Wq, Ws, gw, bias, Y, gy,
+                                                                    Yq, Ys, ws), "epi"), 20)
+    ms_q = time_region(torch, lambda i: _ok(D.linear_bias_requant(Xp, Wq, Ws, gw, bias, None, gy,
+                                                                  Yq, Ys, ws), "epi"), 20)
+    out["prefill_linear_4096x5120x5120_epilogue"] = {
+        "linear_ms": ms_lin,
+        "linear_then_quantize_ms": ms_seq,
+        "bias_requant_fused_ms": ms_epi,
+        "bias_requant_fused_no_bf16_y_ms": ms_q,
+        "TFLOP/s_fused": fl / ms_epi / 1e9,
+        "TFLOP/s_fused_no_bf16_y": fl / ms_q / 1e9,
+    }
+    del Xp, Wq, Ws, Y, Yq, Ys, ws
+    torch.cuda.empty_cache()
     # a5: decode (weight-bandwidth bound), rotating 3 weight copies (> L2)
     dec = workloads.WORKLOADS["decode"]
     n = dec.N[0]
@@ -509,8 +555,9 @@ def run_reference(args):
 
 
 def run_single_op(args):
-    """One kernel on one shape, for profiling: --op gemm|quantize|linear
-    --shape M,N,K (quantize uses M,K). Prints the mean CUDA-event time."""
+    """One kernel on one shape, for profiling: --op gemm|quantize|linear|
+    linear_bias_requant|linear_requant_only --shape M,N,K (quantize uses
+    M,K). Prints the mean CUDA-event time."""
     import torch
 
     import nvfp4_block_scaled_28_b300 as nv
@@ -566,6 +613,20 @@ def run_single_op(args):
         if args.op == "gemm":
             Xq, Xs = nv.nvfp4_quantize(X, g, nv.SF_MMA_128x4)
             fn = lambda i: _ok(D.gemm(Xq, Xs, g, Wq, Ws, gw, M, Nn, K, Y), "gemm")
+        elif args.op in ("linear_bias_requant", "linear_requant_only"):
+            # bias add + NVFP4 re-quantization of Y in the GEMM epilogue
+            # (requant_only: no bfloat16 Y is stored)
+            ws = torch.empty(nv.linear_workspace_bytes(M, Nn, K), dtype=torch.uint8,
+                             device="cuda")
+            bias = workloads.make_bias(Nn, seed=3, device="cuda")
+            _ok(D.linear(X, Wq, Ws, gw, Y, None, nv.LINEAR_UNFUSED, ws), "linear")
+            gy = nv.nvfp4_global_scale(Y)
+            Yq = torch.empty((M, Nn // 2), dtype=torch.uint8, device="cuda")
+            Ys = torch.empty(nv.sf_shape(M, Nn, nv.SF_MMA_128x4), dtype=torch.uint8,
+                             device="cuda")
+            Yo = Y if args.op == "linear_bias_requant" else None
+            fn = lambda i: _ok(D.linear_bias_requant(X, Wq, Ws, gw, bias, Yo, gy, Yq, Ys, ws),
+                               "linear_bias_requant")
         else:
             mode = nv.LINEAR_FUSED if args.mode == "fused" else nv.LINEAR_UNFUSED
             ws = torch.empty(nv.linear_workspace_bytes(M, Nn, K, mode), dtype=torch.uint8,
@@ -590,7 +651,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the per-row extra numbers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=256)
-    ap.add_argument("--op", choices=["gemm", "quantize", "linear", "mma_peak"], default=None,
+    ap.add_argument("--op", choices=["gemm", "quantize", "linear", "linear_bias_requant",
+                                     "linear_requant_only", "mma_peak"], default=None,
                     help="time a single kernel on --shape instead of the benchmark step")
     ap.add_argument("--shape", default="8192,8192,8192", help="M,N,K for --op")
     ap.add_argument("--iters", type=int, default=200000, help="--op mma_peak: MMAs per CTA")

@@ -231,6 +231,41 @@ NVFP4_API nvfp4_status nvfp4_linear_noalloc(const void *X, int64_t M, int64_t K,
                                            const float *g_x, void *stream);
 
 /*
+ * nvfp4_linear with two epilogue steps fused into the GEMM (the pages' DiT
+ * and LLM blocks chain these linears: "nvfp4-difusion" page, section 2,
+ * BlackwellLinear.forward; the FFN's up projection feeds the down
+ * projection, whose first step would quantize this output again):
+ *   Y  = bf16( acc * g_x * g_w + bias[n] )     (bias added in fp32 before
+ *                                              the single bfloat16 rounding)
+ *   Yq, Ys = nvfp4_quantize(Y, g_y, NVFP4_SF_MMA_128x4)   (bit-identical)
+ * so the next linear can take (Yq, Ys, g_y) as its activation operand
+ * (nvfp4_gemm's A) without reading Y back from HBM.
+ * X, Wq, Ws, g_w, g_x, workspace: as nvfp4_linear (mode UNFUSED; the
+ * workspace size is nvfp4_linear_workspace_bytes(M, N, K, 0)).
+ * bias: N bfloat16 values, 16-byte aligned, or NULL for none.
+ * Y: M x N bfloat16 (ldy >= N), or NULL to skip the bfloat16 store.
+ * g_y: device float, the decode-direction global scale of Y. It is an
+ * input: the amax of Y is not known until every tile is done, so g_y comes
+ * from calibration (or from a previous step), as a static activation scale.
+ * Yq: M x N/2 bytes (row pitch N/2), 16-byte aligned.
+ * Ys: nvfp4_sf_bytes(M, N, NVFP4_SF_MMA_128x4) bytes, 16-byte aligned; the
+ * padding rows of the last 128-row group get scale 0.
+ * g_y, Yq and Ys are all given or all NULL; Y and Yq are not both NULL.
+ * Shapes: K % 256 == 0, N % 256 == 0 (one pair tile of columns, and the
+ * next layer's K rule); M > 128 (the CTA-pair kernel that carries this
+ * epilogue; fewer rows return UNSUPPORTED_SHAPE).
+ * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_SHAPE,
+ * WORKSPACE_TOO_SMALL, CUDA.
+ */
+NVFP4_API nvfp4_status nvfp4_linear_bias_requant(const void *X, int64_t M, int64_t K, int64_t ldx,
+                                                const uint8_t *Wq, const uint8_t *Ws,
+                                                const float *g_w, int64_t N, const void *bias,
+                                                void *Y, int64_t ldy, const float *g_y,
+                                                uint8_t *Yq, uint8_t *Ys, const float *g_x,
+                                                void *workspace, size_t workspace_bytes,
+                                                void *stream);
+
+/*
  * Synchronize the current device, then return NVFP4_ERR_TIMEOUT if any
  * kernel of this library recorded a bounded-wait timeout since the last
  * clear, NVFP4_ERR_CUDA if the synchronization failed, else NVFP4_OK.

@@ -21,6 +21,7 @@ from .ops import (  # noqa: F401
     nvfp4_gemm,
     nvfp4_linear,
     nvfp4_linear_noalloc,
+    nvfp4_linear_bias_requant,
     gemm_workspace_bytes,
     linear_workspace_bytes,
     nvfp4_device_error,

@@ -217,6 +217,33 @@ nvfp4_status nvfp4_gemm(const uint8_t *Aq, const uint8_t *As, const float *g_a, 
 // X codes, X scales.
 constexpr size_t kLinearHeader = 256 + sizeof(uint32_t) * kMaxAmaxPartials;
 
+}  // extern "C"
+
+namespace {
+
+// The activation quantization step of the linear layers: X -> codes and
+// tile-layout scales in the workspace. With *g_x == nullptr one launch also
+// computes g_x into the workspace header (a small X: every CTA reduces the
+// amax itself; else amax partials, a grid barrier, quantization) and *g_x is
+// pointed at it; the GEMM that follows runs as its programmatic dependent.
+cudaError_t quantize_activation(const uint16_t *Xh, int64_t M, int64_t K, int64_t ldx,
+                                const float **g_x, uint8_t *ws, cudaStream_t st) {
+    float *gx_slot = reinterpret_cast<float *>(ws);
+    uint32_t *partials = reinterpret_cast<uint32_t *>(ws + 256);
+    uint8_t *xq = ws + kLinearHeader;
+    uint8_t *xs = xq + round_up(static_cast<size_t>(M) * static_cast<size_t>(K / 2), 256);
+    if (*g_x != nullptr) return launch_quantize(Xh, M, K, ldx, *g_x, xq, xs, NVFP4_SF_MMA_128x4, st);
+    unsigned int *counter = reinterpret_cast<unsigned int *>(ws + 64);
+    *g_x = gx_slot;
+    return M * K <= kQuantizeSmallElems
+               ? launch_quantize_small(Xh, M, K, ldx, gx_slot, xq, xs, st)
+               : launch_quantize_fused(Xh, M, K, ldx, partials, counter, gx_slot, xq, xs, st);
+}
+
+}  // namespace
+
+extern "C" {
+
 size_t nvfp4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int mode) {
     if (M < 0 || N < 0 || K < 0 || K % 256 != 0) return 0;
     (void)mode;
@@ -246,8 +273,6 @@ nvfp4_status nvfp4_linear(const void *X, int64_t M, int64_t K, int64_t ldx, cons
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    float *gx_slot = reinterpret_cast<float *>(ws);
-    uint32_t *partials = reinterpret_cast<uint32_t *>(ws + 256);
     uint8_t *xq = ws + kLinearHeader;
     uint8_t *xs = xq + round_up(static_cast<size_t>(M) * static_cast<size_t>(K / 2), 256);
     const uint16_t *Xh = static_cast<const uint16_t *>(X);
@@ -260,20 +285,7 @@ nvfp4_status nvfp4_linear(const void *X, int64_t M, int64_t K, int64_t ldx, cons
     }
     // unfused (and fused beyond 4 rows or K = 6144, where every CTA
     // re-quantizing X costs more than one quantize pass)
-    cudaError_t e;
-    if (g_x == nullptr) {
-        // one launch that also computes g_x into the slot (a small X: every
-        // CTA reduces the amax itself; else amax partials, a grid barrier,
-        // quantization), then the GEMM as its programmatic dependent
-        unsigned int *counter = reinterpret_cast<unsigned int *>(ws + 64);
-        e = M * K <= kQuantizeSmallElems
-                ? launch_quantize_small(Xh, M, K, ldx, gx_slot, xq, xs, st)
-                : launch_quantize_fused(Xh, M, K, ldx, partials, counter, gx_slot, xq, xs, st);
-        g_x = gx_slot;
-    } else {
-        e = launch_quantize(Xh, M, K, ldx, g_x, xq, xs, NVFP4_SF_MMA_128x4, st);
-    }
-    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (quantize_activation(Xh, M, K, ldx, &g_x, ws, st) != cudaSuccess) return NVFP4_ERR_CUDA;
     if (M <= kSkinnyMaxM) {
         SkinnyArgs sa{Wq, Ws, g_w, xq, xs, nullptr, 0, g_x, M, N, K,
                       static_cast<uint16_t *>(Y), ldy, 0};
@@ -281,6 +293,52 @@ nvfp4_status nvfp4_linear(const void *X, int64_t M, int64_t K, int64_t ldx, cons
     }
     GemmArgs a{xq, xs, g_x, Wq, Ws, g_w, M, N, K, static_cast<uint16_t *>(Y), ldy};
     return from_cuda(gemm_use_pair() ? launch_gemm_pair(a, st) : launch_gemm(a, st));
+}
+
+nvfp4_status nvfp4_linear_bias_requant(const void *X, int64_t M, int64_t K, int64_t ldx,
+                                       const uint8_t *Wq, const uint8_t *Ws, const float *g_w,
+                                       int64_t N, const void *bias, void *Y, int64_t ldy,
+                                       const float *g_y, uint8_t *Yq, uint8_t *Ys,
+                                       const float *g_x, void *workspace, size_t workspace_bytes,
+                                       void *stream) {
+    nvfp4_status s = check_bf16_matrix(X, M, K, ldx);
+    if (s != NVFP4_OK) return s;
+    if (M < 0 || N < 0 || K <= 0) return NVFP4_ERR_INVALID_ARG;
+    const bool requant = Yq != nullptr || Ys != nullptr || g_y != nullptr;
+    if (requant && (Yq == nullptr || Ys == nullptr || g_y == nullptr)) return NVFP4_ERR_INVALID_ARG;
+    if (Y == nullptr && !requant) return NVFP4_ERR_INVALID_ARG;
+    if (Y != nullptr && ldy < N) return NVFP4_ERR_INVALID_ARG;
+    if (K % 256 != 0 || N % 256 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || N == 0) return NVFP4_OK;
+    // the epilogue lives in the CTA-pair kernel, the one used above 128 rows
+    if (M <= kSkinnyMaxM || !gemm_use_pair()) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (M * (K / 16) >= kMaxBlocks || M * (N / 16) >= kMaxBlocks)
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!Wq || !Ws || !g_w) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(Wq, 16) || !aligned(Ws, 16) || !aligned(g_w, 4)) return NVFP4_ERR_MISALIGNED;
+    if (!aligned(bias, 16) || !aligned(Y, 2) || !aligned(Yq, 16) || !aligned(Ys, 16) ||
+        !aligned(g_y, 4))
+        return NVFP4_ERR_MISALIGNED;
+    if (g_x != nullptr && !aligned(g_x, 4)) return NVFP4_ERR_MISALIGNED;
+    const size_t need = nvfp4_linear_workspace_bytes(M, N, K, NVFP4_LINEAR_UNFUSED);
+    if (workspace_bytes < need) return NVFP4_ERR_WORKSPACE_TOO_SMALL;
+    if (workspace == nullptr) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return NVFP4_ERR_MISALIGNED;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint8_t *xq = ws + kLinearHeader;
+    uint8_t *xs = xq + round_up(static_cast<size_t>(M) * static_cast<size_t>(K / 2), 256);
+    if (quantize_activation(static_cast<const uint16_t *>(X), M, K, ldx, &g_x, ws, st) !=
+        cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    GemmArgs a{xq, xs, g_x, Wq, Ws, g_w, M, N, K, static_cast<uint16_t *>(Y), Y ? ldy : N};
+    a.bias = static_cast<const uint16_t *>(bias);
+    a.g_y = g_y;
+    a.Yq = Yq;
+    a.Ys = Ys;
+    return from_cuda(launch_gemm_pair(a, st));
 }
 
 nvfp4_status nvfp4_device_error(int clear) {

@@ -44,6 +44,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant_math.cuh"
 #include "tensor_map.h"
 
 namespace nvfp4 {
@@ -102,6 +103,14 @@ struct Params {
     int num_tiles;
     int y_vec;           // rows of Y start 16-byte aligned: 16-byte stores
     int y_tma;           // Y written by TMA stores (rows 16-byte aligned, map valid)
+    int store_y;         // 0: Y is not written (re-quantized output only)
+    const uint16_t *bias;  // optional bfloat16 bias, N values
+    // optional output re-quantization (N % 256 == 0): the bfloat16 Y values
+    // quantized with g_y into codes (M x N/2) and tile-layout scales (rows
+    // padded to 128), as nvfp4_quantize would
+    const float *g_y;
+    uint8_t *Yq;
+    uint8_t *Ys;
     int inject;          // 1: the producers issue nothing (bounded-wait test)
     uint64_t timeout_ns;
     unsigned int *err;   // device error word
@@ -160,12 +169,16 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
     return __shfl_sync(kAll, ok, 0) != 0;
 }
 
+// kEpi: the bias / re-quantization epilogue (a separate instantiation, so
+// the plain kernel's registers are not spent on it).
+template <bool kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSA,
                      const __grid_constant__ CUtensorMap tmSB,
-                     const __grid_constant__ CUtensorMap tmY, const Params p) {
+                     const __grid_constant__ CUtensorMap tmY,
+                     const __grid_constant__ CUtensorMap tmYq, const Params p) {
     // tmSA: A scales as rows of 256 B (8 rows per stage); tmSB: B scales as
     // {256 B, rows of a 128-row group, group} (8 rows x 2 groups per stage)
     extern __shared__ uint8_t smem_raw[];
@@ -199,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmSA);
         tma_prefetch_desc(&tmSB);
         if (p.y_tma) tma_prefetch_desc(&tmY);
+        if (kEpi && p.Yq != nullptr) tma_prefetch_desc(&tmYq);
     }
     if (warp == 2) {
         tmem_alloc_pair(&sh.tmem_base, TMEM_COLS);
@@ -333,18 +347,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(acc_empty0);
-            uint32_t packed[64];
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    packed[c * 16 + i] = pack_bf16x2(__uint_as_float(r[c][2 * i]) * alpha,
-                                                     __uint_as_float(r[c][2 * i + 1]) * alpha);
-
             const int row0 = mt * PM + static_cast<int>(rank) * BM + quarter * 32;
             const int row = row0 + lane;
             const int n0 = nt * BN + half * 128;
-            if (p.y_tma) {
+            uint32_t packed[64];
+            if (!kEpi || p.bias == nullptr) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        packed[c * 16 + i] = pack_bf16x2(__uint_as_float(r[c][2 * i]) * alpha,
+                                                         __uint_as_float(r[c][2 * i + 1]) * alpha);
+            } else {
+                // y = acc * g_a g_b + bias[n] in fp32, then one rounding
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        const int col = n0 + c * 32 + q8 * 8;
+                        uint4 bv = make_uint4(0, 0, 0, 0);
+                        if (col + 8 <= p.N) bv = __ldg(reinterpret_cast<const uint4 *>(p.bias + col));
+                        const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int e = q8 * 8 + 2 * i;  // column within the 32-column chunk
+                            packed[c * 16 + q8 * 4 + i] = pack_bf16x2(
+                                __fadd_rn(__fmul_rn(__uint_as_float(r[c][e]), alpha), bf16_lo(bw[i])),
+                                __fadd_rn(__fmul_rn(__uint_as_float(r[c][e + 1]), alpha),
+                                          bf16_hi(bw[i])));
+                        }
+                    }
+                }
+            }
+            if (kEpi && !p.store_y) {
+                // re-quantized output only
+            } else if (p.y_tma) {
                 // 64-column chunks through this warp's staging tile (128-byte
                 // swizzle: 16-byte piece k of row r sits at piece k ^ (r % 8)),
                 // written out by one TMA store each; rows >= M and columns
@@ -383,8 +420,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            if (kEpi && p.Yq != nullptr) {
+                // re-quantize this thread's 128 bfloat16 values (8 blocks of
+                // 16) for the next layer, after the Y stores are in flight.
+                // Codes (64 bytes of the row) go through the warp's staging
+                // tile (64-byte swizzle: 16-byte piece j of row r at
+                // j ^ ((r / 2) % 4)) and one TMA store, which clips rows >= M;
+                // scales go straight to the tile layout (4 consecutive blocks
+                // = one aligned 32-bit word), 0 on padding rows M .. M
+                // rounded to 128
+                const float gy = *p.g_y;
+                uint32_t code[16];
+                uint32_t sw[2] = {0u, 0u};
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+                    const uint32_t S = quantize16(
+                        make_uint4(packed[8 * b], packed[8 * b + 1], packed[8 * b + 2],
+                                   packed[8 * b + 3]),
+                        make_uint4(packed[8 * b + 4], packed[8 * b + 5], packed[8 * b + 6],
+                                   packed[8 * b + 7]),
+                        gy, code[2 * b], code[2 * b + 1]);
+                    sw[b >> 2] |= S << (8 * (b & 3));
+                }
+                uint8_t *stage = smem + SMEM_EPI + (warp - kFirstEpiWarp) * EPI_BYTES;
+                if (lane == 0) bulk_wait_read_all();  // the Y stores have read the tile
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4 *>(stage + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) =
+                        make_uint4(code[4 * j], code[4 * j + 1], code[4 * j + 2], code[4 * j + 3]);
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmYq, stage, n0 / 2, row0);
+                    bulk_commit_group();
+                }
+                const int64_t rows_pad = (static_cast<int64_t>(p.M) + 127) / 128 * 128;
+                if (row < rows_pad) {
+                    const int kb4y = p.N / 64;
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int kb = n0 / 16 + 4 * h2;  // multiple of 4
+                        const int64_t off =
+                            ((static_cast<int64_t>(row >> 7) * kb4y + (kb >> 2)) << 9) +
+                            ((row & 31) << 4) + (((row & 127) >> 5) << 2);
+                        *reinterpret_cast<uint32_t *>(p.Ys + off) = row < p.M ? sw[h2] : 0u;
+                    }
+                }
+            }
         }
-        if (p.y_tma && lane == 0) bulk_wait_all();
+        if ((p.y_tma || (kEpi && p.Yq != nullptr)) && lane == 0) bulk_wait_all();
         __syncwarp();
     }
 
@@ -412,8 +497,11 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
     static int max_clusters = -1;
     if (max_clusters < 0) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel,
+        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(gemm_pair_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
         if (e != cudaSuccess) return e;
         max_clusters = launch_cfg().num_sms / 2;
         cudaLaunchConfig_t cfg = {};
@@ -428,7 +516,7 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel, &cfg) == cudaSuccess && n > 0 &&
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<false>, &cfg) == cudaSuccess && n > 0 &&
             n < max_clusters)
             max_clusters = n;
     }
@@ -446,10 +534,19 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
                      kb4 * SF_TILE, SF_ROW, (SFB_BYTES / 2) / SF_ROW, 2))
         return cudaErrorInvalidValue;
     CUtensorMap tmY;
-    const bool y_vec = (a.ldy % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.Y) & 15) == 0);
+    const bool store_y = a.Y != nullptr;
+    const bool y_vec =
+        store_y && (a.ldy % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.Y) & 15) == 0);
     const bool y_tma = y_vec && make_map_2d(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.Y, a.N, a.M,
                                             a.ldy * 2, EPI_CHUNK, 32, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!y_tma) memset(&tmY, 0, sizeof(tmY));
+    // re-quantized codes: rows of N/2 bytes, 32-row x 64-byte boxes
+    CUtensorMap tmYq;
+    memset(&tmYq, 0, sizeof(tmYq));
+    if (a.Yq != nullptr &&
+        !make_map_2d(&tmYq, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Yq, a.N / 2, a.M, a.N / 2, 64u, 32,
+                     CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
     Params p;
     p.g_a = a.g_a;
     p.g_b = a.g_b;
@@ -463,6 +560,11 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     p.num_tiles = p.num_m_tiles * p.num_n_tiles;
     p.y_vec = y_vec;
     p.y_tma = y_tma;
+    p.store_y = store_y ? 1 : 0;
+    p.bias = a.bias;
+    p.g_y = a.g_y;
+    p.Yq = a.Yq;
+    p.Ys = a.Ys;
     p.inject = debug_state().inject;
     p.timeout_ns = debug_state().timeout_ns;
     p.err = device_error_word();
@@ -481,7 +583,11 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_pair_kernel, tmA, tmB, tmSA, tmSB, tmY, p);
+    const bool epi = !store_y || a.bias != nullptr || a.Yq != nullptr;
+    cudaError_t e = epi ? cudaLaunchKernelEx(&cfg, gemm_pair_kernel<true>, tmA, tmB, tmSA, tmSB,
+                                             tmY, tmYq, p)
+                        : cudaLaunchKernelEx(&cfg, gemm_pair_kernel<false>, tmA, tmB, tmSA, tmSB,
+                                             tmY, tmYq, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -72,8 +72,16 @@ struct GemmArgs {
     const uint8_t *Bq, *Bs;
     const float *g_b;
     int64_t M, N, K;
-    uint16_t *Y;
+    uint16_t *Y;  // nullptr: the bfloat16 output is not stored
     int64_t ldy;
+    // Epilogue extensions (CTA-pair kernel only): a bfloat16 bias of N added
+    // to every row before the bfloat16 rounding, and the NVFP4 re-quantization
+    // of the bfloat16 output with the decode-direction global scale *g_y into
+    // Yq (M x N/2 bytes, dense) and Ys (the 128x4 tile layout, rows padded).
+    const uint16_t *bias = nullptr;
+    const float *g_y = nullptr;
+    uint8_t *Yq = nullptr;
+    uint8_t *Ys = nullptr;
 };
 
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st);

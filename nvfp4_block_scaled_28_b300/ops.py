@@ -225,6 +225,57 @@ def nvfp4_linear_noalloc(X: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor,
     return Y
 
 
+def nvfp4_linear_bias_requant(X: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor,
+                              g_w: torch.Tensor, g_y: torch.Tensor | None,
+                              bias: torch.Tensor | None = None, g_x: torch.Tensor | None = None,
+                              store_y: bool = True, Y: torch.Tensor | None = None,
+                              Yq: torch.Tensor | None = None, Ys: torch.Tensor | None = None,
+                              workspace: torch.Tensor | None = None):
+    """nvfp4_linear with the bias add and the NVFP4 re-quantization of the
+    bfloat16 output fused into the GEMM epilogue. Returns (Y, Yq, Ys):
+    Y is None when store_y is False; Yq (M, N/2) codes and Ys tile-layout
+    scales of Y under the global scale g_y are None when g_y is None."""
+    _check_bf16_2d(X, "X")
+    M, K = X.shape
+    Nn = Wq.shape[0]
+    _check_codes(Wq, Nn, K, "Wq")
+    _check_scales(Ws, Nn, K, SF_MMA_128x4, "Ws")
+    _check_g(g_w, "g_w")
+    if g_x is not None:
+        _check_g(g_x, "g_x")
+    if g_y is not None:
+        _check_g(g_y, "g_y")
+    if bias is not None:
+        _require(bias.dtype == torch.bfloat16 and tuple(bias.shape) == (Nn,)
+                 and bias.is_contiguous(), "bias must be a contiguous bfloat16 vector of %d" % Nn)
+    _check_cuda(X, Wq, Ws, g_w, g_x, g_y, bias, Y, Yq, Ys, workspace)
+    if store_y:
+        if Y is None:
+            Y = torch.empty((M, Nn), dtype=torch.bfloat16, device=X.device)
+        _check_bf16_2d(Y, "Y")
+        _require(tuple(Y.shape) == (M, Nn), "Y must have shape (%d, %d)" % (M, Nn))
+    else:
+        Y = None
+    if g_y is not None:
+        if Yq is None:
+            Yq = torch.empty((M, Nn // 2), dtype=torch.uint8, device=X.device)
+        if Ys is None:
+            Ys = torch.empty(sf_shape(M, Nn, SF_MMA_128x4), dtype=torch.uint8, device=X.device)
+        _check_codes(Yq, M, Nn, "Yq")
+        _check_scales(Ys, M, Nn, SF_MMA_128x4, "Ys")
+    else:
+        Yq = Ys = None
+    need = linear_workspace_bytes(M, Nn, K, LINEAR_UNFUSED)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=X.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    N.check("nvfp4_linear_bias_requant", N.load().nvfp4_linear_bias_requant(
+        _ptr(X), M, K, X.stride(0), _ptr(Wq), _ptr(Ws), _ptr(g_w), Nn, _ptr(bias), _ptr(Y),
+        Nn if Y is None else Y.stride(0), _ptr(g_y), _ptr(Yq), _ptr(Ys), _ptr(g_x),
+        _ptr(workspace), ws_bytes, _stream()))
+    return Y, Yq, Ys
+
+
 def nvfp4_device_error(clear: bool = True) -> int:
     """Synchronize and return the device-side status (OK or ERR_TIMEOUT)."""
     return int(N.load().nvfp4_device_error(1 if clear else 0))

@@ -89,3 +89,12 @@ def make_w(N: int, K: int, seed: int, std: float = 0.02, device: str = "cpu") ->
     g = torch.Generator(device=device).manual_seed(seed)
     w = torch.randn((N, K), generator=g, dtype=torch.float32, device=device) * std
     return w.to(torch.bfloat16)
+
+
+def make_bias(N: int, seed: int, std: float = 0.5, device: str = "cpu") -> torch.Tensor:
+    """Bias vector (N,) bfloat16 (CPU generator by default), on the scale of
+    the linear layers' outputs (unit-variance activations against 0.02-std
+    weights over thousands of inputs give outputs of order 1)."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    b = torch.randn((N,), generator=g, dtype=torch.float32, device=device) * std
+    return b.to(torch.bfloat16)

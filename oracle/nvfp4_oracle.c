@@ -234,7 +234,10 @@ void oracle_dequantize(const uint8_t *q, const uint8_t *sf, float g,
 /* ----------------------------------------------------------------- GEMM */
 
 /* Y[m, n] = bf16( (sum_k e2m1(Xq[m,k]) s_x[m,k/16] e2m1(Wq[n,k]) s_w[n,k/16])
- *                 * g_x * g_w ), the sum in FP64 in increasing k.
+ *                 * g_x * g_w + bias[n] ), the sum in FP64 in increasing k; bias
+ * is an optional bfloat16 vector of N (NULL: no bias) added exactly in FP64
+ * before the one rounding to bfloat16 (the linear layer's bias, applied where
+ * the pages' forward() applies it: to the matmul output).
  * Row-major operands: Xq M x K/2, Xs M x K/16, Wq N x K/2, Ws N x K/16.
  * Only the n_rows rows listed in row_ids (or all M rows if row_ids is NULL,
  * then n_rows must be M) are computed; output row i of Y (and of Yd, if not
@@ -243,7 +246,7 @@ void oracle_gemm_rows(const uint8_t *Xq, const uint8_t *Xs, float g_x,
                       const uint8_t *Wq, const uint8_t *Ws, float g_w,
                       int64_t M, int64_t N, int64_t K,
                       const int64_t *row_ids, int64_t n_rows,
-                      uint16_t *Y, double *Yd)
+                      const uint16_t *bias, uint16_t *Y, double *Yd)
 {
     (void)M;
     int64_t kh = K / 2, nb = K / 16;
@@ -276,6 +279,8 @@ void oracle_gemm_rows(const uint8_t *Xq, const uint8_t *Xs, float g_x,
                     acc += xrow[k] * (e2m1[code] * e4m3[ws[k / 16]]);
                 }
                 double y = acc * alpha;
+                if (bias)
+                    y += (double)bf16_to_float(bias[n]);
                 if (Yd)
                     Yd[i * N + n] = y;
                 if (Y)
@@ -290,7 +295,7 @@ void oracle_gemm(const uint8_t *Xq, const uint8_t *Xs, float g_x,
                  const uint8_t *Wq, const uint8_t *Ws, float g_w,
                  int64_t M, int64_t N, int64_t K, uint16_t *Y, double *Yd)
 {
-    oracle_gemm_rows(Xq, Xs, g_x, Wq, Ws, g_w, M, N, K, NULL, M, Y, Yd);
+    oracle_gemm_rows(Xq, Xs, g_x, Wq, Ws, g_w, M, N, K, NULL, M, NULL, Y, Yd);
 }
 
 /* ------------------------------------------- generic symmetric integer map */

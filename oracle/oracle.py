@@ -74,7 +74,7 @@ def _load():
         lib.oracle_gemm_rows.restype = None
         lib.oracle_gemm_rows.argtypes = [_u8p, _u8p, ctypes.c_float, _u8p, _u8p,
                                          ctypes.c_float, _i64, _i64, _i64,
-                                         _i64p, _i64, _u16p, _f64p]
+                                         _i64p, _i64, _u16p, _u16p, _f64p]
         lib.oracle_symmetric_quantize.restype = ctypes.c_double
         lib.oracle_symmetric_quantize.argtypes = [_f64p, _i64, ctypes.c_int,
                                                   _i32p, _f64p]
@@ -149,10 +149,11 @@ def dequantize(q: np.ndarray, s: np.ndarray, g: float) -> np.ndarray:
     return out
 
 
-def gemm_rows(xq, xs, g_x, wq, ws, g_w, rows=None, want_fp64=False):
-    """Reference Y = bf16((Xhat @ What^T) * g_x * g_w) for the listed rows of
-    X (all rows if ``rows`` is None). Returns uint16 bf16 bits (and the FP64
-    values before rounding when ``want_fp64``)."""
+def gemm_rows(xq, xs, g_x, wq, ws, g_w, rows=None, want_fp64=False, bias=None):
+    """Reference Y = bf16((Xhat @ What^T) * g_x * g_w + bias) for the listed
+    rows of X (all rows if ``rows`` is None; ``bias``: optional bfloat16 bits,
+    uint16 of length N, added in FP64 before the rounding). Returns uint16
+    bf16 bits (and the FP64 values before rounding when ``want_fp64``)."""
     xq = _c(xq, np.uint8)
     xs = _c(xs, np.uint8)
     wq = _c(wq, np.uint8)
@@ -168,16 +169,20 @@ def gemm_rows(xq, xs, g_x, wq, ws, g_w, rows=None, want_fp64=False):
         n_rows = ids.shape[0]
     y = np.empty((n_rows, N), np.uint16)
     yd = np.empty((n_rows, N), np.float64) if want_fp64 else None
+    b = None if bias is None else _c(bias, np.uint16)
+    if b is not None:
+        assert b.shape == (N,)
     _load().oracle_gemm_rows(
         _ptr(xq, _u8p), _ptr(xs, _u8p), float(g_x), _ptr(wq, _u8p),
         _ptr(ws, _u8p), float(g_w), M, N, K,
         None if ids is None else _ptr(ids, _i64p), n_rows,
+        None if b is None else _ptr(b, _u16p),
         _ptr(y, _u16p), None if yd is None else _ptr(yd, _f64p))
     return (y, yd) if want_fp64 else y
 
 
-def gemm(xq, xs, g_x, wq, ws, g_w, want_fp64=False):
-    return gemm_rows(xq, xs, g_x, wq, ws, g_w, None, want_fp64)
+def gemm(xq, xs, g_x, wq, ws, g_w, want_fp64=False, bias=None):
+    return gemm_rows(xq, xs, g_x, wq, ws, g_w, None, want_fp64, bias)
 
 
 def symmetric_quantize(x, bits: int):

@@ -137,3 +137,23 @@ def test_mma_peak_probe_argument_checks(lib):
     assert p(0, 8, 0, A16, None) == N.ERR_INVALID_ARG
     assert p(1, 8, 0, None, None) == N.ERR_INVALID_ARG
     assert p(1, 8, 0, A16 + 4, None) == N.ERR_MISALIGNED
+
+
+def test_linear_bias_requant_argument_checks(lib):
+    f = lib.nvfp4_linear_bias_requant
+    base = dict(X=A16, M=256, K=512, ldx=512, Wq=A16, Ws=A16, gw=A16, N=512, bias=A16, Y=A16,
+                ldy=512, gy=A16, Yq=A16, Ys=A16, gx=None, ws=A16 * 16, wsb=1 << 30)
+    call = lambda **kw: f(*[{**base, **kw}[k] for k in base], None)
+    assert call(M=128) == N.ERR_UNSUPPORTED_SHAPE       # the CTA-pair kernel: M > 128
+    assert call(N=384, ldy=384) == N.ERR_UNSUPPORTED_SHAPE  # N % 256
+    assert call(K=448, ldx=448) == N.ERR_UNSUPPORTED_SHAPE  # K % 256
+    assert call(Y=None, gy=None, Yq=None, Ys=None) == N.ERR_INVALID_ARG  # no output at all
+    assert call(Ys=None) == N.ERR_INVALID_ARG            # requant outputs all or none
+    assert call(gy=None) == N.ERR_INVALID_ARG
+    assert call(ldy=100) == N.ERR_INVALID_ARG
+    assert call(bias=A16 + 8) == N.ERR_MISALIGNED         # bias read 16 bytes at a time
+    assert call(Yq=A16 + 8) == N.ERR_MISALIGNED
+    assert call(gy=ODD) == N.ERR_MISALIGNED
+    assert call(wsb=16) == N.ERR_WORKSPACE_TOO_SMALL
+    assert call(ws=A16 + 16) == N.ERR_MISALIGNED
+    assert call(M=0) == N.OK and call(N=0, ldy=0) == N.OK  # empty: nothing launched

@@ -1,0 +1,165 @@
+"""GPU parity of the linear layer's fused epilogue: bias add and the NVFP4
+re-quantization of the bfloat16 output for the next layer.
+
+Y is checked against the oracle's FP64 contraction plus bias, rounded once to
+bfloat16, within |y - y_ref| <= 2^-7 |y_ref| + 1e-3 ||Y_ref[m,:]||_2. The
+re-quantized codes and scales must equal, bit for bit, the oracle's
+quantization of the GPU's own Y with the same g_y (the rounding decisions are
+taken on the same bfloat16 values on both sides).
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import bf16_bits, check_gemm_tolerance, sf_rowmajor_to_mma, to_np_u8
+from nvfp4_block_scaled_28_b300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nv():
+    import nvfp4_block_scaled_28_b300 as nv
+    nv.load_library()
+    assert torch.cuda.is_available(), "CUDA device required"
+    nv.nvfp4_device_error(clear=True)
+    return nv
+
+
+def _case(nv, oracle_mod, M, N, K, seed, kind="outlier"):
+    x = workloads.make_x(kind, M, K, seed=seed)
+    w = workloads.make_w(N, K, seed=seed + 1)
+    b = workloads.make_bias(N, seed=seed + 2)
+    xb, wb, bb = bf16_bits(x), bf16_bits(w), bf16_bits(b)
+    gx, gw = oracle_mod.global_scale(xb), oracle_mod.global_scale(wb)
+    xq, xs = oracle_mod.quantize(xb, gx)
+    wq, ws = oracle_mod.quantize(wb, gw)
+    Wq, Ws, g_w = nv.nvfp4_quantize_weight(w.cuda(), nv.SF_MMA_128x4)
+    assert np.array_equal(to_np_u8(Wq), wq)
+    return dict(x=x, b=b, bb=bb, ops=(xq, xs, gx, wq, ws, gw), W=(Wq, Ws, g_w))
+
+
+def _gy(value) -> torch.Tensor:
+    return torch.tensor([np.float32(value)], dtype=torch.float32, device="cuda")
+
+
+def _check_requant(oracle_mod, y_bits, g_y, Yq, Ys, label):
+    """GPU (Yq, Ys) == the oracle's quantization of the GPU's Y under g_y."""
+    q_ref, s_ref = oracle_mod.quantize(y_bits, float(np.float32(g_y)))
+    q = to_np_u8(Yq)
+    assert np.array_equal(q, q_ref), "%s: codes differ at %s" % (
+        label, np.argwhere(q != q_ref)[:4].tolist())
+    s = to_np_u8(Ys)
+    s_mma = sf_rowmajor_to_mma(s_ref)
+    assert s.shape == s_mma.shape
+    assert np.array_equal(s, s_mma), "%s: %d scale bytes differ" % (label, int((s != s_mma).sum()))
+
+
+EPI_SHAPES = [  # (M, N, K): M > 128; N % 256 == 0; ragged M, several N tiles
+    (129, 256, 256), (256, 512, 512), (300, 768, 768), (513, 1024, 1280),
+]
+
+
+@pytest.mark.parametrize("M,N,K", EPI_SHAPES)
+def test_bias_and_requant_match_oracle(nv, oracle_mod, M, N, K):
+    c = _case(nv, oracle_mod, M, N, K, seed=M * 7 + N + K)
+    xq, xs, gx, wq, ws, gw = c["ops"]
+    y_ref = oracle_mod.gemm(xq, xs, gx, wq, ws, gw, bias=c["bb"])
+    g_y = oracle_mod.global_scale(y_ref)  # calibrated on the reference output
+    Wq, Ws, g_w = c["W"]
+    Y, Yq, Ys = nv.nvfp4_linear_bias_requant(c["x"].cuda(), Wq, Ws, g_w, _gy(g_y),
+                                             bias=c["b"].cuda())
+    y_bits = bf16_bits(Y)
+    max_rel, floor_only = check_gemm_tolerance(y_bits, y_ref, "bias %dx%dx%d" % (M, N, K))
+    _check_requant(oracle_mod, y_bits, g_y, Yq, Ys, "requant %dx%dx%d" % (M, N, K))
+    print("bias+requant %dx%dx%d max_rel=%.3g floor_only=%d" % (M, N, K, max_rel, floor_only))
+    assert nv.nvfp4_device_error() == 0
+
+
+def test_requant_only_equals_with_y_and_saturates(nv, oracle_mod):
+    """Skipping the bfloat16 store changes nothing else; a g_y calibrated too
+    small (amax / (6 * 448) of a quarter of the output) saturates scales at
+    448 and codes at 6 on both sides alike."""
+    M, N, K = 384, 512, 1024
+    c = _case(nv, oracle_mod, M, N, K, seed=99, kind="token_scaled")
+    xq, xs, gx, wq, ws, gw = c["ops"]
+    Wq, Ws, g_w = c["W"]
+    xd, bd = c["x"].cuda(), c["b"].cuda()
+    y_ref = oracle_mod.gemm(xq, xs, gx, wq, ws, gw, bias=c["bb"])
+    g_small = oracle_mod.global_scale(y_ref) / 4.0
+    Y, Yq, Ys = nv.nvfp4_linear_bias_requant(xd, Wq, Ws, g_w, _gy(g_small), bias=bd)
+    _check_requant(oracle_mod, bf16_bits(Y), g_small, Yq, Ys, "saturating")
+    assert (to_np_u8(Ys) == 0x7E).any()  # 448 in E4M3
+    Y2, Yq2, Ys2 = nv.nvfp4_linear_bias_requant(xd, Wq, Ws, g_w, _gy(g_small), bias=bd,
+                                                store_y=False)
+    assert Y2 is None
+    assert torch.equal(Yq2, Yq) and torch.equal(Ys2, Ys)
+    assert nv.nvfp4_device_error() == 0
+
+
+def test_no_bias_no_requant_equals_linear(nv, oracle_mod):
+    """With neither step the epilogue kernel writes what nvfp4_linear does."""
+    M, N, K = 640, 768, 768
+    c = _case(nv, oracle_mod, M, N, K, seed=5)
+    Wq, Ws, g_w = c["W"]
+    xd = c["x"].cuda()
+    Y, Yq, Ys = nv.nvfp4_linear_bias_requant(xd, Wq, Ws, g_w, None)
+    assert Yq is None and Ys is None
+    Y_lin = nv.nvfp4_linear(xd, Wq, Ws, g_w)
+    assert torch.equal(Y.view(torch.int16), Y_lin.view(torch.int16))
+    # bias only, given g_x: Y matches the oracle with the bias
+    xq, xs, gx, wq, ws, gw = c["ops"]
+    Yb, _, _ = nv.nvfp4_linear_bias_requant(xd, Wq, Ws, g_w, None, bias=c["b"].cuda(),
+                                            g_x=_gy(gx))
+    check_gemm_tolerance(bf16_bits(Yb), oracle_mod.gemm(xq, xs, gx, wq, ws, gw, bias=c["bb"]),
+                         "bias only")
+    assert nv.nvfp4_device_error() == 0
+
+
+def test_chained_layers(nv, oracle_mod):
+    """The re-quantized output feeds the next layer's GEMM directly: layer 2
+    on (Yq, Ys, g_y) matches the oracle's layer 2 on the oracle's own
+    quantization of layer 1's output."""
+    M, N1, K, N2 = 257, 1024, 512, 384
+    c = _case(nv, oracle_mod, M, N1, K, seed=11)
+    Wq, Ws, g_w = c["W"]
+    xq, xs, gx, wq, ws, gw = c["ops"]
+    y_ref = oracle_mod.gemm(xq, xs, gx, wq, ws, gw, bias=c["bb"])
+    g_y = oracle_mod.global_scale(y_ref)
+    Y, Yq, Ys = nv.nvfp4_linear_bias_requant(c["x"].cuda(), Wq, Ws, g_w, _gy(g_y),
+                                             bias=c["b"].cuda())
+    w2 = workloads.make_w(N2, N1, seed=12)
+    w2b = bf16_bits(w2)
+    gw2 = oracle_mod.global_scale(w2b)
+    w2q, w2s = oracle_mod.quantize(w2b, gw2)
+    W2q, W2s, g_w2 = nv.nvfp4_quantize_weight(w2.cuda(), nv.SF_MMA_128x4)
+    y2 = nv.nvfp4_gemm(Yq, Ys, _gy(g_y), W2q, W2s, g_w2, N1)
+    yq_ref, ys_ref = oracle_mod.quantize(bf16_bits(Y), float(np.float32(g_y)))
+    y2_ref = oracle_mod.gemm(yq_ref, ys_ref, g_y, w2q, w2s, gw2)
+    check_gemm_tolerance(bf16_bits(y2), y2_ref, "chained")
+    assert nv.nvfp4_device_error() == 0
+
+
+def test_full_size_prefill_bias_requant(nv, oracle_mod):
+    """The 4096 x 5120 x 5120 layer with both epilogue steps: sampled rows of
+    Y against the oracle, every code and scale against the oracle's
+    quantization of the GPU's Y."""
+    w_ = workloads.WORKLOADS["prefill"]
+    M, N, K = 4096, 5120, w_.K
+    x = workloads.make_x(w_.x_kind, M, K, workloads.x_seed(w_))
+    w = workloads.make_w(N, K, workloads.w_seed(w_))
+    b = workloads.make_bias(N, seed=77)
+    xb, wb, bb = bf16_bits(x), bf16_bits(w), bf16_bits(b)
+    gx, gw = oracle_mod.global_scale(xb), oracle_mod.global_scale(wb)
+    xq, xs = oracle_mod.quantize(xb, gx)
+    wq, ws = oracle_mod.quantize(wb, gw)
+    Wq, Ws, g_w = nv.nvfp4_quantize_weight(w.cuda(), nv.SF_MMA_128x4)
+    rows = np.unique(np.concatenate([[0, M - 1],
+                                     np.random.default_rng(3).choice(M, 24, replace=False)]))
+    y_ref = oracle_mod.gemm_rows(xq, xs, gx, wq, ws, gw, rows, bias=bb)
+    g_y = oracle_mod.global_scale(y_ref)
+    Y, Yq, Ys = nv.nvfp4_linear_bias_requant(x.cuda(), Wq, Ws, g_w, _gy(g_y), bias=b.cuda())
+    y_bits = bf16_bits(Y)
+    check_gemm_tolerance(y_bits[rows], y_ref, "prefill bias")
+    _check_requant(oracle_mod, y_bits, g_y, Yq, Ys, "prefill requant")
+    assert nv.nvfp4_device_error() == 0

@@ -413,6 +413,31 @@ def test_gemm_selects_one_column(oracle_mod):
     assert np.array_equal(yd, xh)
 
 
+def test_gemm_bias_is_added_before_the_rounding(oracle_mod):
+    """Bias pins: zero bias reproduces the plain product; with all-zero
+    weights Y is the bias itself, bit for bit; in general the FP64 value is
+    the numpy product plus the bias (exact decode of the bias' bfloat16)."""
+    rng = np.random.default_rng(53)
+    M, N, K = 7, 11, 64
+    x = bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    w = bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    gx, gw = oracle_mod.global_scale(x), oracle_mod.global_scale(w)
+    xq, xs = oracle_mod.quantize(x, gx)
+    wq, ws = oracle_mod.quantize(w, gw)
+    y0 = oracle_mod.gemm(xq, xs, gx, wq, ws, gw)
+    assert np.array_equal(oracle_mod.gemm(xq, xs, gx, wq, ws, gw, bias=np.zeros(N, np.uint16)), y0)
+    bias = bf16_bits((rng.standard_normal(N) * 3).astype(np.float32))
+    bias_f = torch.from_numpy(bias.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    zq = np.zeros_like(wq)
+    zs = np.zeros_like(ws)
+    yb = oracle_mod.gemm(xq, xs, gx, zq, zs, gw, bias=bias)
+    assert np.array_equal(yb, np.tile(bias, (M, 1)))
+    y, yd = oracle_mod.gemm(xq, xs, gx, wq, ws, gw, want_fp64=True, bias=bias)
+    ref = _dequant_indep(xq, xs, 1.0) @ _dequant_indep(wq, ws, 1.0).T * (gx * gw) + bias_f
+    assert np.allclose(yd, ref, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(y, np.vectorize(oracle_mod.bf16_from_double, otypes=[np.uint16])(yd))
+
+
 # -------------------------------------------------------- page worked example
 
 def test_symmetric_int8_worked_example(oracle_mod):
