@@ -193,6 +193,13 @@ class Direct:
                                      ws.data_ptr(), ws.numel(), self.stream)
 
 
+    def linear_grouped(self, X, Wq, Ws, gw, group_n_arr, groups, Y, mode, ws):
+        M, K = X.shape
+        return self.lib.nvfp4_linear_grouped(
+            X.data_ptr(), M, K, X.stride(0), Wq.data_ptr(), Ws.data_ptr(), gw.data_ptr(),
+            group_n_arr, groups, Y.data_ptr(), Y.stride(0), None, mode, ws.data_ptr(),
+            ws.numel(), self.stream)
+
     def linear_bias_requant(self, X, Wq, Ws, gw, bias, Y, gy, Yq, Ys, ws):
         M, K = X.shape
         n = Wq.shape[0]
@@ -415,7 +422,32 @@ def extra_rows(torch, nv, D, workloads, peaks):
         ms = time_region(torch, lambda i: _ok(D.linear(Xd, Wq, Ws, gw, Y, None, 0, ws), "lin"), 20)
         out["dit_linear_4096x3072x%d" % n] = {"ms": ms,
                                                "TFLOP/s": 2.0 * dit.M[0] * n * dit.K / ms / 1e9}
-    del Xd
+    # F4: the attention's q, k, v projections (3 x 3072) as one grouped call
+    # (X quantized once, one GEMM launch) against three separate linears
+    import ctypes
+    qkv = [nv.nvfp4_quantize_weight(workloads.make_w(3072, dit.K, workloads.w_seed(dit) + 7 + i,
+                                                     device="cuda"), nv.SF_MMA_128x4)
+           for i in range(3)]
+    Wq3, Ws3, g3, gn3 = nv.pack_weight_groups(qkv)
+    gn_arr = (ctypes.c_int64 * 3)(*gn3)
+    gn_ptr = ctypes.cast(gn_arr, ctypes.c_void_p)
+    Y3 = torch.empty((dit.M[0], sum(gn3)), dtype=torch.bfloat16, device="cuda")
+    ws3 = torch.empty(nv.linear_workspace_bytes(dit.M[0], sum(gn3), dit.K), dtype=torch.uint8,
+                      device="cuda")
+    Ysep = [torch.empty((dit.M[0], 3072), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    ms_g = time_region(torch, lambda i: _ok(D.linear_grouped(Xd, Wq3, Ws3, g3, gn_ptr, 3, Y3, 0,
+                                                             ws3), "grouped"), 20)
+
+    def sep(i):
+        for (wq_, ws_, gw_), y_ in zip(qkv, Ysep):
+            _ok(D.linear(Xd, wq_, ws_, gw_, y_, None, 0, ws3), "lin")
+
+    ms_s = time_region(torch, sep, 20)
+    fl3 = 2.0 * dit.M[0] * sum(gn3) * dit.K
+    out["dit_qkv_grouped_4096x3072x(3x3072)"] = {
+        "grouped_ms": ms_g, "separate_ms": ms_s, "TFLOP/s_grouped": fl3 / ms_g / 1e9,
+        "TFLOP/s_separate": fl3 / ms_s / 1e9}
+    del Xd, qkv, Wq3, Ws3, Y3, ws3, Ysep
     # F1: prefill layer with the bias add and the output's NVFP4
     # re-quantization in the GEMM epilogue, against the same layer followed
     # by a separate quantize pass over Y

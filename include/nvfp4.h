@@ -201,6 +201,37 @@ NVFP4_API nvfp4_status nvfp4_linear(const void *X, int64_t M, int64_t K, int64_t
 NVFP4_API size_t nvfp4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int mode);
 
 /*
+ * Grouped projection: several linear layers that read the same activation
+ * (the attention's to_q / to_k / to_v, which the "nvfp4-difusion" page's
+ * checkpoint stores as one fused qkv matrix sliced in thirds, section 2;
+ * those projections are most of the DiT's compute, section 1) in one call:
+ * X is quantized once and one GEMM launch computes every group, each with
+ * its own weight global scale (or all equal, for slices of one matrix).
+ *   Y[:, cols of group g] = bf16( dequant(quantize(X, g_x)) *
+ *                                 dequant(Wq_g, Ws_g, g_w[g])^T )
+ * Bitwise equal to `groups` separate nvfp4_linear calls on the groups.
+ * Wq: the groups' codes stacked by rows (sum(group_n) x K/2); Ws: their
+ * NVFP4_SF_MMA_128x4 scales stacked the same way (each group's tile-layout
+ * scales are whole 128-row tiles, so stacking the byte arrays is the
+ * layout of the stacked weight).
+ * g_w: device array of `groups` floats, one per group.
+ * group_n: host array of `groups` output-column counts, each > 0 and a
+ * multiple of 256; 1 <= groups <= 8.
+ * Y: M x sum(group_n) bfloat16 (ldy >= sum(group_n)); group g's output
+ * starts at column sum(group_n[0..g-1]).
+ * X, g_x, mode, workspace (nvfp4_linear_workspace_bytes(M, sum(group_n),
+ * K, mode)): as nvfp4_linear.
+ * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_SHAPE,
+ * WORKSPACE_TOO_SMALL, CUDA.
+ */
+NVFP4_API nvfp4_status nvfp4_linear_grouped(const void *X, int64_t M, int64_t K, int64_t ldx,
+                                           const uint8_t *Wq, const uint8_t *Ws,
+                                           const float *g_w, const int64_t *group_n,
+                                           int groups, void *Y, int64_t ldy, const float *g_x,
+                                           int mode, void *workspace, size_t workspace_bytes,
+                                           void *stream);
+
+/*
  * nvfp4_linear for callers that cannot allocate device memory. The pages
  * have no counterpart: this is a deployment variant of nvfp4_linear.
  *

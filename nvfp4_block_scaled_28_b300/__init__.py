@@ -22,6 +22,8 @@ from .ops import (  # noqa: F401
     nvfp4_linear,
     nvfp4_linear_noalloc,
     nvfp4_linear_bias_requant,
+    nvfp4_linear_grouped,
+    pack_weight_groups,
     gemm_workspace_bytes,
     linear_workspace_bytes,
     nvfp4_device_error,

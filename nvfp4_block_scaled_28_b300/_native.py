@@ -48,6 +48,8 @@ SIGNATURES = {
     "nvfp4_linear": (_INT, [_P, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _I64, _P, _INT, _P,
                             _SZ, _P]),
     "nvfp4_linear_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
+    "nvfp4_linear_grouped": (_INT, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _INT, _P, _I64, _P,
+                                    _INT, _P, _SZ, _P]),
     "nvfp4_linear_noalloc": (_INT, [_P, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _I64, _P, _P]),
     "nvfp4_linear_bias_requant": (_INT, [_P, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _P, _I64,
                                          _P, _P, _P, _P, _P, _SZ, _P]),

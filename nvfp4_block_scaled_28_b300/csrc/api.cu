@@ -254,16 +254,24 @@ size_t nvfp4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int mode) {
     return bytes;
 }
 
-nvfp4_status nvfp4_linear(const void *X, int64_t M, int64_t K, int64_t ldx, const uint8_t *Wq,
-                          const uint8_t *Ws, const float *g_w, int64_t N, void *Y, int64_t ldy,
-                          const float *g_x, int mode, void *workspace, size_t workspace_bytes,
-                          void *stream) {
+}  // extern "C"
+
+namespace {
+
+// nvfp4_linear and nvfp4_linear_grouped: `wg` describes the weight groups
+// (count 0: one group, g_w one float).
+nvfp4_status linear_impl(const void *X, int64_t M, int64_t K, int64_t ldx, const uint8_t *Wq,
+                         const uint8_t *Ws, const float *g_w, int64_t N, void *Y, int64_t ldy,
+                         const float *g_x, int mode, void *workspace, size_t workspace_bytes,
+                         void *stream, const WeightGroups &wg) {
     if (mode != NVFP4_LINEAR_UNFUSED && mode != NVFP4_LINEAR_FUSED) return NVFP4_ERR_INVALID_ARG;
     nvfp4_status s = check_bf16_matrix(X, M, K, ldx);
     if (s != NVFP4_OK) return s;
     s = check_gemm_b_and_y(Wq, Ws, g_w, M, N, K, Y, ldy);
     if (s != NVFP4_OK) return s;
     if (M == 0 || N == 0) return NVFP4_OK;
+    // per-group scales live in the CTA-pair kernel's extended epilogue
+    if (wg.count > 1 && M > kSkinnyMaxM && !gemm_use_pair()) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (g_x != nullptr && !aligned(g_x, 4)) return NVFP4_ERR_MISALIGNED;
     const size_t need = nvfp4_linear_workspace_bytes(M, N, K, mode);
     if (workspace_bytes < need) return NVFP4_ERR_WORKSPACE_TOO_SMALL;
@@ -280,7 +288,7 @@ nvfp4_status nvfp4_linear(const void *X, int64_t M, int64_t K, int64_t ldx, cons
         // one launch: the GEMM computes g_x (when not given) and quantizes X
         // tiles in shared memory; no codes in HBM
         SkinnyArgs sa{Wq, Ws, g_w, nullptr, nullptr, Xh, ldx, g_x, M, N, K,
-                      static_cast<uint16_t *>(Y), ldy, 1};
+                      static_cast<uint16_t *>(Y), ldy, 1, wg};
         return from_cuda(launch_gemm_skinny(sa, st));
     }
     // unfused (and fused beyond 4 rows or K = 6144, where every CTA
@@ -288,11 +296,44 @@ nvfp4_status nvfp4_linear(const void *X, int64_t M, int64_t K, int64_t ldx, cons
     if (quantize_activation(Xh, M, K, ldx, &g_x, ws, st) != cudaSuccess) return NVFP4_ERR_CUDA;
     if (M <= kSkinnyMaxM) {
         SkinnyArgs sa{Wq, Ws, g_w, xq, xs, nullptr, 0, g_x, M, N, K,
-                      static_cast<uint16_t *>(Y), ldy, 0};
+                      static_cast<uint16_t *>(Y), ldy, 0, wg};
         return from_cuda(launch_gemm_skinny(sa, st));
     }
     GemmArgs a{xq, xs, g_x, Wq, Ws, g_w, M, N, K, static_cast<uint16_t *>(Y), ldy};
+    a.groups = wg;
     return from_cuda(gemm_use_pair() ? launch_gemm_pair(a, st) : launch_gemm(a, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+nvfp4_status nvfp4_linear(const void *X, int64_t M, int64_t K, int64_t ldx, const uint8_t *Wq,
+                          const uint8_t *Ws, const float *g_w, int64_t N, void *Y, int64_t ldy,
+                          const float *g_x, int mode, void *workspace, size_t workspace_bytes,
+                          void *stream) {
+    return linear_impl(X, M, K, ldx, Wq, Ws, g_w, N, Y, ldy, g_x, mode, workspace,
+                       workspace_bytes, stream, WeightGroups{});
+}
+
+nvfp4_status nvfp4_linear_grouped(const void *X, int64_t M, int64_t K, int64_t ldx,
+                                  const uint8_t *Wq, const uint8_t *Ws, const float *g_w,
+                                  const int64_t *group_n, int groups, void *Y, int64_t ldy,
+                                  const float *g_x, int mode, void *workspace,
+                                  size_t workspace_bytes, void *stream) {
+    if (group_n == nullptr || groups < 1 || groups > kMaxGroups) return NVFP4_ERR_INVALID_ARG;
+    WeightGroups wg;
+    wg.count = groups;
+    int64_t N = 0;
+    for (int g = 0; g < groups; ++g) {
+        if (group_n[g] <= 0) return NVFP4_ERR_INVALID_ARG;
+        if (group_n[g] % 256 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        N += group_n[g];
+        if (N > kMaxDim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        wg.end[g] = static_cast<int>(N);
+    }
+    return linear_impl(X, M, K, ldx, Wq, Ws, g_w, N, Y, ldy, g_x, mode, workspace,
+                       workspace_bytes, stream, wg);
 }
 
 nvfp4_status nvfp4_linear_bias_requant(const void *X, int64_t M, int64_t K, int64_t ldx,

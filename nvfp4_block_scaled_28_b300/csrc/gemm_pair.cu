@@ -111,6 +111,7 @@ struct Params {
     const float *g_y;
     uint8_t *Yq;
     uint8_t *Ys;
+    WeightGroups groups;  // grouped projection: g_b holds one scale per group
     int inject;          // 1: the producers issue nothing (bounded-wait test)
     uint64_t timeout_ns;
     unsigned int *err;   // device error word
@@ -328,7 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // -------------------------------------------------------- epilogue
         const int quarter = warp & 3;
         const int half = (warp - kFirstEpiWarp) >> 2;  // which 128 columns
-        const float alpha = __fmul_rn(*p.g_a, *p.g_b);
+        const float g_a = *p.g_a;
+        const float alpha0 = __fmul_rn(g_a, *p.g_b);
         const uint32_t acc_empty0 = mapa_shared(smem_addr(&sh.acc_empty), 0);
         int it = 0;
         for (int t = 0; t < my_tiles; ++t, ++it) {
@@ -350,6 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row0 = mt * PM + static_cast<int>(rank) * BM + quarter * 32;
             const int row = row0 + lane;
             const int n0 = nt * BN + half * 128;
+            // grouped projection: the tile's weight group sets the scale
+            const float alpha =
+                kEpi ? __fmul_rn(g_a, p.g_b[weight_group_of(p.groups, n0)]) : alpha0;
             uint32_t packed[64];
             if (!kEpi || p.bias == nullptr) {
 #pragma unroll
@@ -565,6 +570,7 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     p.g_y = a.g_y;
     p.Yq = a.Yq;
     p.Ys = a.Ys;
+    p.groups = a.groups;
     p.inject = debug_state().inject;
     p.timeout_ns = debug_state().timeout_ns;
     p.err = device_error_word();
@@ -583,7 +589,7 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    const bool epi = !store_y || a.bias != nullptr || a.Yq != nullptr;
+    const bool epi = !store_y || a.bias != nullptr || a.Yq != nullptr || a.groups.count > 1;
     cudaError_t e = epi ? cudaLaunchKernelEx(&cfg, gemm_pair_kernel<true>, tmA, tmB, tmSA, tmSB,
                                              tmY, tmYq, p)
                         : cudaLaunchKernelEx(&cfg, gemm_pair_kernel<false>, tmA, tmB, tmSA, tmSB,

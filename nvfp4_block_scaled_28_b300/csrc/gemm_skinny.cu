@@ -104,7 +104,8 @@ struct SkParams {
     const uint16_t *X;   // bfloat16 activation (fused; read for amax when g_x is null)
     int64_t ldx;
     const float *g_x;    // fused: null = compute amax(|X|) / (6 * 448) in the kernel
-    const float *g_w;
+    const float *g_w;    // one per weight group
+    WeightGroups groups;
     uint16_t *Y;
     int64_t ldy;
     int M, N, K;
@@ -398,7 +399,7 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
             // fused: the quantizer warps published g_x in shared memory before
             // the MMAs this accumulator completion follows
             const float gx = FUSED ? sh.g_x : *p.g_x;
-            const float alpha = __fmul_rn(gx, *p.g_w);
+            const float alpha = __fmul_rn(gx, p.g_w[weight_group_of(p.groups, nt * SK_BM)]);
             const uint32_t t_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + C::ACC_COL;
             // D[n, m]: lane = weight row n, column = activation row m
             float acc[NX];
@@ -465,6 +466,7 @@ cudaError_t launch_sk(const SkinnyArgs &a, cudaStream_t st) {
     p.ldx = a.ldx;
     p.g_x = a.g_x;
     p.g_w = a.g_w;
+    p.groups = a.groups;
     p.Y = a.Y;
     p.ldy = a.ldy;
     p.M = static_cast<int>(a.M);

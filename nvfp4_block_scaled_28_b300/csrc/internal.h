@@ -66,6 +66,24 @@ cudaLaunchAttribute pdl_attribute();
 cudaError_t launch_sf_to_mma(const uint8_t *sf_rm, int64_t rows, int64_t K, uint8_t *sf_mma,
                              cudaStream_t st);
 
+// Weight groups of a grouped projection: the weight rows (output columns)
+// are `count` consecutive groups, group g ending at column end[g] (each a
+// multiple of 256) with its own global scale g_b[g]. count <= 1: one group.
+constexpr int kMaxGroups = 8;
+struct WeightGroups {
+    int count = 0;
+    int end[kMaxGroups] = {};
+};
+
+// Group of output column n (ends ascending; columns past the last end
+// belong to the last group).
+__host__ __device__ inline int weight_group_of(const WeightGroups &w, int n) {
+    int g = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxGroups - 1; ++i) g += (i < w.count - 1 && n >= w.end[i]) ? 1 : 0;
+    return g;
+}
+
 struct GemmArgs {
     const uint8_t *Aq, *As;
     const float *g_a;
@@ -82,6 +100,7 @@ struct GemmArgs {
     const float *g_y = nullptr;
     uint8_t *Yq = nullptr;
     uint8_t *Ys = nullptr;
+    WeightGroups groups;  // g_b then points at groups.count floats
 };
 
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st);
@@ -106,6 +125,7 @@ struct SkinnyArgs {
     uint16_t *Y;
     int64_t ldy;
     int fused;
+    WeightGroups groups = {};  // g_w then points at groups.count floats
 };
 cudaError_t launch_gemm_skinny(const SkinnyArgs &a, cudaStream_t st);
 

@@ -199,6 +199,60 @@ def nvfp4_linear(X: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, g_w: torch
     return Y
 
 
+def pack_weight_groups(weights):
+    """Stack quantized weights [(Wq, Ws, g_w), ...] (scales in the 128x4 tile
+    layout, rows a multiple of 256 each) into the operands of
+    nvfp4_linear_grouped: (Wq, Ws, g_w (G,), group_n). A one-time copy."""
+    _require(1 <= len(weights) <= 8, "1 to 8 weight groups")
+    K = weights[0][0].shape[1] * 2
+    for Wq, Ws, g in weights:
+        n = Wq.shape[0]
+        _require(n % 256 == 0, "each group's rows must be a multiple of 256, got %d" % n)
+        _check_codes(Wq, n, K, "Wq")
+        _check_scales(Ws, n, K, SF_MMA_128x4, "Ws")
+        _check_g(g, "g_w")
+    Wq = torch.cat([w[0] for w in weights], 0)
+    Ws = torch.cat([w[1].view(torch.uint8).reshape(w[0].shape[0], K // 16) for w in weights], 0)
+    g = torch.cat([w[2].reshape(-1)[:1] for w in weights], 0)
+    return Wq, Ws, g, [int(w[0].shape[0]) for w in weights]
+
+
+def nvfp4_linear_grouped(X: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor,
+                         g_w: torch.Tensor, group_n, g_x: torch.Tensor | None = None,
+                         mode: int = LINEAR_UNFUSED, Y: torch.Tensor | None = None,
+                         workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Several projections of the same X in one call (X quantized once, one
+    GEMM launch), group g with its own global scale g_w[g]; Y's columns are
+    the groups' outputs side by side (see pack_weight_groups)."""
+    import ctypes
+
+    _check_bf16_2d(X, "X")
+    M, K = X.shape
+    group_n = [int(n) for n in group_n]
+    Nn = sum(group_n)
+    _check_codes(Wq, Nn, K, "Wq")
+    _check_scales(Ws, Nn, K, SF_MMA_128x4, "Ws")
+    _require(g_w.dtype == torch.float32 and g_w.numel() == len(group_n) and g_w.is_contiguous(),
+             "g_w must be a contiguous float32 tensor with one scale per group")
+    if g_x is not None:
+        _check_g(g_x, "g_x")
+    _check_cuda(X, Wq, Ws, g_w, g_x, Y, workspace)
+    if Y is None:
+        Y = torch.empty((M, Nn), dtype=torch.bfloat16, device=X.device)
+    _check_bf16_2d(Y, "Y")
+    _require(tuple(Y.shape) == (M, Nn), "Y must have shape (%d, %d)" % (M, Nn))
+    need = linear_workspace_bytes(M, Nn, K, mode)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=X.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    ns = (ctypes.c_int64 * len(group_n))(*group_n)
+    N.check("nvfp4_linear_grouped", N.load().nvfp4_linear_grouped(
+        _ptr(X), M, K, X.stride(0), _ptr(Wq), _ptr(Ws), _ptr(g_w),
+        ctypes.cast(ns, ctypes.c_void_p), len(group_n), _ptr(Y), Y.stride(0), _ptr(g_x), mode,
+        _ptr(workspace), ws_bytes, _stream()))
+    return Y
+
+
 def nvfp4_linear_noalloc(X: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor,
                          g_w: torch.Tensor, g_x: torch.Tensor | None = None,
                          Y: torch.Tensor | None = None) -> torch.Tensor:

@@ -157,3 +157,26 @@ def test_linear_bias_requant_argument_checks(lib):
     assert call(wsb=16) == N.ERR_WORKSPACE_TOO_SMALL
     assert call(ws=A16 + 16) == N.ERR_MISALIGNED
     assert call(M=0) == N.OK and call(N=0, ldy=0) == N.OK  # empty: nothing launched
+
+
+def test_linear_grouped_argument_checks(lib):
+    import ctypes
+    f = lib.nvfp4_linear_grouped
+
+    def call(ns, groups=None, **kw):
+        arr = (ctypes.c_int64 * max(1, len(ns)))(*ns)
+        base = dict(X=A16, M=64, K=512, ldx=512, Wq=A16, Ws=A16, gw=A16,
+                    gn=ctypes.cast(arr, ctypes.c_void_p), G=len(ns) if groups is None else groups,
+                    Y=A16, ldy=sum(ns), gx=None, mode=0, ws=A16 * 16, wsb=1 << 30)
+        base.update(kw)
+        return f(*base.values(), None)
+
+    assert call([256, 256], gn=None) == N.ERR_INVALID_ARG
+    assert call([256], groups=0) == N.ERR_INVALID_ARG
+    assert call([256] * 9) == N.ERR_INVALID_ARG            # at most 8 groups
+    assert call([256, 0]) == N.ERR_INVALID_ARG
+    assert call([256, 128]) == N.ERR_UNSUPPORTED_SHAPE     # multiples of 256
+    assert call([256, 512], ldy=512) == N.ERR_INVALID_ARG  # ldy < sum
+    assert call([256, 512], mode=2) == N.ERR_INVALID_ARG
+    assert call([256, 512], wsb=16) == N.ERR_WORKSPACE_TOO_SMALL
+    assert call([256, 512], M=0) == N.OK
