@@ -18,6 +18,9 @@ from .oracle import (  # noqa: F401
     bf16_from_double,
     global_scale,
     quantize,
+    SCALE_ABSMAX,
+    SCALE_FOUR_OVER_SIX,
+    SCALE_MSE,
     dequantize,
     gemm,
     gemm_rows,

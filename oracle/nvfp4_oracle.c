@@ -18,6 +18,11 @@
  *    (out, in/2) as uint8 with two FP4 values per byte, scales (out, in/16) as
  *    float8_e4m3fn; activations are quantized dynamically in forward(), then
  *    a block-scaled FP4 x FP4 matmul writes bfloat16.
+ *  - The same section's table names two more block-scale rules: "MSE" tries
+ *    several scales and keeps the one with the smallest block reconstruction
+ *    error; "four-over-six" lets each block map its maximum to 4 or to 6,
+ *    whichever errs less (quantize_block_rule states the candidates and the
+ *    tie rule taken where the page gives none).
  *  - Where the pages are silent, the readings of this build are used (each is
  *    also listed in the design doc): a per-tensor FP32 global scale g in the decode
  *    direction (x_hat = e2m1 * e4m3 * g) with g = amax_tensor / (6 * 448);
@@ -175,9 +180,46 @@ float oracle_global_scale(const uint16_t *X, int64_t rows, int64_t cols, int64_t
 
 /* ------------------------------------------------------------ quantizer */
 
-/* Quantize one row segment of 16 values: writes 8 packed bytes and returns
- * the E4M3 scale byte. */
-static uint8_t quantize_block(const uint16_t *x, float g, uint8_t *packed)
+/* The E2M1 codes of the 16 values under block scale byte S: each |x| times
+ * r = 1 / (e4m3(S) * g) (fp32), rounded onto the grid; sign bit from x. */
+static void block_codes(const float *vals, float g, uint8_t S, int *codes)
+{
+    float s = (float)oracle_e4m3_value(S);        /* exact */
+    float denom = s * g;
+    float r = (denom > 0.0f) ? 1.0f / denom : 0.0f;
+    for (int i = 0; i < 16; ++i) {
+        float y = fabsf(vals[i]) * r;
+        int m = oracle_e2m1_rne_satfinite(y);
+        codes[i] = (signbit(vals[i]) ? 8 : 0) | m;
+    }
+}
+
+/* Block reconstruction error of the codes under S: the sum over the 16
+ * values, in element order, of (x - x_hat)^2 in FP64 (one rounding per
+ * subtraction, product and addition), x_hat = e2m1(code) * e4m3(S) * g
+ * (exact in FP64). */
+static double block_error(const float *vals, float g, uint8_t S, const int *codes)
+{
+    double err = 0.0;
+    for (int i = 0; i < 16; ++i) {
+        double xhat = oracle_e2m1_value(codes[i]) * oracle_e4m3_value(S) * (double)g;
+        double d = (double)vals[i] - xhat;
+        double sq = d * d;
+        err = err + sq;
+    }
+    return err;
+}
+
+/* Quantize one row segment of 16 values under a block-scale rule ("nvfp4-gemma4"
+ * page, section 2, the scale-selection table):
+ *   0 absmax: S6 = RNE_E4M3((amax / 6) / g), the block maximum maps to 6;
+ *   1 four-over-six: S6, or S4 = RNE_E4M3((amax / 4) / g) (the maximum maps to
+ *     4), whichever has the smaller block error; equal errors keep S6;
+ *   2 MSE: the smallest block error over S6, S4 and every E4M3 scale from
+ *     e4m3(S6) / 2 to 2 * e4m3(S6); equal errors keep S6, else the smallest
+ *     scale (the pages give no candidate grid: this window is the reading).
+ * Writes 8 packed bytes and returns the E4M3 scale byte. */
+static uint8_t quantize_block_rule(const uint16_t *x, float g, int rule, uint8_t *packed)
 {
     float vals[16];
     float amax = 0.0f;
@@ -189,14 +231,29 @@ static uint8_t quantize_block(const uint16_t *x, float g, uint8_t *packed)
     }
     float v = (amax / 6.0f) / g;                 /* two fp32 divisions */
     uint8_t S = oracle_e4m3_rne_satfinite(v);
-    float s = (float)oracle_e4m3_value(S);        /* exact */
-    float denom = s * g;
-    float r = (denom > 0.0f) ? 1.0f / denom : 0.0f;
     int codes[16];
-    for (int i = 0; i < 16; ++i) {
-        float y = fabsf(vals[i]) * r;
-        int m = oracle_e2m1_rne_satfinite(y);
-        codes[i] = (signbit(vals[i]) ? 8 : 0) | m;
+    block_codes(vals, g, S, codes);
+    if (rule != 0) {
+        double best = block_error(vals, g, S, codes);
+        uint8_t S6 = S;
+        uint8_t S4 = oracle_e4m3_rne_satfinite((amax / 4.0f) / g);
+        double lo = oracle_e4m3_value(S6) / 2.0, hi = oracle_e4m3_value(S6) * 2.0;
+        for (int b = 1; b <= 0x7E; ++b) {
+            if (b == S6)
+                continue;
+            int in = (b == S4) || (rule == 2 && oracle_e4m3_value(b) >= lo &&
+                                   oracle_e4m3_value(b) <= hi);
+            if (!in)
+                continue;
+            int c[16];
+            block_codes(vals, g, (uint8_t)b, c);
+            double e = block_error(vals, g, (uint8_t)b, c);
+            if (e < best) {
+                best = e;
+                S = (uint8_t)b;
+                memcpy(codes, c, sizeof c);
+            }
+        }
     }
     for (int j = 0; j < 8; ++j)
         packed[j] = (uint8_t)(codes[2 * j] | (codes[2 * j + 1] << 4));
@@ -205,16 +262,24 @@ static uint8_t quantize_block(const uint16_t *x, float g, uint8_t *packed)
 
 /* X: bf16 bits, rows x cols (cols % 16 == 0), row stride ld elements.
  * q: rows x cols/2 bytes (row-major, contiguous).
- * sf: rows x cols/16 E4M3 bytes (row-major, contiguous). */
-void oracle_quantize(const uint16_t *X, int64_t rows, int64_t cols, int64_t ld,
-                     float g, uint8_t *q, uint8_t *sf)
+ * sf: rows x cols/16 E4M3 bytes (row-major, contiguous).
+ * rule: 0 absmax, 1 four-over-six, 2 MSE (quantize_block_rule). */
+void oracle_quantize_rule(const uint16_t *X, int64_t rows, int64_t cols, int64_t ld,
+                          float g, int rule, uint8_t *q, uint8_t *sf)
 {
     int64_t nb = cols / 16;
 #pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t b = 0; b < nb; ++b)
-            sf[r * nb + b] = quantize_block(X + r * ld + b * 16, g,
-                                            q + r * (cols / 2) + b * 8);
+            sf[r * nb + b] = quantize_block_rule(X + r * ld + b * 16, g, rule,
+                                                 q + r * (cols / 2) + b * 8);
+}
+
+/* The absmax rule (the one the activations use). */
+void oracle_quantize(const uint16_t *X, int64_t rows, int64_t cols, int64_t ld,
+                     float g, uint8_t *q, uint8_t *sf)
+{
+    oracle_quantize_rule(X, rows, cols, ld, g, 0, q, sf);
 }
 
 /* x_hat = e2m1(code) * e4m3(S) * g, in FP64; out is rows x cols. */

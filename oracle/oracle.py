@@ -68,6 +68,9 @@ def _load():
         lib.oracle_quantize.restype = None
         lib.oracle_quantize.argtypes = [_u16p, _i64, _i64, _i64, ctypes.c_float,
                                         _u8p, _u8p]
+        lib.oracle_quantize_rule.restype = None
+        lib.oracle_quantize_rule.argtypes = [_u16p, _i64, _i64, _i64, ctypes.c_float,
+                                             ctypes.c_int, _u8p, _u8p]
         lib.oracle_dequantize.restype = None
         lib.oracle_dequantize.argtypes = [_u8p, _u8p, ctypes.c_float, _i64, _i64,
                                           _f64p]
@@ -124,18 +127,28 @@ def global_scale(x_bits: np.ndarray) -> float:
     return float(_load().oracle_global_scale(_ptr(x, _u16p), rows, cols, cols))
 
 
-def quantize(x_bits: np.ndarray, g: float):
+SCALE_ABSMAX, SCALE_FOUR_OVER_SIX, SCALE_MSE = 0, 1, 2
+
+
+def quantize(x_bits: np.ndarray, g: float, rule: int = SCALE_ABSMAX):
     """Quantize a 2-D bfloat16 tensor (uint16 bits, cols % 16 == 0) with the
-    decode-direction global scale ``g``. Returns (codes uint8 rows x cols/2,
-    scales uint8 rows x cols/16), both row-major."""
+    decode-direction global scale ``g`` and a block-scale rule (absmax,
+    four-over-six or MSE; "nvfp4-gemma4" page, section 2). Returns (codes
+    uint8 rows x cols/2, scales uint8 rows x cols/16), both row-major."""
     x = _c(x_bits, np.uint16)
     rows, cols = x.shape
     if cols % 16:
         raise ValueError("cols must be a multiple of 16")
+    if rule not in (SCALE_ABSMAX, SCALE_FOUR_OVER_SIX, SCALE_MSE):
+        raise ValueError("unknown scale rule %r" % rule)
     q = np.empty((rows, cols // 2), np.uint8)
     s = np.empty((rows, cols // 16), np.uint8)
-    _load().oracle_quantize(_ptr(x, _u16p), rows, cols, cols, float(g),
-                            _ptr(q, _u8p), _ptr(s, _u8p))
+    if rule == SCALE_ABSMAX:
+        _load().oracle_quantize(_ptr(x, _u16p), rows, cols, cols, float(g),
+                                _ptr(q, _u8p), _ptr(s, _u8p))
+    else:
+        _load().oracle_quantize_rule(_ptr(x, _u16p), rows, cols, cols, float(g), int(rule),
+                                     _ptr(q, _u8p), _ptr(s, _u8p))
     return q, s
 
 

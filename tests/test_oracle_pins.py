@@ -457,3 +457,107 @@ def test_symmetric_int8_worked_example(oracle_mod):
     assert q2[:4].tolist() == o["q_first4"]
     assert np.allclose(xh2[:4], o["x_hat_first4"], atol=5e-4)
     assert abs(np.max(np.abs(np.array(o["w"][:4]) - xh2[:4])) - o["max_abs_err_first4"]) < 2e-3
+
+
+# ------------------------------------------- scale-selection rules (four-over-six, MSE)
+
+def _block_errors(oracle_mod, bits, g, q, sf):
+    """Per-block sum of squared reconstruction errors, through the oracle's
+    plain dequantizer (a path independent of the selection code)."""
+    x = bits_to_f32(bits).astype(np.float64)
+    xh = oracle_mod.dequantize(q, sf, g)
+    d = (x - xh) ** 2
+    return d.reshape(d.shape[0], -1, 16).sum(axis=2)
+
+
+def test_four_over_six_worked_example(oracle_mod):
+    """16 values of 4.0, g = 1. absmax: (4/6)/1 = 0.667 rounds to the E4M3
+    value 0.6875 (byte 0x33: exponent field 6, mantissa 3); 4/0.6875 = 5.82
+    rounds to the E2M1 value 6 (code 7), so x_hat = 4.125 and the block error
+    is 16 * 0.125^2 = 0.25. With the maximum mapped to 4 the scale is 1.0
+    (byte 0x38) and every value is exactly code 6 (value 4): error 0, so
+    four-over-six and MSE take it."""
+    bits = bf16_bits(np.full((1, 16), 4.0, np.float32))
+    q0, s0 = oracle_mod.quantize(bits, 1.0, oracle_mod.SCALE_ABSMAX)
+    assert s0[0, 0] == 0x33 and np.all(q0 == 0x77)
+    assert _block_errors(oracle_mod, bits, 1.0, q0, s0)[0, 0] == 0.25
+    for rule in (oracle_mod.SCALE_FOUR_OVER_SIX, oracle_mod.SCALE_MSE):
+        q, s = oracle_mod.quantize(bits, 1.0, rule)
+        assert s[0, 0] == 0x38 and np.all(q == 0x66)
+        assert _block_errors(oracle_mod, bits, 1.0, q, s)[0, 0] == 0.0
+
+
+def test_rules_keep_an_exact_absmax_scale(oracle_mod):
+    """A block already on the grid at the absmax scale (error 0) keeps it
+    under every rule: equal errors keep the absmax scale."""
+    vals = np.array([6, 4, 3, 2, 1.5, 1, .5, 0, -6, -4, -3, -2, -1.5, -1, -.5, 6],
+                    np.float32) * 0.25
+    bits = bf16_bits(vals.reshape(1, 16))
+    ref = oracle_mod.quantize(bits, 1.0, oracle_mod.SCALE_ABSMAX)
+    assert _block_errors(oracle_mod, bits, 1.0, *ref)[0, 0] == 0.0
+    for rule in (oracle_mod.SCALE_FOUR_OVER_SIX, oracle_mod.SCALE_MSE):
+        q, s = oracle_mod.quantize(bits, 1.0, rule)
+        assert np.array_equal(s, ref[1]) and np.array_equal(q, ref[0])
+
+
+def test_rule_errors_are_ordered(oracle_mod):
+    """Per block: error(MSE) <= error(four-over-six) <= error(absmax), since
+    each rule's candidates contain the previous rule's choice; both
+    selections strictly help on Gaussian blocks overall."""
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((64, 256)).astype(np.float32)
+    x[:, rng.choice(256, 2, replace=False)] *= 30
+    bits = bf16_bits(x)
+    g = oracle_mod.global_scale(bits)
+    e = [_block_errors(oracle_mod, bits, g, *oracle_mod.quantize(bits, g, r))
+         for r in (oracle_mod.SCALE_ABSMAX, oracle_mod.SCALE_FOUR_OVER_SIX, oracle_mod.SCALE_MSE)]
+    tol = 1e-12 * e[0]
+    assert np.all(e[1] <= e[0] + tol) and np.all(e[2] <= e[1] + tol)
+    assert e[1].sum() < 0.97 * e[0].sum() and e[2].sum() < e[1].sum()
+
+
+def test_selection_is_exhaustive_by_brute_force(oracle_mod):
+    """Brute force over every candidate scale, written with the pinned
+    primitives (E4M3 / E2M1 decode and rounding) in plain Python: the oracle's
+    choice has the smallest error, with the stated tie rule."""
+    rng = np.random.default_rng(43)
+    x = rng.standard_normal((24, 16)).astype(np.float32) * rng.uniform(0.1, 10, (24, 1))
+    x[::5, 3] *= 25
+    x = x.astype(np.float32)
+    bits = bf16_bits(x)
+    xs = bits_to_f32(bits)
+    g = float(np.float32(oracle_mod.global_scale(bits)))
+    e4 = [oracle_mod.e4m3_value(b) for b in range(0x7F)]
+
+    def codes_and_error(row, S):
+        s = np.float32(e4[S])
+        denom = np.float32(s * np.float32(g))
+        r = np.float32(1.0) / denom if denom > 0 else np.float32(0.0)
+        err, codes = 0.0, []
+        for v in row:
+            m = oracle_mod.e2m1_rne_satfinite(float(np.float32(abs(v)) * r))
+            c = (8 if math.copysign(1.0, float(v)) < 0 else 0) | m
+            codes.append(c)
+            d = float(v) - oracle_mod.e2m1_value(c) * e4[S] * g
+            err = err + d * d
+        return codes, err
+
+    for rule in (oracle_mod.SCALE_FOUR_OVER_SIX, oracle_mod.SCALE_MSE):
+        q, sf = oracle_mod.quantize(bits, g, rule)
+        for i, row in enumerate(xs):
+            amax = np.float32(np.max(np.abs(row)))
+            S6 = oracle_mod.e4m3_rne_satfinite(float(np.float32(np.float32(amax / np.float32(6)) / np.float32(g))))
+            S4 = oracle_mod.e4m3_rne_satfinite(float(np.float32(np.float32(amax / np.float32(4)) / np.float32(g))))
+            cands = {S6, S4}
+            if rule == oracle_mod.SCALE_MSE:
+                cands |= {b for b in range(1, 0x7F) if e4[S6] / 2 <= e4[b] <= 2 * e4[S6]}
+            errs = {b: codes_and_error(row, b)[1] for b in cands}
+            best = min(errs.values())
+            if errs[S6] == best:
+                want = S6
+            else:
+                want = min(b for b, e in errs.items() if e == best)
+            assert sf[i, 0] == want, (rule, i, sf[i, 0], want)
+            codes = codes_and_error(row, want)[0]
+            packed = [codes[2 * j] | (codes[2 * j + 1] << 4) for j in range(8)]
+            assert list(q[i]) == packed
