@@ -397,6 +397,16 @@ def extra_rows(torch, nv, D, workloads, peaks):
                                    "frac_of_hbm": nbytes / ms / 1e6 / hbm}
     ms = time_region(torch, lambda i: _ok(D.global_scale(X, g), "amax"), 20)
     out["global_scale_16384x16384"] = {"ms": ms, "GB/s": sq.M[0] * sq.K * 2 / ms / 1e6}
+    # F2: offline weight quantization of the 5120 x 5120 prefill weight under
+    # each block-scale rule (global scale included)
+    pf = workloads.WORKLOADS["prefill"]
+    Wp = workloads.make_w(pf.N[0], pf.K, workloads.w_seed(pf), device="cuda")
+    for rule, name in ((0, "absmax"), (1, "four_over_six"), (2, "mse")):
+        nv.nvfp4_quantize_weight(Wp, nv.SF_MMA_128x4, rule=rule)
+        ms = time_region(torch, lambda i: nv.nvfp4_quantize_weight(Wp, nv.SF_MMA_128x4,
+                                                                   rule=rule), 5)
+        out["weight_quantize_5120x5120_%s" % name] = {"ms": ms}
+    del Wp
     # a4: square GEMM 16384^3
     W = workloads.make_w(sq.N[0], sq.K, workloads.w_seed(sq), device="cuda")
     Wq, Ws, gw = nv.nvfp4_quantize_weight(W, nv.SF_MMA_128x4)

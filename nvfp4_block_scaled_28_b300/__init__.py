@@ -11,6 +11,9 @@ from .ops import (  # noqa: F401
     SF_MMA_128x4,
     LINEAR_UNFUSED,
     LINEAR_FUSED,
+    SCALE_ABSMAX,
+    SCALE_FOUR_OVER_SIX,
+    SCALE_MSE,
     NVFP4Error,
     sf_bytes,
     sf_shape,

@@ -28,6 +28,10 @@ SF_MMA_128x4 = 1
 # nvfp4_linear_mode
 LINEAR_UNFUSED = 0
 LINEAR_FUSED = 1
+# nvfp4_scale_rule
+SCALE_ABSMAX = 0
+SCALE_FOUR_OVER_SIX = 1
+SCALE_MSE = 2
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -41,6 +45,7 @@ SIGNATURES = {
     "nvfp4_sf_bytes": (_SZ, [_I64, _I64, _INT]),
     "nvfp4_global_scale": (_INT, [_P, _I64, _I64, _I64, _P, _P]),
     "nvfp4_quantize": (_INT, [_P, _I64, _I64, _I64, _P, _P, _P, _INT, _P]),
+    "nvfp4_quantize_select": (_INT, [_P, _I64, _I64, _I64, _P, _INT, _P, _P, _INT, _P]),
     "nvfp4_quantize_weight": (_INT, [_P, _I64, _I64, _I64, _P, _P, _P, _INT, _P]),
     "nvfp4_sf_to_mma_layout": (_INT, [_P, _I64, _I64, _P, _P]),
     "nvfp4_gemm": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P]),

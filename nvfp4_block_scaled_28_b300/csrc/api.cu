@@ -161,6 +161,20 @@ nvfp4_status nvfp4_quantize(const void *X, int64_t rows, int64_t cols, int64_t l
                                      sf_layout, static_cast<cudaStream_t>(stream)));
 }
 
+nvfp4_status nvfp4_quantize_select(const void *X, int64_t rows, int64_t cols, int64_t ldx,
+                                   const float *g, int rule, uint8_t *q, uint8_t *sf,
+                                   int sf_layout, void *stream) {
+    if (rule != NVFP4_SCALE_ABSMAX && rule != NVFP4_SCALE_FOUR_OVER_SIX && rule != NVFP4_SCALE_MSE)
+        return NVFP4_ERR_INVALID_ARG;
+    nvfp4_status s = check_quantize(X, rows, cols, ldx, g, q, sf, sf_layout);
+    if (s != NVFP4_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint16_t *Xh = static_cast<const uint16_t *>(X);
+    if (rule == NVFP4_SCALE_ABSMAX)
+        return from_cuda(launch_quantize(Xh, rows, cols, ldx, g, q, sf, sf_layout, st));
+    return from_cuda(launch_quantize_select(Xh, rows, cols, ldx, g, rule, q, sf, sf_layout, st));
+}
+
 nvfp4_status nvfp4_quantize_weight(const void *W, int64_t N, int64_t K, int64_t ldw, uint8_t *Wq,
                                    uint8_t *Ws, float *g_w, int sf_layout, void *stream) {
     nvfp4_status s = check_quantize(W, N, K, ldw, g_w, Wq, Ws, sf_layout);

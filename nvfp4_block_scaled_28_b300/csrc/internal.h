@@ -84,6 +84,12 @@ __host__ __device__ inline int weight_group_of(const WeightGroups &w, int n) {
     return g;
 }
 
+// Quantization under the four-over-six or MSE block-scale rule
+// (nvfp4_scale_rule), one thread per 16-element block.
+cudaError_t launch_quantize_select(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
+                                   const float *g, int rule, uint8_t *q, uint8_t *sf, int layout,
+                                   cudaStream_t st);
+
 struct GemmArgs {
     const uint8_t *Aq, *As;
     const float *g_a;

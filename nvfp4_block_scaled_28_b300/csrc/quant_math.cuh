@@ -19,6 +19,13 @@
 
 namespace nvfp4 {
 
+// Byte offset of scale (row, kb) in the 128x4 tensor-core tile layout.
+__device__ __forceinline__ uint64_t sf_mma_offset(uint32_t row, uint32_t kb, uint32_t kb4) {
+    const uint32_t R = row >> 7, r = row & 127u;
+    return ((static_cast<uint64_t>(R) * kb4 + (kb >> 2)) << 9) + ((r & 31u) << 4) +
+           ((r >> 5) << 2) + (kb & 3u);
+}
+
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     uint4 v;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -23,12 +23,6 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// Byte offset of scale (row, kb) in the 128x4 tensor-core tile layout.
-__device__ __forceinline__ uint64_t sf_mma_offset(uint32_t row, uint32_t kb, uint32_t kb4) {
-    const uint32_t R = row >> 7, r = row & 127u;
-    return ((static_cast<uint64_t>(R) * kb4 + (kb >> 2)) << 9) + ((r & 31u) << 4) +
-           ((r >> 5) << 2) + (kb & 3u);
-}
 
 // One warp-uniform round of U blocks per lane: blocks i = base + lane +
 // u * stride (stride a multiple of 32, base of the warp's lane 0). All loads

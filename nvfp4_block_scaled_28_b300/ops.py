@@ -20,6 +20,9 @@ SF_ROW_MAJOR = N.SF_ROW_MAJOR
 SF_MMA_128x4 = N.SF_MMA_128x4
 LINEAR_UNFUSED = N.LINEAR_UNFUSED
 LINEAR_FUSED = N.LINEAR_FUSED
+SCALE_ABSMAX = N.SCALE_ABSMAX
+SCALE_FOUR_OVER_SIX = N.SCALE_FOUR_OVER_SIX
+SCALE_MSE = N.SCALE_MSE
 NVFP4Error = N.NVFP4Error
 
 
@@ -93,9 +96,11 @@ def nvfp4_global_scale(X: torch.Tensor, g: torch.Tensor | None = None) -> torch.
 
 
 def nvfp4_quantize(X: torch.Tensor, g: torch.Tensor, sf_layout: int = SF_ROW_MAJOR,
-                   q: torch.Tensor | None = None, sf: torch.Tensor | None = None):
+                   q: torch.Tensor | None = None, sf: torch.Tensor | None = None,
+                   rule: int = SCALE_ABSMAX):
     """Quantize bfloat16 X (rows, K) to packed E2M1 codes (rows, K/2) uint8
-    and E4M3 block scales (uint8 bytes) in ``sf_layout``."""
+    and E4M3 block scales (uint8 bytes) in ``sf_layout``; ``rule`` picks the
+    block scale (absmax, four-over-six or MSE)."""
     _check_bf16_2d(X, "X")
     _check_g(g, "g")
     _check_cuda(X, g)
@@ -107,17 +112,27 @@ def nvfp4_quantize(X: torch.Tensor, g: torch.Tensor, sf_layout: int = SF_ROW_MAJ
         sf = torch.empty(sf_shape(rows, K, sf_layout), dtype=torch.uint8, device=X.device)
     _check_codes(q, rows, K, "q")
     _check_scales(sf, rows, K, sf_layout, "sf")
-    N.check("nvfp4_quantize", N.load().nvfp4_quantize(
-        _ptr(X), rows, K, X.stride(0), _ptr(g), _ptr(q), _ptr(sf), sf_layout, _stream()))
+    if rule == SCALE_ABSMAX:
+        N.check("nvfp4_quantize", N.load().nvfp4_quantize(
+            _ptr(X), rows, K, X.stride(0), _ptr(g), _ptr(q), _ptr(sf), sf_layout, _stream()))
+    else:
+        N.check("nvfp4_quantize_select", N.load().nvfp4_quantize_select(
+            _ptr(X), rows, K, X.stride(0), _ptr(g), rule, _ptr(q), _ptr(sf), sf_layout,
+            _stream()))
     return q, sf
 
 
-def nvfp4_quantize_weight(W: torch.Tensor, sf_layout: int = SF_MMA_128x4):
+def nvfp4_quantize_weight(W: torch.Tensor, sf_layout: int = SF_MMA_128x4,
+                          rule: int = SCALE_ABSMAX):
     """Offline weight quantization: returns (Wq (N, K/2) uint8, Ws scales,
-    g_w 1-element float32)."""
+    g_w 1-element float32); ``rule`` picks the block scale."""
     _check_bf16_2d(W, "W")
     _check_cuda(W)
     rows, K = W.shape
+    if rule != SCALE_ABSMAX:
+        g = nvfp4_global_scale(W)
+        Wq, Ws = nvfp4_quantize(W, g, sf_layout, rule=rule)
+        return Wq, Ws, g
     Wq = torch.empty((rows, K // 2), dtype=torch.uint8, device=W.device)
     Ws = torch.empty(sf_shape(rows, K, sf_layout), dtype=torch.uint8, device=W.device)
     g = torch.empty(1, dtype=torch.float32, device=W.device)

@@ -180,3 +180,13 @@ def test_linear_grouped_argument_checks(lib):
     assert call([256, 512], mode=2) == N.ERR_INVALID_ARG
     assert call([256, 512], wsb=16) == N.ERR_WORKSPACE_TOO_SMALL
     assert call([256, 512], M=0) == N.OK
+
+
+def test_quantize_select_argument_checks(lib):
+    f = lib.nvfp4_quantize_select
+    assert f(A16, 4, 64, 64, A16, 3, A16, A16, 0, None) == N.ERR_INVALID_ARG   # no such rule
+    assert f(A16, 4, 64, 64, A16, -1, A16, A16, 0, None) == N.ERR_INVALID_ARG
+    assert f(A16, 4, 40, 40, A16, 2, A16, A16, 0, None) == N.ERR_UNSUPPORTED_SHAPE  # K % 16
+    assert f(ODD, 4, 64, 64, A16, 1, A16, A16, 0, None) == N.ERR_MISALIGNED
+    assert f(A16, 4, 64, 64, None, 1, A16, A16, 0, None) == N.ERR_INVALID_ARG   # no g
+    assert f(A16, 0, 64, 64, A16, 2, A16, A16, 0, None) == N.OK                 # empty
