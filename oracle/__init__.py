@@ -24,5 +24,8 @@ from .oracle import (  # noqa: F401
     dequantize,
     gemm,
     gemm_rows,
+    lora_rows,
+    round_bf16,
+    linear_lora_rows,
     symmetric_quantize,
 )

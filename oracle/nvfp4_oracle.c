@@ -356,6 +356,49 @@ void oracle_gemm_rows(const uint8_t *Xq, const uint8_t *Xs, float g_x,
     }
 }
 
+/* Low-rank (LoRA) correction kept beside the NVFP4 weight ("nvfp4-difusion"
+ * page, section 3: a LoRA cannot be merged into NVFP4 codes, so its product
+ * is computed at run time next to the quantized matmul):
+ *   out[i, n] = scale * sum_j ( sum_k X[m,k] * A[j,k] ) * B[n,j],  m = row i
+ * in FP64 on the unquantized bfloat16 activation, sums in increasing k and j.
+ * X: bfloat16 bits M x K (row stride ldx); A: bfloat16 r x K (the down
+ * projection); B: bfloat16 N x r (the up projection); out: n_rows x N.
+ * Rows as oracle_gemm_rows. */
+void oracle_lora_rows(const uint16_t *X, int64_t ldx, int64_t K, const uint16_t *A, int64_t r,
+                      const uint16_t *B, int64_t N, double scale, const int64_t *row_ids,
+                      int64_t n_rows, double *out)
+{
+#pragma omp parallel
+    {
+        double *l = (double *)malloc(sizeof(double) * (size_t)(r > 0 ? r : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < n_rows; ++i) {
+            int64_t m = row_ids ? row_ids[i] : i;
+            for (int64_t j = 0; j < r; ++j) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k)
+                    acc += (double)bf16_to_float(X[m * ldx + k]) *
+                           (double)bf16_to_float(A[j * K + k]);
+                l[j] = acc;
+            }
+            for (int64_t n = 0; n < N; ++n) {
+                double acc = 0.0;
+                for (int64_t j = 0; j < r; ++j)
+                    acc += l[j] * (double)bf16_to_float(B[n * r + j]);
+                out[i * N + n] = scale * acc;
+            }
+        }
+        free(l);
+    }
+}
+
+/* Round FP64 values once to bfloat16 (n values). */
+void oracle_round_bf16(const double *y, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_bf16_from_double(y[i]);
+}
+
 void oracle_gemm(const uint8_t *Xq, const uint8_t *Xs, float g_x,
                  const uint8_t *Wq, const uint8_t *Ws, float g_w,
                  int64_t M, int64_t N, int64_t K, uint16_t *Y, double *Yd)

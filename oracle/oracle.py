@@ -78,6 +78,11 @@ def _load():
         lib.oracle_gemm_rows.argtypes = [_u8p, _u8p, ctypes.c_float, _u8p, _u8p,
                                          ctypes.c_float, _i64, _i64, _i64,
                                          _i64p, _i64, _u16p, _u16p, _f64p]
+        lib.oracle_lora_rows.restype = None
+        lib.oracle_lora_rows.argtypes = [_u16p, _i64, _i64, _u16p, _i64, _u16p, _i64,
+                                         ctypes.c_double, _i64p, _i64, _f64p]
+        lib.oracle_round_bf16.restype = None
+        lib.oracle_round_bf16.argtypes = [_f64p, _i64, _u16p]
         lib.oracle_symmetric_quantize.restype = ctypes.c_double
         lib.oracle_symmetric_quantize.argtypes = [_f64p, _i64, ctypes.c_int,
                                                   _i32p, _f64p]
@@ -196,6 +201,40 @@ def gemm_rows(xq, xs, g_x, wq, ws, g_w, rows=None, want_fp64=False, bias=None):
 
 def gemm(xq, xs, g_x, wq, ws, g_w, want_fp64=False, bias=None):
     return gemm_rows(xq, xs, g_x, wq, ws, g_w, None, want_fp64, bias)
+
+
+def lora_rows(x_bits, a_bits, b_bits, scale, rows=None):
+    """FP64 low-rank correction scale * (X @ A^T) @ B^T on the bfloat16
+    activation (uint16 bits M x K), A r x K, B N x r, for the listed rows."""
+    x = _c(x_bits, np.uint16)
+    a = _c(a_bits, np.uint16)
+    b = _c(b_bits, np.uint16)
+    M, K = x.shape
+    r = a.shape[0]
+    N = b.shape[0]
+    assert a.shape == (r, K) and b.shape == (N, r)
+    ids = None if rows is None else _c(rows, np.int64)
+    n_rows = M if ids is None else ids.shape[0]
+    out = np.empty((n_rows, N), np.float64)
+    _load().oracle_lora_rows(_ptr(x, _u16p), K, K, _ptr(a, _u16p), r, _ptr(b, _u16p), N,
+                             float(scale), None if ids is None else _ptr(ids, _i64p), n_rows,
+                             _ptr(out, _f64p))
+    return out
+
+
+def round_bf16(y: np.ndarray) -> np.ndarray:
+    """Round FP64 values once to bfloat16 bits."""
+    yy = _c(y, np.float64)
+    out = np.empty(yy.shape, np.uint16)
+    _load().oracle_round_bf16(_ptr(yy, _f64p), yy.size, _ptr(out, _u16p))
+    return out
+
+
+def linear_lora_rows(xq, xs, g_x, wq, ws, g_w, x_bits, a_bits, b_bits, scale, rows=None):
+    """Reference NVFP4 linear with a LoRA correction: bf16( (Xhat @ What^T)
+    * g_x * g_w + scale * (X @ A^T) @ B^T ), both terms in FP64, one rounding."""
+    _, yd = gemm_rows(xq, xs, g_x, wq, ws, g_w, rows, want_fp64=True)
+    return round_bf16(yd + lora_rows(x_bits, a_bits, b_bits, scale, rows))
 
 
 def symmetric_quantize(x, bits: int):

@@ -561,3 +561,59 @@ def test_selection_is_exhaustive_by_brute_force(oracle_mod):
             codes = codes_and_error(row, want)[0]
             packed = [codes[2 * j] | (codes[2 * j + 1] << 4) for j in range(8)]
             assert list(q[i]) == packed
+
+
+# ------------------------------------------------- LoRA correction (run-time low rank)
+
+def test_lora_matches_numpy_float64(oracle_mod):
+    """The low-rank term against numpy's float64 matmuls (library pin)."""
+    rng = np.random.default_rng(51)
+    M, K, r, N = 9, 96, 16, 40
+    x = bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    a = bf16_bits((rng.standard_normal((r, K)) * 0.1).astype(np.float32))
+    b = bf16_bits((rng.standard_normal((N, r)) * 0.1).astype(np.float32))
+    want = 0.75 * (bits_to_f32(x).astype(np.float64) @ bits_to_f32(a).astype(np.float64).T) \
+        @ bits_to_f32(b).astype(np.float64).T
+    got = oracle_mod.lora_rows(x, a, b, 0.75)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+    rows = np.array([7, 0, 3])
+    assert np.array_equal(oracle_mod.lora_rows(x, a, b, 0.75, rows), got[rows])
+
+
+def test_lora_selection_closed_form(oracle_mod):
+    """A selects input column k_j for rank j and B maps rank j to output
+    n = j: the term is exactly scale * X[m, k_j] in column j, 0 elsewhere."""
+    rng = np.random.default_rng(53)
+    M, K, r, N = 5, 64, 4, 8
+    x = bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    ks = [3, 17, 40, 63]
+    a = np.zeros((r, K), np.float32)
+    a[np.arange(r), ks] = 1.0
+    b = np.zeros((N, r), np.float32)
+    b[np.arange(r), np.arange(r)] = 1.0
+    got = oracle_mod.lora_rows(x, bf16_bits(a), bf16_bits(b), 2.0)
+    want = np.zeros((M, N))
+    want[:, :r] = 2.0 * bits_to_f32(x)[:, ks]
+    assert np.array_equal(got, want)
+
+
+def test_linear_lora_reduces_to_the_linear(oracle_mod):
+    """scale = 0 gives the plain NVFP4 linear; the combined rounding is the
+    single bfloat16 rounding of the FP64 sum."""
+    rng = np.random.default_rng(57)
+    M, K, N, r = 6, 64, 24, 16
+    xb = bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    wb = bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    ab = bf16_bits((rng.standard_normal((r, K)) * 0.1).astype(np.float32))
+    bb = bf16_bits((rng.standard_normal((N, r)) * 0.1).astype(np.float32))
+    gx, gw = oracle_mod.global_scale(xb), oracle_mod.global_scale(wb)
+    xq, xs = oracle_mod.quantize(xb, gx)
+    wq, ws = oracle_mod.quantize(wb, gw)
+    plain = oracle_mod.gemm(xq, xs, gx, wq, ws, gw)
+    assert np.array_equal(oracle_mod.linear_lora_rows(xq, xs, gx, wq, ws, gw, xb, ab, bb, 0.0),
+                          plain)
+    _, yd = oracle_mod.gemm(xq, xs, gx, wq, ws, gw, want_fp64=True)
+    total = yd + oracle_mod.lora_rows(xb, ab, bb, 1.5)
+    got = oracle_mod.linear_lora_rows(xq, xs, gx, wq, ws, gw, xb, ab, bb, 1.5)
+    want = np.array([[oracle_mod.bf16_from_double(v) for v in row] for row in total])
+    assert np.array_equal(got, want)
