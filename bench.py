@@ -200,6 +200,13 @@ class Direct:
             group_n_arr, groups, Y.data_ptr(), Y.stride(0), None, mode, ws.data_ptr(),
             ws.numel(), self.stream)
 
+    def linear_lora(self, X, Wq, Ws, gw, la, lb, r, scale, Y, ws):
+        M, K = X.shape
+        return self.lib.nvfp4_linear_lora(
+            X.data_ptr(), M, K, X.stride(0), Wq.data_ptr(), Ws.data_ptr(), gw.data_ptr(),
+            Wq.shape[0], la.data_ptr(), lb.data_ptr(), r, scale, Y.data_ptr(), Y.stride(0), None,
+            ws.data_ptr(), ws.numel(), self.stream)
+
     def linear_bias_requant(self, X, Wq, Ws, gw, bias, Y, gy, Yq, Ys, ws):
         M, K = X.shape
         n = Wq.shape[0]
@@ -209,6 +216,10 @@ class Direct:
             n if Y is None else Y.stride(0), None if gy is None else gy.data_ptr(),
             None if Yq is None else Yq.data_ptr(), None if Ys is None else Ys.data_ptr(), None,
             ws.data_ptr(), ws.numel(), self.stream)
+
+
+def lib_lora_ws(nv, M, N, K, r):
+    return nv.load_library().nvfp4_linear_lora_workspace_bytes(M, N, K, r)
 
 
 def _ok(status, what):
@@ -491,7 +502,15 @@ def extra_rows(torch, nv, D, workloads, peaks):
         "TFLOP/s_fused": fl / ms_epi / 1e9,
         "TFLOP/s_fused_no_bf16_y": fl / ms_q / 1e9,
     }
-    del Xp, Wq, Ws, Y, Yq, Ys, ws
+    # F3: the same layer with a rank-32 LoRA correction (down projection in
+    # the quantization pass, up projection as bfloat16 steps in the GEMM)
+    la, lb = workloads.make_lora(32, K, n, seed=5, device="cuda")
+    wsl = torch.empty(int(lib_lora_ws(nv, M, n, K, 32)), dtype=torch.uint8, device="cuda")
+    ms_lora = time_region(torch, lambda i: _ok(D.linear_lora(Xp, Wq, Ws, gw, la, lb, 32, 1.0, Y,
+                                                             wsl), "lora"), 20)
+    out["prefill_linear_4096x5120x5120_lora_r32"] = {
+        "linear_ms": ms_lin, "lora_ms": ms_lora, "TFLOP/s_lora": fl / ms_lora / 1e9}
+    del Xp, Wq, Ws, Y, Yq, Ys, ws, wsl, la, lb
     torch.cuda.empty_cache()
     # a5: decode (weight-bandwidth bound), rotating 3 weight copies (> L2)
     dec = workloads.WORKLOADS["decode"]

@@ -327,6 +327,39 @@ NVFP4_API nvfp4_status nvfp4_linear_bias_requant(const void *X, int64_t M, int64
                                                 void *stream);
 
 /*
+ * NVFP4 linear layer with a run-time low-rank (LoRA) correction, the LoRA
+ * kept beside the quantized weight ("nvfp4-difusion" page, section 3: a LoRA
+ * cannot be merged into NVFP4 codes; its computation is fused with the
+ * activation quantization in one CUDA pass instead):
+ *   Y = bf16( dequant(quantize(X, g_x)) * dequant(Wq, Ws, g_w)^T
+ *             + lora_scale * (X A^T) B^T )
+ * with the LoRA branch on the unquantized bfloat16 X. Launches: (g_x NULL:
+ * the global scale of X), one pass over X writing its NVFP4 codes and
+ * scales and the down projection L' = bf16(lora_scale / (g_x g_w) * X A^T)
+ * (tensor-core warp MMAs on the same loads), then the CTA-pair GEMM, which
+ * adds L' B^T into its FP32 accumulator with r / 16 bfloat16 tensor-core
+ * K-steps per tile before the epilogue scales by g_x g_w.
+ * lora_A: r x K bfloat16 (the down projection), lora_B: N x r bfloat16 (the
+ * up projection), both contiguous and 16-byte aligned; r in {16, 32, 48,
+ * 64}; lora_scale finite (alpha / r in the usual LoRA notation).
+ * Rounding of L' to bfloat16 puts a relative error of about 2^-9 on the
+ * correction term.
+ * M > 128 (the CTA-pair kernel; fewer rows return UNSUPPORTED_SHAPE).
+ * X, Wq, Ws, g_w, Y, g_x: as nvfp4_linear; workspace:
+ * nvfp4_linear_lora_workspace_bytes(M, N, K, r) bytes, 256-byte aligned.
+ * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_SHAPE,
+ * WORKSPACE_TOO_SMALL, CUDA.
+ */
+NVFP4_API nvfp4_status nvfp4_linear_lora(const void *X, int64_t M, int64_t K, int64_t ldx,
+                                        const uint8_t *Wq, const uint8_t *Ws, const float *g_w,
+                                        int64_t N, const void *lora_A, const void *lora_B,
+                                        int64_t r, float lora_scale, void *Y, int64_t ldy,
+                                        const float *g_x, void *workspace,
+                                        size_t workspace_bytes, void *stream);
+
+NVFP4_API size_t nvfp4_linear_lora_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r);
+
+/*
  * Synchronize the current device, then return NVFP4_ERR_TIMEOUT if any
  * kernel of this library recorded a bounded-wait timeout since the last
  * clear, NVFP4_ERR_CUDA if the synchronization failed, else NVFP4_OK.

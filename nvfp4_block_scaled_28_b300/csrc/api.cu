@@ -1,5 +1,6 @@
 // C ABI of the NVFP4 library: argument checks, status codes, workspace
 // carving and the launch sequences of each entry point (see include/nvfp4.h).
+#include <cmath>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -348,6 +349,60 @@ nvfp4_status nvfp4_linear_grouped(const void *X, int64_t M, int64_t K, int64_t l
     }
     return linear_impl(X, M, K, ldx, Wq, Ws, g_w, N, Y, ldy, g_x, mode, workspace,
                        workspace_bytes, stream, wg);
+}
+
+size_t nvfp4_linear_lora_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r) {
+    if (M < 0 || N < 0 || K < 0 || r < 0 || K % 256 != 0) return 0;
+    return nvfp4_linear_workspace_bytes(M, N, K, NVFP4_LINEAR_UNFUSED) +
+           round_up(static_cast<size_t>(M) * static_cast<size_t>(r) * 2, 256);
+}
+
+nvfp4_status nvfp4_linear_lora(const void *X, int64_t M, int64_t K, int64_t ldx,
+                               const uint8_t *Wq, const uint8_t *Ws, const float *g_w, int64_t N,
+                               const void *lora_A, const void *lora_B, int64_t r,
+                               float lora_scale, void *Y, int64_t ldy, const float *g_x,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+    nvfp4_status s = check_bf16_matrix(X, M, K, ldx);
+    if (s != NVFP4_OK) return s;
+    s = check_gemm_b_and_y(Wq, Ws, g_w, M, N, K, Y, ldy);
+    if (s != NVFP4_OK) return s;
+    if (r != 16 && r != 32 && r != 48 && r != 64) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!std::isfinite(lora_scale)) return NVFP4_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return NVFP4_OK;
+    // the up projection rides in the CTA-pair kernel, the one used above 128 rows
+    if (M <= kSkinnyMaxM || !gemm_use_pair()) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (M * (K / 16) >= kMaxBlocks) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (lora_A == nullptr || lora_B == nullptr) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(lora_A, 16) || !aligned(lora_B, 16)) return NVFP4_ERR_MISALIGNED;
+    if (g_x != nullptr && !aligned(g_x, 4)) return NVFP4_ERR_MISALIGNED;
+    const size_t need = nvfp4_linear_lora_workspace_bytes(M, N, K, r);
+    if (workspace_bytes < need) return NVFP4_ERR_WORKSPACE_TOO_SMALL;
+    if (workspace == nullptr) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return NVFP4_ERR_MISALIGNED;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *gx_slot = reinterpret_cast<float *>(ws);
+    uint8_t *xq = ws + kLinearHeader;
+    uint8_t *xs = xq + round_up(static_cast<size_t>(M) * static_cast<size_t>(K / 2), 256);
+    uint16_t *Lp = reinterpret_cast<uint16_t *>(
+        ws + nvfp4_linear_workspace_bytes(M, N, K, NVFP4_LINEAR_UNFUSED));
+    const uint16_t *Xh = static_cast<const uint16_t *>(X);
+    if (g_x == nullptr) {
+        if (launch_global_scale(Xh, M, K, ldx, gx_slot, st) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        g_x = gx_slot;
+    }
+    // one pass over X: codes, scales and the pre-scaled down projection
+    if (launch_quantize_lora(Xh, M, K, ldx, g_x, g_w, lora_scale,
+                             static_cast<const uint16_t *>(lora_A), r, xq, xs, Lp,
+                             st) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    GemmArgs a{xq, xs, g_x, Wq, Ws, g_w, M, N, K, static_cast<uint16_t *>(Y), ldy};
+    a.lora_Lp = Lp;
+    a.lora_B = static_cast<const uint16_t *>(lora_B);
+    a.lora_r = r;
+    return from_cuda(launch_gemm_pair(a, st));
 }
 
 nvfp4_status nvfp4_linear_bias_requant(const void *X, int64_t M, int64_t K, int64_t ldx,

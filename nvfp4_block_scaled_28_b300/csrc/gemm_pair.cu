@@ -65,6 +65,9 @@ constexpr int SF_TILE = 512;
 constexpr int SF_ROW = 256;                // scale arrays as rows of 256 bytes
 constexpr int CTA_STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
 constexpr uint32_t STAGE_TX = 2 * CTA_STAGE_BYTES;  // both CTAs, counted at rank 0
+// LoRA stage (after a tile's FP4 stages): L' (128 rows x 64 bfloat16) in the
+// A slot, the up projection (128 rows x 64 bfloat16) in the B slot, no scales
+constexpr uint32_t LORA_TX = 2 * (A_BYTES + B_BYTES);
 constexpr int MMAS_PER_STAGE = BK / 64;    // 4
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;            // 256 FP32 columns
@@ -112,6 +115,7 @@ struct Params {
     uint8_t *Yq;
     uint8_t *Ys;
     WeightGroups groups;  // grouped projection: g_b holds one scale per group
+    int lora_r;           // > 0: one LoRA stage of lora_r / 16 bfloat16 K-steps per tile
     int inject;          // 1: the producers issue nothing (bounded-wait test)
     uint64_t timeout_ns;
     unsigned int *err;   // device error word
@@ -179,7 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tmSA,
                      const __grid_constant__ CUtensorMap tmSB,
                      const __grid_constant__ CUtensorMap tmY,
-                     const __grid_constant__ CUtensorMap tmYq, const Params p) {
+                     const __grid_constant__ CUtensorMap tmYq,
+                     const __grid_constant__ CUtensorMap tmL,
+                     const __grid_constant__ CUtensorMap tmLB, const Params p) {
     // tmSA: A scales as rows of 256 B (8 rows per stage); tmSB: B scales as
     // {256 B, rows of a 128-row group, group} (8 rows x 2 groups per stage)
     extern __shared__ uint8_t smem_raw[];
@@ -214,6 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmSB);
         if (p.y_tma) tma_prefetch_desc(&tmY);
         if (kEpi && p.Yq != nullptr) tma_prefetch_desc(&tmYq);
+        if (kEpi && p.lora_r > 0) {
+            tma_prefetch_desc(&tmL);
+            tma_prefetch_desc(&tmLB);
+        }
     }
     if (warp == 2) {
         tmem_alloc_pair(&sh.tmem_base, TMEM_COLS);
@@ -264,6 +274,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 __syncwarp();
+            }
+            if (kEpi && ok && p.lora_r > 0) {
+                // the tile's LoRA stage: A/B producer only (no scales)
+                const int s = g % STAGES;
+                if (!scales) {
+                    if (!warp_wait(&sh.empty[s], ((g / STAGES) & 1) ^ 1, p, sh)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        const uint32_t bar = full0 + static_cast<uint32_t>(s) * 8u;
+                        if (leader) mbar_arrive_expect_tx(&sh.full[s], LORA_TX);
+                        tma_load_2d_pair(smem + SMEM_A + s * A_BYTES, &tmL, bar, 0, arow, pol);
+                        tma_load_2d_pair(smem + SMEM_B + s * B_BYTES, &tmLB, bar, 0, brow, pol);
+                    }
+                    __syncwarp();
+                }
+                ++g;
             }
         }
         if (ok) {
@@ -316,6 +344,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             sdesc_sf(sfb_smem + j * SF_TILE),
                                             sdesc_sf(sfb_smem + SFB_BYTES / 2 + j * SF_TILE));
                 tc_commit_pair_mc_elect(&sh.empty[s], kPairMask);
+            }
+            if (kEpi && ok && p.lora_r > 0) {
+                // LoRA up projection into the same accumulator: L' (this
+                // pair's 256 rows x r) times the up-projection rows (256 x r),
+                // r / 16 bfloat16 K-steps of 32 bytes in the swizzled rows
+                constexpr uint32_t idesc_l = idesc_bf16(PM, BN);
+                const int s = g % STAGES;
+                if (!warp_wait(&sh.full[s], (g / STAGES) & 1, p, sh)) {
+                    ok = false;
+                } else {
+                    tc_fence_after();
+                    const uint32_t a_smem = smem_addr(smem + SMEM_A + s * A_BYTES);
+                    const uint32_t b_smem = smem_addr(smem + SMEM_B + s * B_BYTES);
+                    for (int j = 0; j < p.lora_r / 16; ++j)
+                        mma_bf16_pair_elect(tmem + ACC_COL, sdesc_sw128(a_smem + j * 32),
+                                            sdesc_sw128(b_smem + j * 32), idesc_l, 1u);
+                    tc_commit_pair_mc_elect(&sh.empty[s], kPairMask);
+                    ++g;
+                }
             }
             if (ok) tc_commit_pair_mc_elect(&sh.acc_full, kPairMask);
         }
@@ -545,6 +592,17 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     const bool y_tma = y_vec && make_map_2d(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.Y, a.N, a.M,
                                             a.ldy * 2, EPI_CHUNK, 32, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!y_tma) memset(&tmY, 0, sizeof(tmY));
+    // LoRA operands: L' (M x r) and the up projection (N x r), bfloat16,
+    // 128-row x 64-element boxes (columns past r read as 0)
+    CUtensorMap tmL, tmLB;
+    memset(&tmL, 0, sizeof(tmL));
+    memset(&tmLB, 0, sizeof(tmLB));
+    if (a.lora_Lp != nullptr &&
+        (!make_map_2d(&tmL, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.lora_Lp, a.lora_r, a.M,
+                      a.lora_r * 2, 64u, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+         !make_map_2d(&tmLB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.lora_B, a.lora_r, a.N,
+                      a.lora_r * 2, 64u, BNH, CU_TENSOR_MAP_SWIZZLE_128B)))
+        return cudaErrorInvalidValue;
     // re-quantized codes: rows of N/2 bytes, 32-row x 64-byte boxes
     CUtensorMap tmYq;
     memset(&tmYq, 0, sizeof(tmYq));
@@ -571,6 +629,7 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     p.Yq = a.Yq;
     p.Ys = a.Ys;
     p.groups = a.groups;
+    p.lora_r = a.lora_Lp != nullptr ? static_cast<int>(a.lora_r) : 0;
     p.inject = debug_state().inject;
     p.timeout_ns = debug_state().timeout_ns;
     p.err = device_error_word();
@@ -589,11 +648,12 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    const bool epi = !store_y || a.bias != nullptr || a.Yq != nullptr || a.groups.count > 1;
+    const bool epi = !store_y || a.bias != nullptr || a.Yq != nullptr || a.groups.count > 1 ||
+                     a.lora_Lp != nullptr;
     cudaError_t e = epi ? cudaLaunchKernelEx(&cfg, gemm_pair_kernel<true>, tmA, tmB, tmSA, tmSB,
-                                             tmY, tmYq, p)
+                                             tmY, tmYq, tmL, tmLB, p)
                         : cudaLaunchKernelEx(&cfg, gemm_pair_kernel<false>, tmA, tmB, tmSA, tmSB,
-                                             tmY, tmYq, p);
+                                             tmY, tmYq, tmL, tmLB, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -107,7 +107,20 @@ struct GemmArgs {
     uint8_t *Yq = nullptr;
     uint8_t *Ys = nullptr;
     WeightGroups groups;  // g_b then points at groups.count floats
+    // LoRA: L' (M x lora_r bfloat16, pre-scaled by lora_scale / (g_a g_b))
+    // and the up projection (N x lora_r bfloat16) add L' B^T to the FP4
+    // accumulator; lora_r in {16, 32, 48, 64}
+    const uint16_t *lora_Lp = nullptr;
+    const uint16_t *lora_B = nullptr;
+    int64_t lora_r = 0;
 };
+
+// The fused pass for a LoRA linear: NVFP4 codes + tile-layout scales of X
+// (given g_x) and L' = bf16((lora_scale / (g_x g_w)) X A^T), A r x K.
+cudaError_t launch_quantize_lora(const uint16_t *X, int64_t rows, int64_t K, int64_t ldx,
+                                 const float *g_x, const float *g_w, float lora_scale,
+                                 const uint16_t *A, int64_t r, uint8_t *q, uint8_t *sf,
+                                 uint16_t *Lp, cudaStream_t st);
 
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st);
 // The same GEMM on CTA pairs (tcgen05 cta_group::2), 256 x 256 tiles.

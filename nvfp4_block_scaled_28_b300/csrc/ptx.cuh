@@ -579,6 +579,19 @@ __device__ __forceinline__ void mma_mxf4nvf4_pair_elect(uint32_t d_tmem, uint64_
         : "memory");
 }
 
+// D[tmem] (+)= A x B^T on CTA pairs, BF16 inputs, K = 16 (kind::f16).
+__device__ __forceinline__ void mma_bf16_pair_elect(uint32_t d_tmem, uint64_t adesc,
+                                                    uint64_t bdesc, uint32_t idesc,
+                                                    uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // One K = 64 step of the pair MMA with its scales, under a single elect:
 // the three scale copies (as sf_copy3_pair_elect) then the MMA reading
 // them. Copies and MMA from one thread reach both SMs' tensor cores in

@@ -268,6 +268,42 @@ def nvfp4_linear_grouped(X: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor,
     return Y
 
 
+def nvfp4_linear_lora(X: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, g_w: torch.Tensor,
+                      lora_A: torch.Tensor, lora_B: torch.Tensor, lora_scale: float,
+                      g_x: torch.Tensor | None = None, Y: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """NVFP4 linear with a run-time LoRA correction lora_scale * (X A^T) B^T
+    (A: (r, K), B: (N, r) bfloat16, r in 16/32/48/64) on the unquantized
+    activation; the down projection is computed in the quantization pass."""
+    _check_bf16_2d(X, "X")
+    M, K = X.shape
+    Nn = Wq.shape[0]
+    _check_codes(Wq, Nn, K, "Wq")
+    _check_scales(Ws, Nn, K, SF_MMA_128x4, "Ws")
+    _check_g(g_w, "g_w")
+    if g_x is not None:
+        _check_g(g_x, "g_x")
+    r = lora_A.shape[0]
+    _require(lora_A.dtype == torch.bfloat16 and tuple(lora_A.shape) == (r, K)
+             and lora_A.is_contiguous(), "lora_A must be a contiguous bfloat16 (r, K) tensor")
+    _require(lora_B.dtype == torch.bfloat16 and tuple(lora_B.shape) == (Nn, r)
+             and lora_B.is_contiguous(), "lora_B must be a contiguous bfloat16 (N, r) tensor")
+    _check_cuda(X, Wq, Ws, g_w, g_x, lora_A, lora_B, Y, workspace)
+    if Y is None:
+        Y = torch.empty((M, Nn), dtype=torch.bfloat16, device=X.device)
+    _check_bf16_2d(Y, "Y")
+    _require(tuple(Y.shape) == (M, Nn), "Y must have shape (%d, %d)" % (M, Nn))
+    need = int(N.load().nvfp4_linear_lora_workspace_bytes(M, Nn, K, r))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=X.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    N.check("nvfp4_linear_lora", N.load().nvfp4_linear_lora(
+        _ptr(X), M, K, X.stride(0), _ptr(Wq), _ptr(Ws), _ptr(g_w), Nn, _ptr(lora_A),
+        _ptr(lora_B), r, float(lora_scale), _ptr(Y), Y.stride(0), _ptr(g_x), _ptr(workspace),
+        ws_bytes, _stream()))
+    return Y
+
+
 def nvfp4_linear_noalloc(X: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor,
                          g_w: torch.Tensor, g_x: torch.Tensor | None = None,
                          Y: torch.Tensor | None = None) -> torch.Tensor:

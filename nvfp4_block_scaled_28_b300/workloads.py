@@ -98,3 +98,13 @@ def make_bias(N: int, seed: int, std: float = 0.5, device: str = "cpu") -> torch
     g = torch.Generator(device=device).manual_seed(seed)
     b = torch.randn((N,), generator=g, dtype=torch.float32, device=device) * std
     return b.to(torch.bfloat16)
+
+
+def make_lora(r: int, K: int, N: int, seed: int, std: float = 0.02, device: str = "cpu"):
+    """LoRA factors (A: (r, K) down projection, B: (N, r) up projection),
+    bfloat16, both ~N(0, std^2) (CPU generator by default); with unit-variance
+    activations the correction is about a tenth of the layer's output."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    a = torch.randn((r, K), generator=g, dtype=torch.float32, device=device) * std
+    b = torch.randn((N, r), generator=g, dtype=torch.float32, device=device) * std
+    return a.to(torch.bfloat16), b.to(torch.bfloat16)

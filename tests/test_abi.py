@@ -190,3 +190,21 @@ def test_quantize_select_argument_checks(lib):
     assert f(ODD, 4, 64, 64, A16, 1, A16, A16, 0, None) == N.ERR_MISALIGNED
     assert f(A16, 4, 64, 64, None, 1, A16, A16, 0, None) == N.ERR_INVALID_ARG   # no g
     assert f(A16, 0, 64, 64, A16, 2, A16, A16, 0, None) == N.OK                 # empty
+
+
+def test_linear_lora_argument_checks(lib):
+    f = lib.nvfp4_linear_lora
+    base = dict(X=A16, M=256, K=512, ldx=512, Wq=A16, Ws=A16, gw=A16, N=256, la=A16, lb=A16,
+                r=32, s=1.0, Y=A16, ldy=256, gx=None, ws=A16 * 16, wsb=1 << 30)
+    call = lambda **kw: f(*[{**base, **kw}[k] for k in base], None)
+    assert call(M=128) == N.ERR_UNSUPPORTED_SHAPE          # the CTA-pair kernel: M > 128
+    assert call(r=24) == N.ERR_UNSUPPORTED_SHAPE           # r in 16, 32, 48, 64
+    assert call(r=128) == N.ERR_UNSUPPORTED_SHAPE
+    assert call(K=448, ldx=448) == N.ERR_UNSUPPORTED_SHAPE
+    assert call(s=float("nan")) == N.ERR_INVALID_ARG
+    assert call(la=None) == N.ERR_INVALID_ARG
+    assert call(lb=A16 + 8) == N.ERR_MISALIGNED
+    assert call(wsb=16) == N.ERR_WORKSPACE_TOO_SMALL
+    assert call(M=0) == N.OK
+    need = lib.nvfp4_linear_lora_workspace_bytes(256, 256, 512, 32)
+    assert need >= lib.nvfp4_linear_workspace_bytes(256, 256, 512, 0) + 256 * 32 * 2
