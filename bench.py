@@ -63,6 +63,8 @@ def gemm_traffic_per_launch():
 
 # Dense FP4 rate measured by the library's tcgen05 probe (profiles/mma_peak_probe.md)
 FP4_PROBE_PEAK_TFLOPS = 9230.0
+# NVIDIA's nominal dense NVFP4 rate of one B300 (context only)
+FP4_NOMINAL_DENSE_TFLOPS = 13500.0
 
 
 def measured_peaks():
@@ -360,6 +362,7 @@ def run_native(args):
                 "timing": "CUDA events over %d GEMM-only launches on the step's rotating "
                           "input sets, right after the timed steps" % gemm_iters,
                 "frac_of_probe_peak": achieved / FP4_PROBE_PEAK_TFLOPS,
+                "frac_of_nominal_fp4": achieved / FP4_NOMINAL_DENSE_TFLOPS,
                 "gemm_ms": gemm_ms, "traffic": gemm_traffic_per_launch(),
                 "traffic_unit": "bytes per launch (ncu dram read + write)"}
 
@@ -487,6 +490,13 @@ def extra_rows(torch, nv, D, workloads, peaks):
     gy = nv.nvfp4_global_scale(Y)
     fl = 2.0 * M * n * K
     ms_lin = time_region(torch, lambda i: _ok(D.linear(Xp, Wq, Ws, gw, Y, None, 0, ws), "lin"), 20)
+    gxp = nv.nvfp4_global_scale(Xp)
+    ms_lin_gx = time_region(torch, lambda i: _ok(D.linear(Xp, Wq, Ws, gw, Y, gxp, 0, ws), "lin"),
+                            20)
+    out["prefill_linear_4096x5120x5120_given_gx"] = {
+        "ms": ms_lin_gx, "TFLOP/s": fl / ms_lin_gx / 1e9,
+        "note": "given activation global scale (quantize_kernel + GEMM); the headline step "
+                "computes it from X"}
     ms_seq = time_region(torch, lambda i: (_ok(D.linear(Xp, Wq, Ws, gw, Y, None, 0, ws), "lin"),
                                            _ok(D.quantize(Y, gy, Yq, Ys, nv.SF_MMA_128x4), "q")),
                          20)
