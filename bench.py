@@ -627,8 +627,8 @@ def run_reference(args):
 
 def run_single_op(args):
     """One kernel on one shape, for profiling: --op gemm|quantize|linear|
-    linear_bias_requant|linear_requant_only --shape M,N,K (quantize uses
-    M,K). Prints the mean CUDA-event time."""
+    linear_bias_requant|linear_requant_only|linear_lora --shape M,N,K
+    (quantize uses M,K). Prints the mean CUDA-event time."""
     import torch
 
     import nvfp4_block_scaled_28_b300 as nv
@@ -684,6 +684,12 @@ def run_single_op(args):
         if args.op == "gemm":
             Xq, Xs = nv.nvfp4_quantize(X, g, nv.SF_MMA_128x4)
             fn = lambda i: _ok(D.gemm(Xq, Xs, g, Wq, Ws, gw, M, Nn, K, Y), "gemm")
+        elif args.op == "linear_lora":
+            # rank-32 LoRA correction (--iters unused)
+            la, lb = workloads.make_lora(32, K, Nn, seed=5, device="cuda")
+            ws = torch.empty(int(lib_lora_ws(nv, M, Nn, K, 32)), dtype=torch.uint8,
+                             device="cuda")
+            fn = lambda i: _ok(D.linear_lora(X, Wq, Ws, gw, la, lb, 32, 1.0, Y, ws), "lora")
         elif args.op in ("linear_bias_requant", "linear_requant_only"):
             # bias add + NVFP4 re-quantization of Y in the GEMM epilogue
             # (requant_only: no bfloat16 Y is stored)
@@ -723,7 +729,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=256)
     ap.add_argument("--op", choices=["gemm", "quantize", "linear", "linear_bias_requant",
-                                     "linear_requant_only", "mma_peak"], default=None,
+                                     "linear_requant_only", "linear_lora", "mma_peak"],
+                    default=None,
                     help="time a single kernel on --shape instead of the benchmark step")
     ap.add_argument("--shape", default="8192,8192,8192", help="M,N,K for --op")
     ap.add_argument("--iters", type=int, default=200000, help="--op mma_peak: MMAs per CTA")

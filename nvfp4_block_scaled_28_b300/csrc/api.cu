@@ -354,7 +354,8 @@ nvfp4_status nvfp4_linear_grouped(const void *X, int64_t M, int64_t K, int64_t l
 size_t nvfp4_linear_lora_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r) {
     if (M < 0 || N < 0 || K < 0 || r < 0 || K % 256 != 0) return 0;
     return nvfp4_linear_workspace_bytes(M, N, K, NVFP4_LINEAR_UNFUSED) +
-           round_up(static_cast<size_t>(M) * static_cast<size_t>(r) * 2, 256);
+           round_up(static_cast<size_t>(M) * static_cast<size_t>(r) * 2, 256) +
+           round_up(lora_partial_bytes(M, r), 256);
 }
 
 nvfp4_status nvfp4_linear_lora(const void *X, int64_t M, int64_t K, int64_t ldx,
@@ -385,8 +386,10 @@ nvfp4_status nvfp4_linear_lora(const void *X, int64_t M, int64_t K, int64_t ldx,
     float *gx_slot = reinterpret_cast<float *>(ws);
     uint8_t *xq = ws + kLinearHeader;
     uint8_t *xs = xq + round_up(static_cast<size_t>(M) * static_cast<size_t>(K / 2), 256);
-    uint16_t *Lp = reinterpret_cast<uint16_t *>(
-        ws + nvfp4_linear_workspace_bytes(M, N, K, NVFP4_LINEAR_UNFUSED));
+    uint8_t *lora_ws = ws + nvfp4_linear_workspace_bytes(M, N, K, NVFP4_LINEAR_UNFUSED);
+    uint16_t *Lp = reinterpret_cast<uint16_t *>(lora_ws);
+    float *part = reinterpret_cast<float *>(
+        lora_ws + round_up(static_cast<size_t>(M) * static_cast<size_t>(r) * 2, 256));
     const uint16_t *Xh = static_cast<const uint16_t *>(X);
     if (g_x == nullptr) {
         if (launch_global_scale(Xh, M, K, ldx, gx_slot, st) != cudaSuccess)
@@ -395,7 +398,7 @@ nvfp4_status nvfp4_linear_lora(const void *X, int64_t M, int64_t K, int64_t ldx,
     }
     // one pass over X: codes, scales and the pre-scaled down projection
     if (launch_quantize_lora(Xh, M, K, ldx, g_x, g_w, lora_scale,
-                             static_cast<const uint16_t *>(lora_A), r, xq, xs, Lp,
+                             static_cast<const uint16_t *>(lora_A), r, xq, xs, part, Lp,
                              st) != cudaSuccess)
         return NVFP4_ERR_CUDA;
     GemmArgs a{xq, xs, g_x, Wq, Ws, g_w, M, N, K, static_cast<uint16_t *>(Y), ldy};

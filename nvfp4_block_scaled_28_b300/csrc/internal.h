@@ -116,11 +116,14 @@ struct GemmArgs {
 };
 
 // The fused pass for a LoRA linear: NVFP4 codes + tile-layout scales of X
-// (given g_x) and L' = bf16((lora_scale / (g_x g_w)) X A^T), A r x K.
+// (given g_x) and the down projection X A^T (A r x K) per K range into
+// `part` (lora_partial_bytes), then L' = bf16((lora_scale / (g_x g_w)) *
+// the ranges' sum, in range order).
 cudaError_t launch_quantize_lora(const uint16_t *X, int64_t rows, int64_t K, int64_t ldx,
                                  const float *g_x, const float *g_w, float lora_scale,
                                  const uint16_t *A, int64_t r, uint8_t *q, uint8_t *sf,
-                                 uint16_t *Lp, cudaStream_t st);
+                                 float *part, uint16_t *Lp, cudaStream_t st);
+size_t lora_partial_bytes(int64_t rows, int64_t r);
 
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st);
 // The same GEMM on CTA pairs (tcgen05 cta_group::2), 256 x 256 tiles.

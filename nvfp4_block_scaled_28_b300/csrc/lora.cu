@@ -11,13 +11,15 @@
 // FP4 products (extra bfloat16 tensor-core steps) before its epilogue
 // multiplies everything by g_x * g_w.
 //
-// Work split: a CTA owns 16 rows; its 8 warps take 64-column chunks of K
-// round robin. Per 16 x 16 piece a warp holds the bfloat16 values in the
-// register layout of mma.sync m16n8k16 (lane = 4 g + c: rows g and g + 8,
-// columns 2c, 2c + 1, 8 + 2c, 9 + 2c), so one load feeds both the quantizer
-// (a 16-element block is one row of the piece, spread over a lane quad) and
-// the tensor-core product with A. The warps' partial products are summed in
-// warp order (deterministic).
+// Work split: a CTA owns 64 rows (16 per warp) and one K range; the K
+// ranges' partial down projections go to FP32 workspace and a small kernel
+// sums them in range order (deterministic) and applies the scale. X and A
+// chunks of 64 columns stream into a 4-deep shared-memory ring (cp.async,
+// 16-byte pieces, XOR-swizzled rows). From each chunk in shared memory the
+// threads quantize one 16-element block each (the standalone quantizer's
+// arithmetic) and the warps take their 16 x 16 pieces with ldmatrix for the
+// tensor-core product with A (mma.sync m16n8k16), so X is read from HBM once
+// for both.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -29,7 +31,10 @@ namespace nvfp4 {
 
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 4;
+constexpr int kRows = 16 * kWarps;  // rows per CTA
+constexpr int kStages = 4;          // shared-memory ring depth (64-column chunks)
+constexpr int kMaxSplit = 8;        // K ranges per row tile
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
                                                uint32_t a2, uint32_t a3, uint32_t b0,
@@ -41,138 +46,224 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t ld_u32(const uint16_t *p) {
-    return __ldg(reinterpret_cast<const unsigned int *>(p));
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                            uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
 }
 
-// Scale byte and the two code words of one 16-element block held by a lane
-// quad: this lane has elements (2c, 2c+1) in w_lo and (8+2c, 9+2c) in w_hi.
-// Returns S; `lo` / `hi` get the block's code bytes 0..3 / 4..7 (every lane
-// of the quad ends with the same words).
-__device__ __forceinline__ uint32_t quantize_quad(uint32_t w_lo, uint32_t w_hi, int c, float g,
-                                                  uint32_t &lo, uint32_t &hi) {
-    uint32_t m = max_u16x2(w_lo & 0x7FFF7FFFu, w_hi & 0x7FFF7FFFu);
-    m = max(m & 0xFFFFu, m >> 16);
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-    const float amax = __uint_as_float(m << 16);
-    const float v = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
-    const uint32_t S = cvt_e4m3_satfinite(v);
-    const float s = e4m3_to_f32(S);
-    const float denom = __fmul_rn(s, g);
-    const float r = denom > 0.0f ? __frcp_rn(denom) : 0.0f;
-    const uint64_t rr = (static_cast<uint64_t>(__float_as_uint(r)) << 32) | __float_as_uint(r);
-    lo = codes2(w_lo, rr) << (8 * c);
-    hi = codes2(w_hi, rr) << (8 * c);
-    lo |= __shfl_xor_sync(0xFFFFFFFFu, lo, 1);
-    hi |= __shfl_xor_sync(0xFFFFFFFFu, hi, 1);
-    lo |= __shfl_xor_sync(0xFFFFFFFFu, lo, 2);
-    hi |= __shfl_xor_sync(0xFFFFFFFFu, hi, 2);
-    return S;
+// 16-byte global -> shared copy; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Byte offset of 16-byte piece `p` of row `r` in a ring tile of 128-byte rows.
+__device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t p) {
+    return r * 128u + ((p ^ (r & 7u)) << 4);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
 }
 
 template <int R>
+struct LoraCfg {
+    static constexpr int X_TILE = kRows * 128;  // 64 bfloat16 per row (8 KiB)
+    static constexpr int A_TILE = R * 128;
+    static constexpr int SMEM = kStages * (X_TILE + A_TILE);
+};
+
+// Grid: (row tiles of 128, K ranges). part: FP32 [range][rows_pad][R].
+template <int R>
 __global__ void __launch_bounds__(32 * kWarps)
     quantize_lora_kernel(const uint16_t *__restrict__ X, uint32_t rows, uint32_t K, uint64_t ldx,
-                         const float *__restrict__ g_x, const float *__restrict__ g_w,
-                         float lora_scale, const uint16_t *__restrict__ A, uint8_t *__restrict__ q,
-                         uint8_t *__restrict__ sf, uint16_t *__restrict__ Lp) {
-    __shared__ float red[kWarps][16][R];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+                         const float *__restrict__ g_x, const uint16_t *__restrict__ A,
+                         uint32_t chunks_per_range, uint32_t rows_pad, uint8_t *__restrict__ q,
+                         uint8_t *__restrict__ sf, float *__restrict__ part) {
+    using C = LoraCfg<R>;
+    extern __shared__ __align__(128) uint8_t lsmem[];
+    const uint32_t xs0 = smem_addr(lsmem);
+    const uint32_t as0 = xs0 + kStages * C::X_TILE;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, c = lane & 3;
-    const uint32_t row0 = blockIdx.x * 16u;
-    const uint32_t ra = row0 + gq, rb = ra + 8;
+    const uint32_t row0 = blockIdx.x * kRows;
     const uint32_t kb4 = K / 64;
+    const uint32_t c_begin = blockIdx.y * chunks_per_range;
+    const uint32_t c_end = min(kb4, c_begin + chunks_per_range);
+    const int nch = static_cast<int>(c_end - c_begin);
     pdl_launch_dependents();
     pdl_wait();
-    if (row0 >= rows) {
-        // padding rows of the 128-row scale tiles: scale 0
-        for (uint32_t i = threadIdx.x; i < 16u * kb4; i += blockDim.x)
-            *reinterpret_cast<uint32_t *>(sf + sf_mma_offset(row0 + i / kb4, (i % kb4) * 4, kb4)) =
-                0u;
-        return;
-    }
-    const bool va = ra < rows, vb = rb < rows;
     const float g = *g_x;
-    const uint16_t *xa = X + static_cast<uint64_t>(va ? ra : 0) * ldx;
-    const uint16_t *xb = X + static_cast<uint64_t>(vb ? rb : 0) * ldx;
+
+    // one chunk of X (128 rows x 128 B) and of A (R rows x 128 B) into slot s
+    auto load = [&](int s, uint32_t ch) {
+#pragma unroll
+        for (int i = 0; i < kRows * 8 / (32 * kWarps); ++i) {
+            const uint32_t p = tid + i * 32 * kWarps;
+            const uint32_t r = p >> 3, piece = p & 7u;
+            const bool ok = row0 + r < rows;
+            const uint16_t *src = X + (ok ? (row0 + r) * ldx : 0) + ch * 64u + piece * 8u;
+            cp_async16(xs0 + s * C::X_TILE + swz(r, piece), src, ok ? 16u : 0u);
+        }
+        for (uint32_t p = tid; p < R * 8u; p += 32 * kWarps) {
+            const uint32_t j = p >> 3, piece = p & 7u;
+            cp_async16(as0 + s * C::A_TILE + swz(j, piece),
+                       A + static_cast<uint64_t>(j) * K + ch * 64u + piece * 8u, 16u);
+        }
+    };
+#pragma unroll
+    for (int s = 0; s < kStages - 1; ++s) {
+        if (s < nch) load(s, c_begin + s);
+        cp_async_commit();
+    }
+
     float acc[R / 8][4];
 #pragma unroll
     for (int n = 0; n < R / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
-
-    for (uint32_t ch = warp; ch < kb4; ch += kWarps) {
-        uint32_t qa0 = 0, qa1 = 0, qb0 = 0, qb1 = 0, sa = 0, sb = 0;
+    const uint32_t ra = row0 + warp * 16 + gq;
+    // ldmatrix lane roles: matrix m = lane / 8, row lane % 8
+    const uint32_t lm = lane >> 3, lr = lane & 7;
+    const uint32_t a_row = warp * 16 + (lm & 1u) * 8 + lr;  // X piece rows of this lane
+    for (int i = 0; i < nch; ++i) {
+        cp_async_wait<kStages - 2>();
+        __syncthreads();  // chunk i landed; every warp is done with chunk i - 1
+        if (i + kStages - 1 < nch) load((i + kStages - 1) % kStages, c_begin + i + kStages - 1);
+        cp_async_commit();
+        const int s = i % kStages;
+        const uint32_t xs = xs0 + s * C::X_TILE, as = as0 + s * C::A_TILE;
+        const uint32_t ch = c_begin + i;
+        // quantization: one thread per 16-element block (4 per row of the
+        // chunk), the standalone quantizer's arithmetic; the four lanes of a
+        // row gather its scale bytes into one aligned word of the tile layout
+#pragma unroll
+        for (int u = 0; u < kRows * 4 / (32 * kWarps); ++u) {
+            const uint32_t id = tid + u * 32 * kWarps;
+            const uint32_t r = id >> 2, blk = id & 3u;
+            const uint4 a = lds128(xs + swz(r, 2u * blk)), b = lds128(xs + swz(r, 2u * blk + 1u));
+            uint32_t lo, hi;
+            const uint32_t S = quantize16(a, b, g, lo, hi);
+            const uint32_t row = row0 + r;
+            if (row < rows)
+                *reinterpret_cast<uint2 *>(q + static_cast<uint64_t>(row) * (K / 2) + ch * 32u +
+                                           blk * 8u) = make_uint2(lo, hi);
+            uint32_t w = S << (8u * blk);
+            w |= __shfl_xor_sync(0xFFFFFFFFu, w, 1);
+            w |= __shfl_xor_sync(0xFFFFFFFFu, w, 2);
+            if (blk == 0) *reinterpret_cast<uint32_t *>(sf + sf_mma_offset(row, ch * 4u, kb4)) = w;
+        }
+        // down projection: this warp's 16 rows times the chunk of A
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t k0 = ch * 64u + ks * 16u + 2u * c;
-            const uint32_t a0 = va ? ld_u32(xa + k0) : 0u, a2 = va ? ld_u32(xa + k0 + 8) : 0u;
-            const uint32_t a1 = vb ? ld_u32(xb + k0) : 0u, a3 = vb ? ld_u32(xb + k0 + 8) : 0u;
-            uint32_t lo, hi;
-            sa |= quantize_quad(a0, a2, c, g, lo, hi) << (8 * ks);
-            if (c == ks) {
-                qa0 = lo;
-                qa1 = hi;
-            }
-            sb |= quantize_quad(a1, a3, c, g, lo, hi) << (8 * ks);
-            if (c == ks) {
-                qb0 = lo;
-                qb1 = hi;
-            }
+            uint32_t a0, a1, a2, a3;
+            ldmatrix_x4(xs + swz(a_row, 2u * ks + (lm >> 1)), a0, a1, a2, a3);
 #pragma unroll
-            for (int n = 0; n < R / 8; ++n) {
-                const uint16_t *arow = A + static_cast<uint64_t>(n * 8 + gq) * K + k0;
-                mma_bf16_16816(acc[n], a0, a1, a2, a3, ld_u32(arow), ld_u32(arow + 8));
+            for (int pr = 0; pr < R / 16; ++pr) {
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4(as + swz(pr * 16u + (lm >> 1) * 8u + lr, 2u * ks + (lm & 1u)), b0, b1,
+                            b2, b3);
+                mma_bf16_16816(acc[2 * pr], a0, a1, a2, a3, b0, b1);
+                mma_bf16_16816(acc[2 * pr + 1], a0, a1, a2, a3, b2, b3);
             }
         }
-        // lane c stores block c of the chunk for both rows; lanes 0 / 1 the
-        // rows' four scale bytes (one aligned word of the tile layout)
-        if (va)
-            *reinterpret_cast<uint2 *>(q + static_cast<uint64_t>(ra) * (K / 2) + ch * 32u + c * 8u) =
-                make_uint2(qa0, qa1);
-        if (vb)
-            *reinterpret_cast<uint2 *>(q + static_cast<uint64_t>(rb) * (K / 2) + ch * 32u + c * 8u) =
-                make_uint2(qb0, qb1);
-        if (c == 0)
-            *reinterpret_cast<uint32_t *>(sf + sf_mma_offset(ra, ch * 4u, kb4)) = va ? sa : 0u;
-        if (c == 1)
-            *reinterpret_cast<uint32_t *>(sf + sf_mma_offset(rb, ch * 4u, kb4)) = vb ? sb : 0u;
     }
+    cp_async_wait<0>();
+    // this K range's partial down projection, rows ra and rb
+    float *pa = part + (static_cast<uint64_t>(blockIdx.y) * rows_pad + ra) * R;
+    float *pb = pa + 8 * R;
 #pragma unroll
     for (int n = 0; n < R / 8; ++n) {
-        red[warp][gq][n * 8 + 2 * c] = acc[n][0];
-        red[warp][gq][n * 8 + 2 * c + 1] = acc[n][1];
-        red[warp][gq + 8][n * 8 + 2 * c] = acc[n][2];
-        red[warp][gq + 8][n * 8 + 2 * c + 1] = acc[n][3];
+        *reinterpret_cast<float2 *>(pa + n * 8 + 2 * c) = make_float2(acc[n][0], acc[n][1]);
+        *reinterpret_cast<float2 *>(pb + n * 8 + 2 * c) = make_float2(acc[n][2], acc[n][3]);
     }
-    __syncthreads();
-    const float factor = __fdiv_rn(lora_scale, __fmul_rn(g, *g_w));
-    for (int i = threadIdx.x; i < 16 * R; i += blockDim.x) {
-        const int rr = i / R, col = i % R;
-        float sum = red[0][rr][col];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) sum = __fadd_rn(sum, red[w][rr][col]);
-        if (row0 + rr < rows) {
-            const __nv_bfloat16 v = __float2bfloat16_rn(__fmul_rn(sum, factor));
-            Lp[static_cast<uint64_t>(row0 + rr) * R + col] = *reinterpret_cast<const uint16_t *>(&v);
-        }
+}
+
+// L'[m, j] = bf16( lora_scale / (g_x g_w) * sum over K ranges, in order ).
+template <int R>
+__global__ void __launch_bounds__(256)
+    lora_finalize_kernel(const float *__restrict__ part, uint32_t rows, uint32_t rows_pad,
+                         uint32_t ranges, const float *__restrict__ g_x,
+                         const float *__restrict__ g_w, float lora_scale,
+                         uint16_t *__restrict__ Lp) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const float factor = __fdiv_rn(lora_scale, __fmul_rn(*g_x, *g_w));
+    const uint64_t total = static_cast<uint64_t>(rows) * R;
+    for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<uint64_t>(gridDim.x) * blockDim.x) {
+        float sum = part[i];
+        for (uint32_t sidx = 1; sidx < ranges; ++sidx)
+            sum = __fadd_rn(sum, part[static_cast<uint64_t>(sidx) * rows_pad * R + i]);
+        const __nv_bfloat16 v = __float2bfloat16_rn(__fmul_rn(sum, factor));
+        Lp[i] = *reinterpret_cast<const uint16_t *>(&v);
     }
+}
+
+struct Split {
+    uint32_t ranges, chunks_per_range;
+};
+
+// K ranges per 64-row tile: about four CTAs per SM in all, at most
+// kMaxSplit, every range non-empty.
+Split lora_split(int64_t rows_pad, int64_t K) {
+    const uint32_t kb4 = static_cast<uint32_t>(K / 64);
+    const uint32_t tiles = static_cast<uint32_t>(rows_pad / kRows);
+    uint32_t want = (4u * static_cast<uint32_t>(launch_cfg().num_sms) + tiles - 1) / tiles;
+    want = want < 1 ? 1 : (want > kMaxSplit ? kMaxSplit : want);
+    if (want > kb4) want = kb4;
+    const uint32_t cpr = (kb4 + want - 1) / want;
+    return {(kb4 + cpr - 1) / cpr, cpr};
 }
 
 template <int R>
 cudaError_t launch_r(const uint16_t *X, int64_t rows, int64_t K, int64_t ldx, const float *g_x,
                      const float *g_w, float lora_scale, const uint16_t *A, uint8_t *q, uint8_t *sf,
-                     uint16_t *Lp, cudaStream_t st) {
+                     float *part, uint16_t *Lp, cudaStream_t st) {
+    using C = LoraCfg<R>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(quantize_lora_kernel<R>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
     const uint32_t rows_pad = static_cast<uint32_t>((rows + 127) / 128 * 128);
+    const Split sp = lora_split(rows_pad, K);
     cudaLaunchAttribute attr = pdl_attribute();
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(32 * kWarps, 1, 1);
-    cfg.gridDim = dim3(rows_pad / 16, 1, 1);
+    cfg.gridDim = dim3(rows_pad / kRows, sp.ranges, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, quantize_lora_kernel<R>, X, static_cast<uint32_t>(rows),
-                              static_cast<uint32_t>(K), static_cast<uint64_t>(ldx), g_x, g_w,
-                              lora_scale, A, q, sf, Lp);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_lora_kernel<R>, X,
+                                       static_cast<uint32_t>(rows), static_cast<uint32_t>(K),
+                                       static_cast<uint64_t>(ldx), g_x, A, sp.chunks_per_range,
+                                       rows_pad, q, sf, part);
+    if (e != cudaSuccess) return e;
+    const uint64_t total = static_cast<uint64_t>(rows) * R;
+    uint64_t blocks = (total + 255) / 256;
+    const uint64_t cap = static_cast<uint64_t>(launch_cfg().num_sms) * 4;
+    if (blocks > cap) blocks = cap;
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, lora_finalize_kernel<R>, part, static_cast<uint32_t>(rows),
+                              rows_pad, sp.ranges, g_x, g_w, lora_scale, Lp);
 }
 
 }  // namespace
@@ -180,15 +271,20 @@ cudaError_t launch_r(const uint16_t *X, int64_t rows, int64_t K, int64_t ldx, co
 cudaError_t launch_quantize_lora(const uint16_t *X, int64_t rows, int64_t K, int64_t ldx,
                                  const float *g_x, const float *g_w, float lora_scale,
                                  const uint16_t *A, int64_t r, uint8_t *q, uint8_t *sf,
-                                 uint16_t *Lp, cudaStream_t st) {
+                                 float *part, uint16_t *Lp, cudaStream_t st) {
     if (rows == 0) return cudaSuccess;
     switch (r) {
-        case 16: return launch_r<16>(X, rows, K, ldx, g_x, g_w, lora_scale, A, q, sf, Lp, st);
-        case 32: return launch_r<32>(X, rows, K, ldx, g_x, g_w, lora_scale, A, q, sf, Lp, st);
-        case 48: return launch_r<48>(X, rows, K, ldx, g_x, g_w, lora_scale, A, q, sf, Lp, st);
-        case 64: return launch_r<64>(X, rows, K, ldx, g_x, g_w, lora_scale, A, q, sf, Lp, st);
+        case 16: return launch_r<16>(X, rows, K, ldx, g_x, g_w, lora_scale, A, q, sf, part, Lp, st);
+        case 32: return launch_r<32>(X, rows, K, ldx, g_x, g_w, lora_scale, A, q, sf, part, Lp, st);
+        case 48: return launch_r<48>(X, rows, K, ldx, g_x, g_w, lora_scale, A, q, sf, part, Lp, st);
+        case 64: return launch_r<64>(X, rows, K, ldx, g_x, g_w, lora_scale, A, q, sf, part, Lp, st);
         default: return cudaErrorInvalidValue;
     }
+}
+
+size_t lora_partial_bytes(int64_t rows, int64_t r) {
+    return static_cast<size_t>(kMaxSplit) * static_cast<size_t>((rows + 127) / 128 * 128) *
+           static_cast<size_t>(r) * sizeof(float);
 }
 
 }  // namespace nvfp4
