@@ -16,10 +16,16 @@ namespace nvfp4 {
 // wait runs out. Kernels receive its address as a parameter.
 __device__ unsigned int g_device_error = 0;
 
-unsigned int *device_error_word() {
-    static unsigned int *addr[64] = {};
+int device_slot() {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return kMaxDevices;
+    return dev;
+}
+
+unsigned int *device_error_word() {
+    static unsigned int *addr[kMaxDevices] = {};
+    const int dev = device_slot();
+    if (dev == kMaxDevices) return nullptr;
     if (addr[dev] == nullptr) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
@@ -29,17 +35,18 @@ unsigned int *device_error_word() {
 }
 
 const LaunchCfg &launch_cfg() {
-    static LaunchCfg cfg;
-    static bool init = false;
-    if (!init) {
-        int dev = 0, sms = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess &&
+    static LaunchCfg cfg[kMaxDevices + 1];
+    static bool init[kMaxDevices + 1] = {};
+    const int dev = device_slot();
+    if (!init[dev]) {
+        int sms = 0;
+        if (dev < kMaxDevices &&
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
             sms > 0)
-            cfg.num_sms = sms;
-        init = true;
+            cfg[dev].num_sms = sms;
+        init[dev] = true;
     }
-    return cfg;
+    return cfg[dev];
 }
 
 DebugState &debug_state() {

@@ -399,8 +399,9 @@ bool make_operand_map(CUtensorMap *map, const uint8_t *ptr, int64_t rows, int64_
 
 template <int CM>
 cudaError_t launch_cm(const CUtensorMap &tmA, const CUtensorMap &tmB, Params p, cudaStream_t st) {
-    static int max_clusters = -1;
-    if (max_clusters < 0) {
+    static int max_clusters_of[kMaxDevices + 1] = {};  // 0: not yet queried
+    int &max_clusters = max_clusters_of[device_slot()];
+    if (max_clusters <= 0) {
         cudaError_t e = cudaFuncSetAttribute(gemm_kernel<CM>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
         if (e != cudaSuccess) return e;

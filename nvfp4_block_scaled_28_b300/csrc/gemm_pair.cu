@@ -547,8 +547,9 @@ int gemm_use_pair() {
 
 cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
-    static int max_clusters = -1;
-    if (max_clusters < 0) {
+    static int max_clusters_of[kMaxDevices + 1] = {};  // 0: not yet queried
+    int &max_clusters = max_clusters_of[device_slot()];
+    if (max_clusters <= 0) {
         cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
         if (e != cudaSuccess) return e;

@@ -441,7 +441,8 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
 template <int NX, int XR, bool FUSED, int KC>
 cudaError_t launch_sk(const SkinnyArgs &a, cudaStream_t st) {
     using C = SkCfg<NX, XR, FUSED, KC>;
-    static bool attr = false;
+    static bool attr_of[kMaxDevices + 1] = {};
+    bool &attr = attr_of[device_slot()];
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(skinny_kernel<NX, XR, FUSED, KC>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);

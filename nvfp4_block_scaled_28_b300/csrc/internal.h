@@ -29,9 +29,16 @@ struct FastDiv {
     }
 };
 
+// Slot of the current device for per-device one-time set-up (kernel
+// attributes, occupancy queries, device symbols): 0 .. kMaxDevices - 1, or
+// kMaxDevices when the device cannot be told.
+constexpr int kMaxDevices = 64;
+int device_slot();
+
 struct LaunchCfg {
     int num_sms = 148;
 };
+// Launch configuration of the current device.
 const LaunchCfg &launch_cfg();
 
 // global scale (g_out doubles as the reduction cell)

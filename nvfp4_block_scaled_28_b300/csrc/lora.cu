@@ -233,7 +233,8 @@ cudaError_t launch_r(const uint16_t *X, int64_t rows, int64_t K, int64_t ldx, co
                      const float *g_w, float lora_scale, const uint16_t *A, uint8_t *q, uint8_t *sf,
                      float *part, uint16_t *Lp, cudaStream_t st) {
     using C = LoraCfg<R>;
-    static bool attr_set = false;
+    static bool attr_set_of[kMaxDevices + 1] = {};
+    bool &attr_set = attr_set_of[device_slot()];
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(quantize_lora_kernel<R>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);

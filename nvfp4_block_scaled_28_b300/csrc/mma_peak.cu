@@ -242,7 +242,8 @@ __global__ void __launch_bounds__(kPeakThreads, 1)
 }
 
 cudaError_t launch_pair(int ctas, int iters, unsigned long long *cycles, cudaStream_t st) {
-    static bool attr = false;
+    static bool attr_of[kMaxDevices + 1] = {};
+    bool &attr = attr_of[device_slot()];
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(mma_peak_pair_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
@@ -269,7 +270,8 @@ cudaError_t launch_pair(int ctas, int iters, unsigned long long *cycles, cudaStr
 
 template <int V>
 cudaError_t launch_v(int ctas, int iters, unsigned long long *cycles, cudaStream_t st) {
-    static bool attr = false;
+    static bool attr_of[kMaxDevices + 1] = {};
+    bool &attr = attr_of[device_slot()];
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(mma_peak_kernel<V>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);

@@ -411,7 +411,8 @@ cudaError_t launch_quantize_small(const uint16_t *X, int64_t rows, int64_t cols,
 cudaError_t launch_quantize_fused(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
                                   uint32_t *partials, unsigned int *counter, float *g_out,
                                   uint8_t *q, uint8_t *sf, cudaStream_t st) {
-    static int per_sm = 0;
+    static int per_sm_of[kMaxDevices + 1] = {};
+    int &per_sm = per_sm_of[device_slot()];
     if (per_sm == 0) {
         int n = 0;
         cudaError_t e =
