@@ -65,6 +65,8 @@ constexpr int SF_TILE = 512;
 constexpr int SF_ROW = 256;                // scale arrays as rows of 256 bytes
 constexpr int CTA_STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
 constexpr uint32_t STAGE_TX = 2 * CTA_STAGE_BYTES;  // both CTAs, counted at rank 0
+// a stage of a column-half unit (256 x 128): each CTA loads 64 B rows
+constexpr uint32_t STAGE_TX_HALF = 2 * (CTA_STAGE_BYTES - B_BYTES / 2);
 // LoRA stage (after a tile's FP4 stages): L' (128 rows x 64 bfloat16) in the
 // A slot, the up projection (128 rows x 64 bfloat16) in the B slot, no scales
 constexpr uint32_t LORA_TX = 2 * (A_BYTES + B_BYTES);
@@ -116,6 +118,12 @@ struct Params {
     uint8_t *Ys;
     WeightGroups groups;  // grouped projection: g_b holds one scale per group
     int lora_r;           // > 0: one LoRA stage of lora_r / 16 bfloat16 K-steps per tile
+    // Work units: [0, num_full) are whole 256 x 256 tiles; the remaining
+    // tiles (the partial last wave) run as two 256 x 128 column halves each
+    // (N = 128 MMAs on otherwise idle pairs; the same K order, so the same
+    // bits per element).
+    int num_full;
+    int num_units;
     int inject;          // 1: the producers issue nothing (bounded-wait test)
     uint64_t timeout_ns;
     unsigned int *err;   // device error word
@@ -140,6 +148,16 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int &mt
     const int local = t - group * per_group;
     mt = first_m + local % gsz;
     nt = local / gsz;
+}
+
+// Work unit u: a whole tile (half -1) or one column half (0 / 1) of a tile.
+struct Unit {
+    int tile, half;
+};
+__device__ __forceinline__ Unit unit_of(int u, const Params &p) {
+    if (u < p.num_full) return {u, -1};
+    const int v = u - p.num_full;
+    return {p.num_full + (v >> 1), v & 1};
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -185,7 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tmY,
                      const __grid_constant__ CUtensorMap tmYq,
                      const __grid_constant__ CUtensorMap tmL,
-                     const __grid_constant__ CUtensorMap tmLB, const Params p) {
+                     const __grid_constant__ CUtensorMap tmLB,
+                     const __grid_constant__ CUtensorMap tmB64, const Params p) {
     // tmSA: A scales as rows of 256 B (8 rows per stage); tmSB: B scales as
     // {256 B, rows of a 128-row group, group} (8 rows x 2 groups per stage)
     extern __shared__ uint8_t smem_raw[];
@@ -199,8 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = rank == 0;
     const int pair = blockIdx.x >> 1;
     const int num_pairs = gridDim.x >> 1;
-    const int my_tiles =
-        pair < p.num_tiles ? (p.num_tiles - pair + num_pairs - 1) / num_pairs : 0;
+    const int my_units =
+        pair < p.num_units ? (p.num_units - pair + num_pairs - 1) / num_pairs : 0;
     const int num_k = p.K / BK;
     const int kb4 = p.K / 64;  // 512-byte scale tiles per 128-row group
 
@@ -216,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (p.num_units > p.num_full) tma_prefetch_desc(&tmB64);
         tma_prefetch_desc(&tmSA);
         tma_prefetch_desc(&tmSB);
         if (p.y_tma) tma_prefetch_desc(&tmY);
@@ -244,11 +264,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t full0 = mapa_shared(smem_addr(&sh.full[0]), 0);
         int g = 0;
         bool ok = !p.inject;
-        for (int t = 0; ok && t < my_tiles; ++t) {
+        for (int t = 0; ok && t < my_units; ++t) {
+            const Unit un = unit_of(pair + t * num_pairs, p);
+            const bool hu = un.half >= 0;
             int mt, nt;
-            tile_coords(pair + t * num_pairs, p.num_m_tiles, p.num_n_tiles, mt, nt);
+            tile_coords(un.tile, p.num_m_tiles, p.num_n_tiles, mt, nt);
             const int arow = mt * PM + static_cast<int>(rank) * BM;
-            const int brow = nt * BN + static_cast<int>(rank) * BNH;
+            // B rows of this CTA: 128 of the tile's 256, or 64 of a half's 128
+            const int brow = hu ? nt * BN + un.half * BNH + static_cast<int>(rank) * (BNH / 2)
+                                : nt * BN + static_cast<int>(rank) * BNH;
+            const int sfb_group = nt * 2 + (hu ? un.half : 0);
             // scale rows of 256 B: group grp, stage kt starts at row
             // (grp * kb4 + 4 kt) * 2; groups past the array read as 0
             const int sfa_row = (mt * 2 + static_cast<int>(rank)) * kb4 * 2;
@@ -261,16 +286,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     const uint32_t bar = full0 + static_cast<uint32_t>(s) * 8u;
                     if (!scales) {
-                        if (leader) mbar_arrive_expect_tx(&sh.full[s], STAGE_TX);
+                        if (leader)
+                            mbar_arrive_expect_tx(&sh.full[s], hu ? STAGE_TX_HALF : STAGE_TX);
                         tma_load_2d_pair(smem + SMEM_A + s * A_BYTES, &tmA, bar, kt * (BK / 2),
                                          arow, pol);
-                        tma_load_2d_pair(smem + SMEM_B + s * B_BYTES, &tmB, bar, kt * (BK / 2),
-                                         brow, pol);
+                        tma_load_2d_pair(smem + SMEM_B + s * B_BYTES, hu ? &tmB64 : &tmB, bar,
+                                         kt * (BK / 2), brow, pol);
                     } else {
                         tma_load_2d_pair(smem + SMEM_SFA + s * SFA_BYTES, &tmSA, bar, 0,
                                          sfa_row + kt * 8, pol);
                         tma_load_3d_pair(smem + SMEM_SFB + s * SFB_BYTES, &tmSB, bar, 0, kt * 8,
-                                         nt * 2, pol);
+                                         sfb_group, pol);
                     }
                 }
                 __syncwarp();
@@ -311,10 +337,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1 && leader) {
         // ------------------------------------------- MMA issuer (rank 0)
-        constexpr uint32_t idesc = idesc_mxf4nvf4(PM, BN);
+        constexpr uint32_t idesc_full = idesc_mxf4nvf4(PM, BN);
+        constexpr uint32_t idesc_half = idesc_mxf4nvf4(PM, BN / 2);
         int g = 0, it = 0;
         bool ok = true;
-        for (int t = 0; ok && t < my_tiles; ++t, ++it) {
+        for (int t = 0; ok && t < my_units; ++t, ++it) {
+            const uint32_t idesc = unit_of(pair + t * num_pairs, p).half >= 0 ? idesc_half
+                                                                              : idesc_full;
             if (!warp_wait(&sh.acc_empty, (it & 1) ^ 1, p, sh)) {
                 ok = false;
                 break;
@@ -380,11 +409,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float alpha0 = __fmul_rn(g_a, *p.g_b);
         const uint32_t acc_empty0 = mapa_shared(smem_addr(&sh.acc_empty), 0);
         int it = 0;
-        for (int t = 0; t < my_tiles; ++t, ++it) {
+        for (int t = 0; t < my_units; ++t, ++it) {
+            const Unit un = unit_of(pair + t * num_pairs, p);
             if (!warp_wait(&sh.acc_full, it & 1, p, sh)) break;
             tc_fence_after();
+            if (un.half >= 0 && half == 1) {
+                // a column-half unit fills accumulator columns 0..127 only
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(acc_empty0);
+                continue;
+            }
             int mt, nt;
-            tile_coords(pair + t * num_pairs, p.num_m_tiles, p.num_n_tiles, mt, nt);
+            tile_coords(un.tile, p.num_m_tiles, p.num_n_tiles, mt, nt);
             const uint32_t t_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + ACC_COL +
                                     static_cast<uint32_t>(half * 128);
             // all four 32-column loads in flight, one wait, release the
@@ -398,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive_cluster(acc_empty0);
             const int row0 = mt * PM + static_cast<int>(rank) * BM + quarter * 32;
             const int row = row0 + lane;
-            const int n0 = nt * BN + half * 128;
+            const int n0 = nt * BN + (un.half >= 0 ? un.half : half) * 128;
             // grouped projection: the tile's weight group sets the scale
             const float alpha =
                 kEpi ? __fmul_rn(g_a, p.g_b[weight_group_of(p.groups, n0)]) : alpha0;
@@ -576,11 +613,13 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     const int64_t kb4 = a.K / 64;
     const int64_t sf_rows_a = (a.M + 127) / 128 * kb4 * 2;  // 256-byte rows
     const int64_t groups_b = (a.N + 127) / 128;
-    CUtensorMap tmA, tmB, tmSA, tmSB;
+    CUtensorMap tmA, tmB, tmSA, tmSB, tmB64;
     if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Aq, a.K / 2, a.M, a.K / 2, 128u, BM,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Bq, a.K / 2, a.N, a.K / 2, 128u, BNH,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_2d(&tmB64, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Bq, a.K / 2, a.N, a.K / 2, 128u,
+                     BNH / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map_2d(&tmSA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.As, SF_ROW, sf_rows_a, SF_ROW,
                      SF_ROW, SFA_BYTES / SF_ROW, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map_3d(&tmSB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Bs, SF_ROW, kb4 * 2, groups_b, SF_ROW,
@@ -630,12 +669,22 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     p.Yq = a.Yq;
     p.Ys = a.Ys;
     p.groups = a.groups;
+    // the partial last wave's tiles as column halves, when they then fit in
+    // one wave (plain epilogue only)
+    const bool epi = !store_y || a.bias != nullptr || a.Yq != nullptr || a.groups.count > 1 ||
+                     a.lora_Lp != nullptr;
+    p.num_full = p.num_tiles;
+    {
+        const int R = p.num_tiles % max_clusters;
+        if (!epi && R > 0 && 2 * R <= max_clusters) p.num_full = p.num_tiles - R;
+    }
+    p.num_units = p.num_full + 2 * (p.num_tiles - p.num_full);
     p.lora_r = a.lora_Lp != nullptr ? static_cast<int>(a.lora_r) : 0;
     p.inject = debug_state().inject;
     p.timeout_ns = debug_state().timeout_ns;
     p.err = device_error_word();
     if (p.err == nullptr) return cudaErrorInvalidSymbol;
-    const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
+    const int clusters = p.num_units < max_clusters ? p.num_units : max_clusters;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -649,12 +698,10 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    const bool epi = !store_y || a.bias != nullptr || a.Yq != nullptr || a.groups.count > 1 ||
-                     a.lora_Lp != nullptr;
     cudaError_t e = epi ? cudaLaunchKernelEx(&cfg, gemm_pair_kernel<true>, tmA, tmB, tmSA, tmSB,
-                                             tmY, tmYq, tmL, tmLB, p)
+                                             tmY, tmYq, tmL, tmLB, tmB64, p)
                         : cudaLaunchKernelEx(&cfg, gemm_pair_kernel<false>, tmA, tmB, tmSA, tmSB,
-                                             tmY, tmYq, tmL, tmLB, p);
+                                             tmY, tmYq, tmL, tmLB, tmB64, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
