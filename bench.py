@@ -492,6 +492,7 @@ def extra_rows(torch, nv, D, workloads, peaks):
     ws3 = torch.empty(nv.linear_workspace_bytes(dit.M[0], sum(gn3), dit.K), dtype=torch.uint8,
                       device="cuda")
     Ysep = [torch.empty((dit.M[0], 3072), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    _ok(D.linear_grouped(Xd, Wq3, Ws3, g3, gn_ptr, 3, Y3, 0, ws3), "grouped")  # set-up
     ms_g = time_region(torch, lambda i: _ok(D.linear_grouped(Xd, Wq3, Ws3, g3, gn_ptr, 3, Y3, 0,
                                                              ws3), "grouped"), 20)
 
@@ -533,6 +534,7 @@ def extra_rows(torch, nv, D, workloads, peaks):
     ms_seq = time_region(torch, lambda i: (_ok(D.linear(Xp, Wq, Ws, gw, Y, None, 0, ws), "lin"),
                                            _ok(D.quantize(Y, gy, Yq, Ys, nv.SF_MMA_128x4), "q")),
                          20)
+    _ok(D.linear_bias_requant(Xp, Wq, Ws, gw, bias, Y, gy, Yq, Ys, ws), "epi")  # set-up
     ms_epi = time_region(torch, lambda i: _ok(D.linear_bias_requant(Xp, Wq, Ws, gw, bias, Y, gy,
                                                                     Yq, Ys, ws), "epi"), 20)
     ms_q = time_region(torch, lambda i: _ok(D.linear_bias_requant(Xp, Wq, Ws, gw, bias, None, gy,
@@ -549,8 +551,9 @@ def extra_rows(torch, nv, D, workloads, peaks):
     # the quantization pass, up projection as bfloat16 steps in the GEMM)
     la, lb = workloads.make_lora(32, K, n, seed=5, device="cuda")
     wsl = torch.empty(int(lib_lora_ws(nv, M, n, K, 32)), dtype=torch.uint8, device="cuda")
-    ms_lora = time_region(torch, lambda i: _ok(D.linear_lora(Xp, Wq, Ws, gw, la, lb, 32, 1.0, Y,
-                                                             wsl), "lora"), 20)
+    lora_fn = lambda i: _ok(D.linear_lora(Xp, Wq, Ws, gw, la, lb, 32, 1.0, Y, wsl), "lora")
+    lora_fn(0)  # first call: one-time kernel set-up outside the timed region
+    ms_lora = time_region(torch, lora_fn, 20)
     out["prefill_linear_4096x5120x5120_lora_r32"] = {
         "linear_ms": ms_lin, "lora_ms": ms_lora, "TFLOP/s_lora": fl / ms_lora / 1e9}
     del Xp, Wq, Ws, Y, Yq, Ys, ws, wsl, la, lb
