@@ -142,6 +142,25 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(value: float, device: str = "cuda") -> float:
+    """The largest of the ranks' values (the slowest rank's time sets the
+    job's time); the value itself on a single process."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(flops_per_step: float, steps: int, world: int, elapsed_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank runs `steps` steps of `flops_per_step`
+    (weak scaling, independent replicas) within the max-over-ranks time."""
+    return world * flops_per_step * steps / (elapsed_ms * 1e-3) / 1e12
+
+
 def physical_gpu_index(local_rank: int) -> int:
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     if vis:
@@ -323,12 +342,9 @@ def run_native(args):
         sets[i % n_sets]["Wq"], sets[i % n_sets]["Ws"], sets[i % n_sets]["gw"], M, Nn, K,
         sets[i % n_sets]["Y"]), "gemm"), gemm_iters)
 
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(elapsed_ms)
     ms_per_step = elapsed_ms / args.steps
-    value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+    value = job_rate(flops, args.steps, world, elapsed_ms)
 
     # ---- end to end through the C ABI with host buffers: every step copies
     # its X in from pinned host memory and its whole Y back out, inside the
