@@ -108,6 +108,8 @@ __global__ void __launch_bounds__(32 * kWarps)
     pdl_launch_dependents();
     pdl_wait();
     const float g = *g_x;
+    __shared__ float rtab[128];
+    fill_recip_table(rtab, g);  // ordered before its first use by the loop's barrier
 
     // one chunk of X (128 rows x 128 B) and of A (R rows x 128 B) into slot s
     auto load = [&](int s, uint32_t ch) {
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(32 * kWarps)
             const uint32_t r = id >> 2, blk = id & 3u;
             const uint4 a = lds128(xs + swz(r, 2u * blk)), b = lds128(xs + swz(r, 2u * blk + 1u));
             uint32_t lo, hi;
-            const uint32_t S = quantize16(a, b, g, lo, hi);
+            const uint32_t S = quantize16_tab(a, b, g, rtab, lo, hi);
             const uint32_t row = row0 + r;
             if (row < rows)
                 *reinterpret_cast<uint2 *>(q + static_cast<uint64_t>(row) * (K / 2) + ch * 32u +

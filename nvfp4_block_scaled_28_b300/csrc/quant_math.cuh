@@ -80,19 +80,50 @@ __device__ __forceinline__ uint32_t codes4(uint32_t w0, uint32_t w1, uint64_t rr
     return codes2(w0, rr) | (codes2(w1, rr) << 8);
 }
 
+// The per-block multiplier r = 1 / (e4m3(S) * g), 0 when the product is 0
+// (or not a number: byte 0x7F, which the saturating conversion never
+// produces).
+__device__ __forceinline__ float scale_recip(uint32_t S, float g) {
+    const float denom = __fmul_rn(e4m3_to_f32(S), g);
+    return denom > 0.0f ? __frcp_rn(denom) : 0.0f;
+}
+
+// scale_recip for all 128 scale bytes, by the threads of the block (the
+// caller synchronizes before use).
+__device__ __forceinline__ void fill_recip_table(float *rtab, float g) {
+    for (uint32_t i = threadIdx.x; i < 128u; i += blockDim.x) rtab[i] = scale_recip(i, g);
+}
+
+// The block's scale byte S = E4M3_rne_satfinite((amax / 6) / g).
+__device__ __forceinline__ uint32_t block_scale(uint4 a, uint4 b, float g) {
+    const float amax = __uint_as_float(amax_bits16(a, b) << 16);
+    return cvt_e4m3_satfinite(__fdiv_rn(__fdiv_rn(amax, 6.0f), g));
+}
+
+// The block's 16 codes under the multiplier r, into (lo, hi).
+__device__ __forceinline__ void block_codes16(uint4 a, uint4 b, float r, uint32_t &lo,
+                                              uint32_t &hi) {
+    const uint64_t rr = (static_cast<uint64_t>(__float_as_uint(r)) << 32) | __float_as_uint(r);
+    lo = codes4(a.x, a.y, rr) | (codes4(a.z, a.w, rr) << 16);
+    hi = codes4(b.x, b.y, rr) | (codes4(b.z, b.w, rr) << 16);
+}
+
 // Quantize one 16-element block held in (a, b). Returns the scale byte and
 // writes the 8 code bytes into (lo, hi).
 __device__ __forceinline__ uint32_t quantize16(uint4 a, uint4 b, float g, uint32_t &lo,
                                                uint32_t &hi) {
-    const float amax = __uint_as_float(amax_bits16(a, b) << 16);
-    const float v = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
-    const uint32_t S = cvt_e4m3_satfinite(v);
-    const float s = e4m3_to_f32(S);
-    const float denom = __fmul_rn(s, g);
-    const float r = denom > 0.0f ? __frcp_rn(denom) : 0.0f;
-    const uint64_t rr = (static_cast<uint64_t>(__float_as_uint(r)) << 32) | __float_as_uint(r);
-    lo = codes4(a.x, a.y, rr) | (codes4(a.z, a.w, rr) << 16);
-    hi = codes4(b.x, b.y, rr) | (codes4(b.z, b.w, rr) << 16);
+    const uint32_t S = block_scale(a, b, g);
+    block_codes16(a, b, scale_recip(S, g), lo, hi);
+    return S;
+}
+
+// quantize16 with r read from a table that fill_recip_table filled for the
+// same g (the table holds exactly what scale_recip computes).
+__device__ __forceinline__ uint32_t quantize16_tab(uint4 a, uint4 b, float g,
+                                                   const float *rtab, uint32_t &lo,
+                                                   uint32_t &hi) {
+    const uint32_t S = block_scale(a, b, g);
+    block_codes16(a, b, rtab[S], lo, hi);
     return S;
 }
 

@@ -36,8 +36,8 @@ template <int kLayout, int U, bool kGather>
 __device__ __forceinline__ void quantize_round(const uint16_t *__restrict__ X, uint32_t base,
                                                uint32_t stride, uint32_t total,
                                                uint32_t total_pad, uint32_t kbpr, uint64_t ldx,
-                                               FastDiv div_kbpr, float g, uint8_t *__restrict__ q,
-                                               uint8_t *__restrict__ sf) {
+                                               FastDiv div_kbpr, float g, const float *rtab,
+                                               uint8_t *__restrict__ q, uint8_t *__restrict__ sf) {
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t kb4 = kbpr >> 2;
     uint4 va[U], vb[U];
@@ -60,7 +60,7 @@ __device__ __forceinline__ void quantize_round(const uint16_t *__restrict__ X, u
         const uint32_t i = base + lane + u * stride;
         uint32_t S = 0, lo, hi;
         if (i < total) {
-            S = quantize16(va[u], vb[u], g, lo, hi);
+            S = quantize16_tab(va[u], vb[u], g, rtab, lo, hi);
             *reinterpret_cast<uint2 *>(q + static_cast<uint64_t>(i) * 8) = make_uint2(lo, hi);
         }
         const uint32_t end = kLayout == NVFP4_SF_ROW_MAJOR ? total : total_pad;
@@ -100,13 +100,16 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t *__re
                                                             uint8_t *__restrict__ q,
                                                             uint8_t *__restrict__ sf) {
     const float g = *g_ptr;
+    __shared__ float rtab[128];
+    fill_recip_table(rtab, g);
+    __syncthreads();
     const uint32_t total = rows * kbpr;
     const uint32_t stride = gridDim.x * blockDim.x;
     constexpr int U = 4;
     for (uint32_t base = blockIdx.x * blockDim.x + (threadIdx.x & ~31u); base < total;
          base += U * stride)
-        quantize_round<kLayout, U, true>(X, base, stride, total, total, kbpr, ldx, div_kbpr, g, q,
-                                         sf);
+        quantize_round<kLayout, U, true>(X, base, stride, total, total, kbpr, ldx, div_kbpr, g,
+                                         rtab, q, sf);
 }
 
 // amax(|X|) over 16-byte vectors as a bfloat16 magnitude bit pattern,
@@ -231,6 +234,9 @@ __global__ void __launch_bounds__(kThreads) quantize_fused_kernel(
     __syncthreads();
     const float g = g_sh;
     if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+    __shared__ float rtab[128];
+    fill_recip_table(rtab, g);
+    __syncthreads();
     // ---- quantize (padding rows of the last 128-row group get scale 0)
     const uint32_t total = rows * kbpr;
     const uint32_t total_pad = rows_pad * kbpr;
@@ -239,7 +245,7 @@ __global__ void __launch_bounds__(kThreads) quantize_fused_kernel(
     for (uint32_t base = blockIdx.x * blockDim.x + (threadIdx.x & ~31u); base < total_pad;
          base += U * stride)
         quantize_round<NVFP4_SF_MMA_128x4, U, false>(X, base, stride, total, total_pad, kbpr, ldx,
-                                                     div_kbpr, g, q, sf);
+                                                     div_kbpr, g, rtab, q, sf);
 }
 
 // Dynamic quantization of a small activation (decode rows) in one plain
@@ -296,6 +302,9 @@ __global__ void __launch_bounds__(kThreads) quantize_small_kernel(
     }
     const float g = g_sh;
     if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+    __shared__ float rtab[128];
+    fill_recip_table(rtab, g);
+    __syncthreads();
     const uint32_t total = rows * kbpr;
     const uint32_t total_pad = rows_pad * kbpr;
     const uint32_t stride = gridDim.x * blockDim.x;
@@ -303,7 +312,7 @@ __global__ void __launch_bounds__(kThreads) quantize_small_kernel(
     for (uint32_t base = blockIdx.x * blockDim.x + (threadIdx.x & ~31u); base < total_pad;
          base += U * stride)
         quantize_round<NVFP4_SF_MMA_128x4, U, false>(X, base, stride, total, total_pad, kbpr, ldx,
-                                                     div_kbpr, g, q, sf);
+                                                     div_kbpr, g, rtab, q, sf);
 }
 
 // g = amax / (6 * 448), or 1 for an all-zero tensor; in place over the cell.
