@@ -177,8 +177,10 @@ NVFP4_API nvfp4_status nvfp4_sf_to_mma_layout(const uint8_t *sf_row_major, int64
  * aligned, i.e. 16-byte aligned Y and ldy % 8 == 0, get 16-byte stores).
  * K % 256 == 0; M, N >= 0 (0 is a no-op).
  * M <= 128 (decode) runs a weight-streaming kernel that computes Y^T = W X^T
- * with the weights as the 128-row MMA operand; larger M runs the 128 x 256
- * tile kernel.
+ * with the weights as the 128-row MMA operand; larger M runs the CTA-pair
+ * kernel on 256 x 256 tiles (its partial last wave as 256 x 128 column
+ * halves; the same bits either way), or with NVFP4_GEMM_PAIR=0 in the
+ * environment the single-CTA kernel on 128 x 256 tiles.
  * workspace / workspace_bytes: scratch; query nvfp4_gemm_workspace_bytes()
  * (0 for every shape in this version). May be NULL when that returns 0.
  * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_SHAPE,
