@@ -208,3 +208,10 @@ def test_linear_lora_argument_checks(lib):
     assert call(M=0) == N.OK
     need = lib.nvfp4_linear_lora_workspace_bytes(256, 256, 512, 32)
     assert need >= lib.nvfp4_linear_workspace_bytes(256, 256, 512, 0) + 256 * 32 * 2
+
+
+def test_library_is_built_from_the_current_sources():
+    """A library older than any of its sources would test stale code: the
+    artifact's own time stamp is compared with every source (no stamp files)."""
+    from nvfp4_block_scaled_28_b300 import build
+    assert build.up_to_date(), "the library is older than its sources: rebuild it"
