@@ -23,8 +23,8 @@
  *    error; "four-over-six" lets each block map its maximum to 4 or to 6,
  *    whichever errs less (quantize_block_rule states the candidates and the
  *    tie rule taken where the page gives none).
- *  - Where the pages are silent, the readings of this build are used (each is
- *    also listed in the design doc): a per-tensor FP32 global scale g in the decode
+ *  - Where the pages are silent, these readings are taken: a per-tensor
+ *    FP32 global scale g in the decode
  *    direction (x_hat = e2m1 * e4m3 * g) with g = amax_tensor / (6 * 448);
  *    block scale S = RNE_E4M3_satfinite((amax_block / 6) / g); codes by RNE
  *    onto the E2M1 grid with saturation at 6, ties to the even code; even-k
