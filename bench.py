@@ -61,7 +61,7 @@ def gemm_traffic_per_launch():
     return None
 
 
-# Dense FP4 rate measured by the library's tcgen05 probe (profiles/mma_peak_probe.md)
+# Dense FP4 rate measured by the library's tcgen05 probe (bench.py --op mma_peak)
 FP4_PROBE_PEAK_TFLOPS = 9230.0
 # NVIDIA's nominal dense NVFP4 rate of one B300 (context only)
 FP4_NOMINAL_DENSE_TFLOPS = 13500.0
