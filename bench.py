@@ -308,9 +308,11 @@ def run_native(args):
         s = sets[i % n_sets]
         _ok(D.linear(s["X"], s["Wq"], s["Ws"], s["gw"], s["Y"], None, mode, s["ws"]), "linear")
 
-    # amax partials, quantize (reducing g_x), GEMM: three kernels per step,
-    # chained by programmatic dependent launch inside nvfp4_linear
-    kernels_per_step = 3
+    # two kernels of this library per step: quantize_fused_kernel (amax
+    # partials, grid barrier, g_x, quantization; its barrier counter is
+    # zeroed by a 4-byte cudaMemsetAsync before it) and gemm_pair_kernel,
+    # the latter a programmatic dependent of the former
+    kernels_per_step = 2
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
