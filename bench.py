@@ -1,19 +1,21 @@
 #!/usr/bin/env python
 """Benchmark of the NVFP4 linear layer on B300.
 
-One step = one pass of the hot path over one batch of the LLM prefill
-projection (M=4096 tokens, K=5120 -> N=5120, X ~ N(0,1) with 0.1 % outlier
-channels x50, W ~ N(0, 0.02) quantized offline): per-tensor amax of X ->
-global scale, dynamic NVFP4 quantization of X, tcgen05 block-scaled FP4 GEMM
-against the NVFP4 weights, bfloat16 out.
+One step = one pass of the hot path over one batch of the largest workload,
+the square 16384 x 16384 x 16384 NVFP4 linear (X ~ N(0,1) with 0.1 %
+outlier channels x50, W ~ N(0, 0.02) quantized offline): per-tensor amax of
+X -> global scale, dynamic NVFP4 quantization of X, tcgen05 block-scaled
+FP4 GEMM against the NVFP4 weights, bfloat16 out.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 
 Prints one JSON line (rank 0). ``value`` is the whole-job TFLOP/s
 (2 M N K per step, summed over ranks, divided by the max-over-ranks time).
-Inputs rotate through enough independent sets that each step reads operands
-that are not L2-resident. The ``reference`` arm times the CPU oracle (test
-infrastructure) on a bounded row sample of the same workload.
+The step's operands are ten times the size of L2. ``roofline`` times the
+GEMM kernel alone; ``rows`` hold the other workloads (standalone quantize,
+prefill, DiT, decode, the extension rows). The ``reference`` arm times the
+CPU oracle (test infrastructure) on a bounded row sample of the same
+workload.
 """
 from __future__ import annotations
 
@@ -48,7 +50,7 @@ def gemm_traffic_per_launch():
     ncu capture, valid only while the kernel source is the one captured."""
     import hashlib
     try:
-        with open(os.path.join(ROOT, "profiles", "gemm_prefill_traffic.json")) as f:
+        with open(os.path.join(ROOT, "profiles", "gemm_square_traffic.json")) as f:
             rec = json.load(f)
         h = hashlib.sha256()
         for name in GEMM_SOURCES:
@@ -277,42 +279,34 @@ def run_native(args):
     D = Direct(lib, stream.cuda_stream)
     peaks = measured_peaks()
 
-    wl = workloads.WORKLOADS["prefill"]
+    # The step: nvfp4_linear on the largest workload, 16384 x 16384 x 16384
+    # with the activation's global scale computed from X (amax, quantize,
+    # GEMM). Its operands (537 MB of X, 151 MB of weights, 537 MB of Y) are
+    # ten times L2, so consecutive steps cannot find them there.
+    wl = workloads.WORKLOADS["square"]
     M, K, Nn = wl.M[0], wl.K, wl.N[0]
     flops = 2.0 * M * Nn * K
     mode = nv.LINEAR_FUSED if args.mode == "fused" else nv.LINEAR_UNFUSED
-
-    # ---- input sets, rotated so that no step finds its operands in L2
-    set_bytes = (M * K * 2 + Nn * K // 2 + Nn * K // 16 + M * Nn * 2 + M * K // 2 + M * K // 16)
-    n_sets = max(2, math.ceil(3 * L2_BYTES / set_bytes))
-    sets = []
-    for r in range(n_sets):
-        X = workloads.make_x(wl.x_kind, M, K, workloads.x_seed(wl) + 1000 * r + 17 * rank,
-                             device="cuda")
-        W = workloads.make_w(Nn, K, workloads.w_seed(wl) + 1000 * r, device="cuda")
-        Wq, Ws, gw = nv.nvfp4_quantize_weight(W, nv.SF_MMA_128x4)
-        del W
-        gx = torch.empty(1, dtype=torch.float32, device="cuda")
-        Xq = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
-        Xs = torch.empty(nv.sf_shape(M, K, nv.SF_MMA_128x4), dtype=torch.uint8, device="cuda")
-        Y = torch.empty((M, Nn), dtype=torch.bfloat16, device="cuda")
-        ws = torch.empty(nv.linear_workspace_bytes(M, Nn, K, mode), dtype=torch.uint8,
-                         device="cuda")
-        sets.append(dict(X=X, Wq=Wq, Ws=Ws, gw=gw, gx=gx, Xq=Xq, Xs=Xs, Y=Y, ws=ws))
+    X = workloads.make_x(wl.x_kind, M, K, workloads.x_seed(wl) + 17 * rank, device="cuda")
+    W = workloads.make_w(Nn, K, workloads.w_seed(wl), device="cuda")
+    Wq, Ws, gw = nv.nvfp4_quantize_weight(W, nv.SF_MMA_128x4)
+    del W
+    Y = torch.empty((M, Nn), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(nv.linear_workspace_bytes(M, Nn, K, mode), dtype=torch.uint8, device="cuda")
+    step_bytes = M * K * 2 + Nn * K // 2 + Nn * K // 16 + M * Nn * 2
+    torch.cuda.empty_cache()
     # one checked call through the binding before the raw loop
-    nv.nvfp4_linear(sets[0]["X"], sets[0]["Wq"], sets[0]["Ws"], sets[0]["gw"], Y=sets[0]["Y"],
-                    mode=mode, workspace=sets[0]["ws"])
+    nv.nvfp4_linear(X, Wq, Ws, gw, Y=Y, mode=mode, workspace=ws)
     torch.cuda.synchronize()
 
     def step(i):
-        s = sets[i % n_sets]
-        _ok(D.linear(s["X"], s["Wq"], s["Ws"], s["gw"], s["Y"], None, mode, s["ws"]), "linear")
+        _ok(D.linear(X, Wq, Ws, gw, Y, None, mode, ws), "linear")
 
-    # two kernels of this library per step: quantize_fused_kernel (amax
-    # partials, grid barrier, g_x, quantization; its barrier counter is
-    # zeroed by a 4-byte cudaMemsetAsync before it) and gemm_pair_kernel,
-    # the latter a programmatic dependent of the former
+    # per step: a 4-byte cudaMemsetAsync of the quantizer's barrier counter,
+    # quantize_fused_kernel (amax partials, grid barrier, g_x, quantization)
+    # and gemm_pair_kernel (a programmatic dependent of the quantizer)
     kernels_per_step = 2
+    ops_per_step = 3
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
@@ -332,38 +326,42 @@ def run_native(args):
         dist.barrier()
     elapsed_ms = t0.elapsed_time(t1)
     assert nv.nvfp4_device_error() == 0, "a kernel recorded a bounded-wait timeout"
-
-    # The GEMM kernel's own launch duration: CUDA events around GEMM-only
-    # launches on the same rotating sets (operands quantized as in the step).
-    for s_ in sets:
-        nv.nvfp4_global_scale(s_["X"], s_["gx"])
-        nv.nvfp4_quantize(s_["X"], s_["gx"], nv.SF_MMA_128x4, q=s_["Xq"], sf=s_["Xs"])
-    gemm_iters = max(20, min(args.steps, 400))
-    gemm_ms = time_region(torch, lambda i: _ok(D.gemm(
-        sets[i % n_sets]["Xq"], sets[i % n_sets]["Xs"], sets[i % n_sets]["gx"],
-        sets[i % n_sets]["Wq"], sets[i % n_sets]["Ws"], sets[i % n_sets]["gw"], M, Nn, K,
-        sets[i % n_sets]["Y"]), "gemm"), gemm_iters)
-
     elapsed_ms = max_over_ranks(elapsed_ms)
     ms_per_step = elapsed_ms / args.steps
     value = job_rate(flops, args.steps, world, elapsed_ms)
+
+    # ---- the dominant kernel (the GEMM) alone: GEMM-only launches on the
+    # step's operands (X quantized as in the step) for at least a second,
+    # CUDA events on the launching stream, clocks sampled meanwhile
+    gx = nv.nvfp4_global_scale(X)
+    Xq = ws[8448:8448 + M * K // 2].view(M, K // 2)
+    sf_off = 8448 + (M * K // 2 + 255) // 256 * 256
+    Xs = ws[sf_off:sf_off + nv.sf_bytes(M, K, nv.SF_MMA_128x4)]
+    nv.nvfp4_quantize(X, gx, nv.SF_MMA_128x4, q=Xq, sf=Xs.view(nv.sf_shape(M, K, nv.SF_MMA_128x4)))
+    gemm_fn = lambda i: _ok(D.gemm(Xq, Xs, gx, Wq, Ws, gw, M, Nn, K, Y), "gemm")
+    probe_ms = time_region(torch, gemm_fn, 3)
+    gemm_iters = max(20, int(math.ceil(args.gemm_seconds * 1e3 / max(probe_ms, 1e-3))))
+    gsampler = ClockSampler(physical_gpu_index(local))
+    gsampler.start()
+    gemm_ms = time_region(torch, gemm_fn, gemm_iters)
+    gclocks = gsampler.stop()
+    quant_ms = ms_per_step - gemm_ms  # the rest of the step: memset + dynamic quantizer
 
     # ---- end to end through the C ABI with host buffers: every step copies
     # its X in from pinned host memory and its whole Y back out, inside the
     # timed region. The copies run on their own streams, double-buffered, so
     # step i's copy-in, step i-1's compute and step i-2's copy-out overlap
     # (the serving pattern); events order each buffer's reuse.
-    s0 = sets[0]
-    Xh = s0["X"].cpu().pin_memory()
+    Xh = X.cpu().pin_memory()
     Yh = [torch.empty((M, Nn), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    Xd = [torch.empty_like(s0["X"]) for _ in range(2)]
-    Yd = [s0["Y"], torch.empty_like(s0["Y"])]
+    Xd = [X, torch.empty_like(X)]
+    Yd = [Y, torch.empty_like(Y)]
     s_cmp = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_cmp = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
-    e2e_iters = max(4, min(args.steps, 20))
+    e2e_iters = max(4, min(args.steps, args.e2e_steps))
 
     def e2e_step(i):
         b = i % 2
@@ -373,8 +371,7 @@ def run_native(args):
             ev_in[b].record(s_in)
         s_cmp.wait_event(ev_in[b])
         s_cmp.wait_event(ev_out[b])           # step i-2's Y has left Yd[b]
-        _ok(D.linear(Xd[b], s0["Wq"], s0["Ws"], s0["gw"], Yd[b], None, mode, s0["ws"]),
-            "linear")
+        _ok(D.linear(Xd[b], Wq, Ws, gw, Yd[b], None, mode, ws), "linear")
         ev_cmp[b].record(s_cmp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_cmp[b])
@@ -395,28 +392,44 @@ def run_native(args):
     t_b.record(s_cmp)
     torch.cuda.synchronize()
     e2e_ms = t_a.elapsed_time(t_b) / e2e_iters
+    e2e_ms = max_over_ranks(e2e_ms)
     e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
            "h2d_bytes_per_step": int(Xh.numel() * 2), "d2h_bytes_per_step": int(Yh[0].numel() * 2),
-           "ms_per_step": e2e_ms,
+           "ms_per_step": e2e_ms, "steps": e2e_iters,
            "pipeline": "copy-in, compute and copy-out on separate streams, double-buffered"}
+    del Xh, Yh, Xd, Yd
+    torch.cuda.empty_cache()
 
-    # ---- roofline of the dominant kernel (the GEMM)
-    peak_sust = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
+    # ---- roofline of the dominant kernel (the GEMM, timed alone: the burst
+    # peak is its denominator)
     peak_burst = peaks["bf16_tflops"] * FP4_OVER_BF16
+    peak_sust = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
     achieved = flops / (gemm_ms * 1e-3) / 1e12
+    mhz = gclocks.get("sm_mhz")
     roofline = {"bound": "tensor",
                 "kernel": "gemm_pair_kernel (tcgen05 cta_group::2 kind::mxf4nvf4)",
-                "achieved": achieved, "peak": peak_sust, "unit": "TFLOP/s",
-                "frac": achieved / peak_sust, "frac_of_burst_peak": achieved / peak_burst,
-                "peak_note": "%s bf16 %s x %.0f (fp4:bf16 nominal 13.5:2.25), sustained"
-                             % (peaks["source"], peaks["bf16_tflops_sustained"], FP4_OVER_BF16),
-                "timing": "CUDA events over %d GEMM-only launches on the step's rotating "
-                          "input sets, right after the timed steps" % gemm_iters,
+                "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
+                "frac": achieved / peak_burst,
+                "peak_note": "%s bf16 burst %s TFLOP/s x %.0f (fp4:bf16 nominal 13.5:2.25): the "
+                             "GEMM is timed alone" % (peaks["source"], peaks["bf16_tflops"],
+                                                      FP4_OVER_BF16),
+                "frac_of_sustained_peak": achieved / peak_sust,
                 "frac_of_probe_peak": achieved / FP4_PROBE_PEAK_TFLOPS,
+                "probe_peak_note": "kind::mxf4nvf4 K=64 MMAs back to back at 2032 MHz "
+                                   "(python bench.py --op mma_peak --variant 7)",
                 "frac_of_nominal_fp4": achieved / FP4_NOMINAL_DENSE_TFLOPS,
-                "gemm_ms": gemm_ms, "traffic": gemm_traffic_per_launch(),
+                "gemm_ms": gemm_ms, "gemm_launches_timed": gemm_iters,
+                "gemm_clocks": gclocks,
+                "gemm_ms_x_sm_ghz": gemm_ms * mhz / 1e3 if mhz else None,
+                "timing": "CUDA events over %d back-to-back GEMM-only launches (%.1f s) on the "
+                          "step's operands, after the timed steps" % (gemm_iters,
+                                                                     gemm_iters * gemm_ms / 1e3),
+                "rest_of_step_ms": quant_ms,
+                "traffic": gemm_traffic_per_launch(),
                 "traffic_unit": "bytes per launch (ncu dram read + write)"}
 
+    del X, Y, Wq, Ws, ws
+    torch.cuda.empty_cache()
     rows = {}
     if not args.no_extras and rank == 0:
         rows = extra_rows(torch, nv, D, workloads, peaks)
@@ -426,14 +439,19 @@ def run_native(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
         "data": "synthetic (seeded; X ~ N(0,1) with 0.1% outlier channels x50, W ~ N(0,0.02))",
-        "config": {"workload": "LLM prefill projection M=4096 K=5120 N=5120 (NVFP4 linear, "
-                               "dynamic activation global scale)",
+        "config": {"workload": "square NVFP4 linear M=N=K=16384 (dynamic activation global "
+                               "scale: amax, quantize, GEMM)",
                    "M": M, "N": Nn, "K": K, "mode": args.mode,
-                   "l2": "%d rotating input sets of %.0f MB (> 3x L2)" % (n_sets, set_bytes / 1e6),
+                   "l2": "inputs larger than L2: %.0f MB of operands and output per step vs "
+                         "126 MB of L2" % (step_bytes / 1e6),
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": kernels_per_step * args.steps,
+        "gpu_launches": ops_per_step * args.steps,
+        "gpu_ops_per_step": {"kernels": kernels_per_step, "memsets": ops_per_step -
+                             kernels_per_step,
+                             "note": "the 4-byte cudaMemsetAsync that zeroes the quantizer's "
+                                     "barrier counter is the third GPU operation of a step"},
         "clocks": clocks,
         "rows": rows,
     }
@@ -472,18 +490,39 @@ def extra_rows(torch, nv, D, workloads, peaks):
                                                                    rule=rule), 5)
         out["weight_quantize_5120x5120_%s" % name] = {"ms": ms}
     del Wp
-    # a4: square GEMM 16384^3
-    W = workloads.make_w(sq.N[0], sq.K, workloads.w_seed(sq), device="cuda")
-    Wq, Ws, gw = nv.nvfp4_quantize_weight(W, nv.SF_MMA_128x4)
-    del W
-    Xq, Xs = nv.nvfp4_quantize(X, g, nv.SF_MMA_128x4)
     del X, q, sf
-    Y = torch.empty((sq.M[0], sq.N[0]), dtype=torch.bfloat16, device="cuda")
-    ms = time_region(torch, lambda i: _ok(D.gemm(Xq, Xs, g, Wq, Ws, gw, sq.M[0], sq.N[0], sq.K, Y),
-                                          "gemm"), 5)
-    fl = 2.0 * sq.M[0] * sq.N[0] * sq.K
-    out["gemm_16384^3"] = {"ms": ms, "TFLOP/s": fl / ms / 1e9}
-    del Xq, Xs, Wq, Ws, Y
+    torch.cuda.empty_cache()
+    # a4 on the LLM prefill projection: the whole linear (dynamic global
+    # scale) and the GEMM alone, on 3 rotating input sets (> 2x L2 in all)
+    pf = workloads.WORKLOADS["prefill"]
+    M, n, K = pf.M[0], pf.N[0], pf.K
+    psets = []
+    for r in range(3):
+        Xp = workloads.make_x(pf.x_kind, M, K, workloads.x_seed(pf) + 1000 * r, device="cuda")
+        W = workloads.make_w(n, K, workloads.w_seed(pf) + 1000 * r, device="cuda")
+        Wq, Ws, gw = nv.nvfp4_quantize_weight(W, nv.SF_MMA_128x4)
+        del W
+        gxp = nv.nvfp4_global_scale(Xp)
+        Xq, Xs = nv.nvfp4_quantize(Xp, gxp, nv.SF_MMA_128x4)
+        psets.append(dict(X=Xp, Wq=Wq, Ws=Ws, gw=gw, gx=gxp, Xq=Xq, Xs=Xs,
+                          Y=torch.empty((M, n), dtype=torch.bfloat16, device="cuda"),
+                          ws=torch.empty(nv.linear_workspace_bytes(M, n, K), dtype=torch.uint8,
+                                         device="cuda")))
+    fl = 2.0 * M * n * K
+    lin = lambda i: _ok(D.linear(psets[i % 3]["X"], psets[i % 3]["Wq"], psets[i % 3]["Ws"],
+                                 psets[i % 3]["gw"], psets[i % 3]["Y"], None, 0,
+                                 psets[i % 3]["ws"]), "lin")
+    gem = lambda i: _ok(D.gemm(psets[i % 3]["Xq"], psets[i % 3]["Xs"], psets[i % 3]["gx"],
+                               psets[i % 3]["Wq"], psets[i % 3]["Ws"], psets[i % 3]["gw"], M, n,
+                               K, psets[i % 3]["Y"]), "gemm")
+    lin(0)
+    ms_l = time_region(torch, lin, 200)
+    ms_g = time_region(torch, gem, 200)
+    out["prefill_linear_4096x5120x5120"] = {
+        "ms": ms_l, "TFLOP/s": fl / ms_l / 1e9, "gemm_ms": ms_g, "gemm_TFLOP/s": fl / ms_g / 1e9,
+        "gemm_frac_of_burst_peak": fl / ms_g / 1e9 / (peaks["bf16_tflops"] * FP4_OVER_BF16),
+        "inputs": "3 rotating sets"}
+    del psets
     torch.cuda.empty_cache()
     # DiT block linears
     dit = workloads.WORKLOADS["dit"]
@@ -609,7 +648,13 @@ def extra_rows(torch, nv, D, workloads, peaks):
 
 # ------------------------------------------------------------ CPU oracle leg
 
-def _oracle_prefill_sample(rows_sample: int):
+_SQ_SAMPLE_NOTE = ("%d of 16384 rows per step of the square workload (global scale and quantize "
+                   "of the sampled activation rows, FP64 GEMM of those rows against all 16384 "
+                   "weight rows; the weight is quantized once beforehand, untimed, as it is "
+                   "offline on the GPU path)")
+
+
+def _oracle_square_sample(rows_sample: int):
     """Quantize W once (offline in the real path), then time the oracle's
     step on `rows_sample` rows of X: global scale, quantize, GEMM rows."""
     import numpy as np
@@ -618,12 +663,13 @@ def _oracle_prefill_sample(rows_sample: int):
     import oracle
     from nvfp4_block_scaled_28_b300 import workloads
 
-    wl = workloads.WORKLOADS["prefill"]
+    wl = workloads.WORKLOADS["square"]
     K, Nn = wl.K, wl.N[0]
     bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
     wb = bits(workloads.make_w(Nn, K, workloads.w_seed(wl)))
     gw = oracle.global_scale(wb)
     wq, ws = oracle.quantize(wb, gw)
+    del wb
     xb = bits(workloads.make_x(wl.x_kind, rows_sample, K, workloads.x_seed(wl)))
 
     def step():
@@ -637,14 +683,12 @@ def _oracle_prefill_sample(rows_sample: int):
 def cpu_baseline(rows_sample: int):
     import oracle
     oracle.build()
-    step, fl = _oracle_prefill_sample(rows_sample)
+    step, fl = _oracle_square_sample(rows_sample)
     t = time.perf_counter()
     step()
     dt = time.perf_counter() - t
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "seconds": dt,
-            "sample": "%d of 4096 rows of the prefill workload (global scale + quantize of the "
-                      "sample, FP64 GEMM against all 5120 weight rows)" % rows_sample}
+            "kind": "oracle", "seconds": dt, "sample": _SQ_SAMPLE_NOTE % rows_sample}
 
 
 def run_reference(args):
@@ -653,8 +697,10 @@ def run_reference(args):
         return
     import oracle
     oracle.build()
-    rows = max(1, min(256, 2048 // max(1, args.steps + args.warmup)))
-    step, fl = _oracle_prefill_sample(rows)
+    # about 0.02 s of oracle work per sampled row on 16 host cores: keep the
+    # whole run (steps + warm-up) within a couple of minutes
+    rows = max(1, min(256, 3072 // max(1, args.steps + args.warmup)))
+    step, fl = _oracle_square_sample(rows)
     for _ in range(args.warmup):
         step()
     t = time.perf_counter()
@@ -662,18 +708,16 @@ def run_reference(args):
         step()
     dt = time.perf_counter() - t
     value = fl * args.steps / dt / 1e12
-    sample = ("%d of 4096 rows per step of the prefill workload (global scale + quantize of the "
-              "sample, FP64 GEMM against all 5120 weight rows)" % rows)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
-        "config": {"workload": "LLM prefill projection M=4096 K=5120 N=5120 (NVFP4 linear, "
-                               "dynamic activation global scale)", "M": 4096, "N": 5120,
-                   "K": 5120},
+        "config": {"workload": "square NVFP4 linear M=N=K=16384 (dynamic activation global "
+                               "scale: amax, quantize, GEMM)", "M": 16384, "N": 16384,
+                   "K": 16384},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": _SQ_SAMPLE_NOTE % rows},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }))
@@ -698,7 +742,9 @@ def run_single_op(args):
         if v == 7:
             ctas &= ~1
         n_mma = 128 if v in (1, 2) else 256
-        fn = lambda i: _ok(lib.nvfp4_mma_peak_probe(ctas, iters, v, cyc.data_ptr(), D.stream),
+        from nvfp4_block_scaled_28_b300 import _native
+        probe = _native.load_probe()
+        fn = lambda i: _ok(probe.nvfp4_mma_peak_probe(ctas, iters, v, cyc.data_ptr(), D.stream),
                            "peak")
         for i in range(max(1, args.warmup)):
             fn(i)
@@ -775,13 +821,16 @@ def run_single_op(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=600)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--gemm-seconds", type=float, default=1.5,
+                    help="length of the GEMM-only roofline loop")
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--mode", choices=["unfused", "fused"], default="unfused")
     ap.add_argument("--no-extras", action="store_true", help="skip the per-row extra numbers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=256)
+    ap.add_argument("--cpu-rows", type=int, default=384)
     ap.add_argument("--op", choices=["gemm", "quantize", "linear", "linear_bias_requant",
                                      "linear_requant_only", "linear_lora", "mma_peak"],
                     default=None,

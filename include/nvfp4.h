@@ -179,8 +179,9 @@ NVFP4_API nvfp4_status nvfp4_sf_to_mma_layout(const uint8_t *sf_row_major, int64
  * M <= 128 (decode) runs a weight-streaming kernel that computes Y^T = W X^T
  * with the weights as the 128-row MMA operand; larger M runs the CTA-pair
  * kernel on 256 x 256 tiles (its partial last wave as 256 x 128 column
- * halves; the same bits either way), or with NVFP4_GEMM_PAIR=0 in the
- * environment the single-CTA kernel on 128 x 256 tiles.
+ * halves; the same bits either way), or, once
+ * nvfp4_debug_select_gemm_kernel(1) was called, the single-CTA kernel on
+ * 128 x 256 tiles.
  * workspace / workspace_bytes: scratch; query nvfp4_gemm_workspace_bytes()
  * (0 for every shape in this version). May be NULL when that returns 0.
  * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_SHAPE,
@@ -218,9 +219,13 @@ typedef enum nvfp4_linear_mode {
  * g_x: device pointer to the activation's global scale, or NULL to compute
  * it from X on the device first (one extra read of X).
  * mode: nvfp4_linear_mode.
- * workspace: nvfp4_linear_workspace_bytes(M, N, K, mode) bytes (holds the
- * quantized activation, its scales and, when g_x is NULL, g_x itself),
- * 256-byte aligned.
+ * workspace: nvfp4_linear_workspace_bytes(M, N, K, mode) bytes, 256-byte
+ * aligned. After the call it holds X's quantized form, which a caller may
+ * read (to reuse it, or to check it): the global scale used (fp32 at byte
+ * 0; written when g_x is NULL), X's codes (M x K/2 bytes at byte 8448) and
+ * their NVFP4_SF_MMA_128x4 scales (at byte 8448 + M*K/2 rounded up to a
+ * multiple of 256). The fused mode for M <= 4 leaves nothing there (its
+ * operand stays in shared memory).
  * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_SHAPE,
  * WORKSPACE_TOO_SMALL, CUDA.
  */
@@ -282,8 +287,11 @@ NVFP4_API nvfp4_status nvfp4_linear_grouped(const void *X, int64_t M, int64_t K,
  * exceed 16 MiB (about M * K / 2 * 1.125 bytes; 4096 x 5120 fits), else
  * NVFP4_ERR_WORKSPACE_TOO_SMALL and nothing is launched.
  * The first call on each device looks the array's device address up
- * (cudaGetSymbolAddress) while that device is current; make that first call
- * before any stream capture begins. Every call shares the one array and it
+ * (cudaGetSymbolAddress) while that device is current and keeps it for the
+ * life of the process; make that first call before any stream capture
+ * begins. A cudaDeviceReset (or anything else that destroys the device's
+ * primary context) invalidates the kept address: do not call this entry
+ * point on that device again in the same process. Every call shares the one array and it
  * keeps the previous call's contents: calls whose work overlaps on the GPU
  * (different streams, or different host threads without ordering) race on
  * it, so serialize them.
@@ -370,34 +378,6 @@ NVFP4_API size_t nvfp4_linear_lora_workspace_bytes(int64_t M, int64_t N, int64_t
 NVFP4_API nvfp4_status nvfp4_device_error(int clear);
 
 /*
- * Dense FP4 tensor-core peak probe (measurement, not part of the linear
- * layer): `ctas` CTAs each issue `iters` back-to-back tcgen05.mma
- * kind::mxf4nvf4 instructions on shared-memory-resident operands, from a
- * loop specialised per variant (so the issuing warp's own work does not
- * set the rate):
- *   0  128 x 256 x 64 into one TMEM accumulator
- *   1  128 x 128 x 64
- *   2  128 x 128 x 64 from two warps, one accumulator each (iters / 2 each)
- *   3  variant 0 with the GEMM's three shared->TMEM scale copies
- *      (tcgen05.cp 32x128b.warpx4) in front of every MMA, same thread
- *   4  variant 0 with those copies issued by a second warp concurrently
- *   5  variant 0 with a GEMM stage's bookkeeping after every 4 MMAs:
- *      tcgen05.commit, an mbarrier poll (lane 0 + shuffle), a fence
- *   6  kind::f16 BF16 128 x 256 x 16 (calibration against the BF16 rate)
- *   7  CTA pairs (clusters of 2, tcgen05 cta_group::2): rank 0 issues
- *      256 x 256 x 64 MMAs computed half on each SM (ctas rounded down
- *      to even, at least 2)
- * iters must be a multiple of 4 (of 8 for variant 2).
- * FLOPs = ctas * iters * 2 * 128 * N * K (N = 128 for variants 1 and 2,
- * else 256; K = 16 for variant 6, else 64; for variant 7 per CTA of the
- * even count); time it with events on
- * `stream`. CTA 0 writes its SM clock cycles to *cycles (device pointer).
- * Errors: INVALID_ARG, MISALIGNED, CUDA.
- */
-NVFP4_API nvfp4_status nvfp4_mma_peak_probe(int ctas, int iters, int variant,
-                                           unsigned long long *cycles, void *stream);
-
-/*
  * Testing hook for the bounded waits (no fault is involved): with
  * mode = 1 the next GEMM launches' TMA producer issues no loads, so the
  * consumers' waits run out after timeout_us microseconds and the kernel
@@ -405,6 +385,28 @@ NVFP4_API nvfp4_status nvfp4_mma_peak_probe(int ctas, int iters, int variant,
  * operation; timeout_us = 0 restores the default limit (2 s).
  */
 NVFP4_API nvfp4_status nvfp4_debug_set_fault_injection(int mode, uint32_t timeout_us);
+
+/*
+ * Testing and comparison hook: the GEMM kernel used for M > 128 by
+ * nvfp4_gemm and nvfp4_linear from the next call on (process-wide, all
+ * devices). kernel = 0: the CTA-pair kernel (default); kernel = 1: the
+ * single-CTA kernel (128 x 256 tiles, one SM per tile). The entry points
+ * whose epilogues live only in the CTA-pair kernel (bias / re-quantization,
+ * LoRA, grouped projections above 128 rows) return UNSUPPORTED_SHAPE while
+ * kernel = 1. Errors: INVALID_ARG (kernel not 0 or 1).
+ */
+NVFP4_API nvfp4_status nvfp4_debug_select_gemm_kernel(int kernel);
+
+/*
+ * Testing hook for the fused decode mode (NVFP4_LINEAR_FUSED with M <= 4,
+ * K <= 6144), whose quantized activation otherwise never leaves shared
+ * memory: with on = 1, CTA 0 of the fused kernel also writes the codes and
+ * tile-layout scales it produced into the workspace, at the offsets where
+ * the unfused path leaves them (see nvfp4_linear), so that they can be
+ * compared byte for byte. Process-wide; on = 0 (default) turns it off.
+ * Errors: INVALID_ARG (on not 0 or 1).
+ */
+NVFP4_API nvfp4_status nvfp4_debug_capture_fused_operand(int on);
 
 #ifdef __cplusplus
 }

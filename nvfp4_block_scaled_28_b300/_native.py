@@ -62,8 +62,9 @@ SIGNATURES = {
                                  ctypes.c_float, _P, _I64, _P, _P, _SZ, _P]),
     "nvfp4_linear_lora_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64]),
     "nvfp4_device_error": (_INT, [_INT]),
-    "nvfp4_mma_peak_probe": (_INT, [_INT, _INT, _INT, _P, _P]),
     "nvfp4_debug_set_fault_injection": (_INT, [_INT, _U32]),
+    "nvfp4_debug_select_gemm_kernel": (_INT, [_INT]),
+    "nvfp4_debug_capture_fused_operand": (_INT, [_INT]),
 }
 
 _lock = threading.Lock()
@@ -92,6 +93,33 @@ def load() -> ctypes.CDLL:
             f.restype = res
             f.argtypes = args
         _lib = lib
+        return lib
+
+
+PROBE_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnvfp4_probe.so")
+# the measurement library of include/nvfp4_probe.h
+PROBE_SIGNATURES = {
+    "nvfp4_mma_peak_probe": (_INT, [_INT, _INT, _INT, _P, _P]),
+    "nvfp4_probe_error": (_INT, [_INT]),
+}
+_probe = None
+
+
+def load_probe() -> ctypes.CDLL:
+    """Load the measurement library (once). Raises if it has not been built."""
+    global _probe
+    with _lock:
+        if _probe is not None:
+            return _probe
+        if not os.path.exists(PROBE_LIB_PATH):
+            raise ImportError("%s is not built; run `python -m nvfp4_block_scaled_28_b300.build`"
+                              % PROBE_LIB_PATH)
+        lib = ctypes.CDLL(PROBE_LIB_PATH)
+        for name, (res, args) in PROBE_SIGNATURES.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        _probe = lib
         return lib
 
 

@@ -1,14 +1,26 @@
-"""Build the in-tree C-ABI library ``libnvfp4_b300.so`` for sm_103a.
+"""Build the in-tree shared libraries for sm_103a.
 
-One nvcc invocation compiles every ``csrc/*.cu`` into a shared library next to
-this file (static CUDA runtime; the driver API is reached at run time through
-cudaGetDriverEntryPointByVersion, so the library loads on machines without a
-GPU driver). No fast-math: the quantizer's bytes depend on IEEE binary32
-division, reciprocal and multiplication.
+``libnvfp4_b300.so``   the C-ABI library of include/nvfp4.h: one nvcc
+                       invocation over every ``csrc/*.cu``;
+``libnvfp4_probe.so``  the measurement library of include/nvfp4_probe.h
+                       (the dense FP4 tensor-core peak probe, ``probe/``);
+                       it is not part of the product library.
+
+Both link the CUDA runtime statically; the driver API is reached at run time
+through cudaGetDriverEntryPointByVersion, so the libraries load on machines
+without a GPU driver. No fast-math: the quantizer's bytes depend on IEEE
+binary32 division, reciprocal and multiplication.
+
+A library is rebuilt when the SHA-256 of its inputs (every source and header
+it is built from, this file, and the nvcc command line) differs from the one
+recorded beside it when it was last built; file times play no part, so a
+copied tree or a restored checkout cannot skip a rebuild.
 """
 from __future__ import annotations
 
 import glob
+import hashlib
+import json
 import os
 import shutil
 import subprocess
@@ -17,9 +29,11 @@ import sys
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
+PROBE_SRC = os.path.join(PKG_DIR, "probe")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libnvfp4_b300.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
+PROBE_LIB_PATH = os.path.join(PKG_DIR, "libnvfp4_probe.so")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -39,27 +53,66 @@ def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _inputs():
-    return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + \
-        glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h")) + \
-        [os.path.abspath(__file__)]
+def probe_sources():
+    return sorted(glob.glob(os.path.join(PROBE_SRC, "*.cu")))
+
+
+def _headers():
+    return sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) +
+                  glob.glob(os.path.join(INCLUDE, "*.h")))
+
+
+class Target:
+    def __init__(self, path, srcs, extra_flags=()):
+        self.path = path
+        self.srcs = srcs
+        self.extra_flags = list(extra_flags)
+
+    @property
+    def stamp(self):
+        return self.path + ".sha256"
+
+    def command(self, out):
+        return ([nvcc()] + ARCH_FLAGS + NVCC_FLAGS + self.extra_flags +
+                ["-I", INCLUDE, "-I", CSRC, "-o", out] + self.srcs)
+
+    def digest(self):
+        h = hashlib.sha256()
+        for p in self.srcs + _headers() + [os.path.abspath(__file__)]:
+            h.update(os.path.relpath(p, ROOT).encode())
+            with open(p, "rb") as f:
+                h.update(hashlib.sha256(f.read()).digest())
+        # the command line without the output path and the nvcc location
+        h.update(json.dumps(ARCH_FLAGS + NVCC_FLAGS + self.extra_flags).encode())
+        return h.hexdigest()
+
+    def up_to_date(self):
+        if not (os.path.exists(self.path) and os.path.exists(self.stamp)):
+            return False
+        with open(self.stamp) as f:
+            return f.read().strip() == self.digest()
+
+
+def product_target():
+    return Target(LIB_PATH, sources())
+
+
+def probe_target():
+    return Target(PROBE_LIB_PATH, probe_sources())
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
-        return False
-    t = os.path.getmtime(LIB_PATH)
-    return all(os.path.getmtime(p) <= t for p in _inputs())
+    return product_target().up_to_date()
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB_PATH
-    tmp = LIB_PATH + ".tmp.%d" % os.getpid()
-    cmd = [nvcc()] + ARCH_FLAGS + NVCC_FLAGS + ["-I", INCLUDE, "-I", CSRC,
-                                                "-o", tmp] + sources()
+def _build(t: Target, force: bool, verbose: bool) -> str:
+    if not force and t.up_to_date():
+        return t.path
+    digest = t.digest()
+    tmp = t.path + ".tmp.%d" % os.getpid()
+    cmd = t.command(tmp)
     res = subprocess.run(cmd, capture_output=True, text=True)
-    log = os.path.join(PKG_DIR, "build.log")
+    log = os.path.splitext(t.path)[0] + ".build.log"
     with open(log, "w") as f:
         f.write(" ".join(cmd) + "\n" + res.stdout + res.stderr)
     if res.returncode != 0:
@@ -67,10 +120,22 @@ def build(force: bool = False, verbose: bool = False) -> str:
         raise RuntimeError("nvcc failed (see %s)" % log)
     if verbose:
         sys.stdout.write(res.stdout + res.stderr)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, t.path)
+    with open(t.stamp, "w") as f:
+        f.write(digest + "\n")
+    return t.path
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Build the product library (and the probe library beside it)."""
+    path = _build(product_target(), force, verbose)
+    _build(probe_target(), force, verbose)
+    return path
+
+
+def build_probe(force: bool = False, verbose: bool = False) -> str:
+    return _build(probe_target(), force, verbose)
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True)
-    print(LIB_PATH)
+    print(build(force="--force" in sys.argv, verbose=True))

@@ -66,9 +66,13 @@ inline nvfp4_status from_cuda(cudaError_t e) {
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Limits of the 32-bit index arithmetic inside the kernels.
-constexpr int64_t kMaxBlocks = int64_t(1) << 31;
+// Limits of the 32-bit index arithmetic inside the kernels: the element,
+// 16-element-block and 16-byte-vector indices of a tensor, plus the few
+// grid strides a thread adds ahead of its bounds test, stay below 2^32 when
+// a tensor has fewer than 2^28 blocks (2^32 elements, 8 GiB of bfloat16).
+constexpr int64_t kMaxBlocks = int64_t(1) << 28;
 constexpr int64_t kMaxDim = int64_t(1) << 30;
+constexpr int64_t kMaxOutputs = int64_t(1) << 42;  // M x N of one GEMM
 
 nvfp4_status check_bf16_matrix(const void *X, int64_t rows, int64_t cols, int64_t ld) {
     if (rows < 0 || cols < 0 || ld < cols) return NVFP4_ERR_INVALID_ARG;
@@ -99,6 +103,7 @@ nvfp4_status check_gemm_b_and_y(const uint8_t *Bq, const uint8_t *Bs, const floa
     if (M < 0 || N < 0 || K <= 0 || ldy < N) return NVFP4_ERR_INVALID_ARG;
     if (K % 256 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (M * N >= kMaxOutputs) return NVFP4_ERR_UNSUPPORTED_SHAPE;  // tile counts stay 32-bit
     if (M == 0 || N == 0) return NVFP4_OK;
     if (!Bq || !Bs || !g_b || !Y) return NVFP4_ERR_INVALID_ARG;
     if (!aligned(Bq, 16) || !aligned(Bs, 16) || !aligned(g_b, 4) || !aligned(Y, 2))
@@ -156,7 +161,7 @@ nvfp4_status nvfp4_global_scale(const void *X, int64_t rows, int64_t cols, int64
     if (g == nullptr) return NVFP4_ERR_INVALID_ARG;
     if (!aligned(g, 4)) return NVFP4_ERR_MISALIGNED;
     if (cols % 8 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    if (rows * (cols / 8) >= kMaxBlocks) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (rows * cols >= kMaxBlocks * 16) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     return from_cuda(launch_global_scale(static_cast<const uint16_t *>(X), rows, cols, ldx, g,
                                          static_cast<cudaStream_t>(stream)));
 }
@@ -238,6 +243,7 @@ nvfp4_status nvfp4_gemm(const uint8_t *Aq, const uint8_t *As, const float *g_a, 
 // nvfp4_linear workspace: [g_x, barrier counter | amax partials] header,
 // X codes, X scales.
 constexpr size_t kLinearHeader = 256 + sizeof(uint32_t) * kMaxAmaxPartials;
+static_assert(kLinearHeader == 8448, "offset of X's codes documented in nvfp4.h");
 
 }  // extern "C"
 
@@ -311,6 +317,12 @@ nvfp4_status linear_impl(const void *X, int64_t M, int64_t K, int64_t ldx, const
         // tiles in shared memory; no codes in HBM
         SkinnyArgs sa{Wq, Ws, g_w, nullptr, nullptr, Xh, ldx, g_x, M, N, K,
                       static_cast<uint16_t *>(Y), ldy, 1, wg};
+        if (debug_state().capture_fused_operand) {
+            // testing hook: the operand the kernel quantized in shared
+            // memory goes where the unfused path leaves it
+            sa.dbg_xq = xq;
+            sa.dbg_xs = xs;
+        }
         return from_cuda(launch_gemm_skinny(sa, st));
     }
     // unfused (and fused beyond 4 rows or K = 6144, where every CTA
@@ -474,16 +486,16 @@ nvfp4_status nvfp4_device_error(int clear) {
     return (word & kDevErrTimeout) ? NVFP4_ERR_TIMEOUT : NVFP4_OK;
 }
 
-nvfp4_status nvfp4_mma_peak_probe(int ctas, int iters, int variant, unsigned long long *cycles,
-                                  void *stream) {
-    if (ctas <= 0 || iters <= 0 || cycles == nullptr) return NVFP4_ERR_INVALID_ARG;
-    if (variant < 0 || variant > 7) return NVFP4_ERR_INVALID_ARG;
-    if (variant == 7 && ctas < 2) return NVFP4_ERR_INVALID_ARG;  // clusters of 2
-    // unrolled by 4 MMAs per warp; variant 2 splits them over two warps
-    if (iters % (variant == 2 ? 8 : 4) != 0) return NVFP4_ERR_INVALID_ARG;
-    if (!aligned(cycles, 8)) return NVFP4_ERR_MISALIGNED;
-    return from_cuda(launch_mma_peak(ctas, iters, variant, cycles,
-                                     static_cast<cudaStream_t>(stream)));
+nvfp4_status nvfp4_debug_select_gemm_kernel(int kernel) {
+    if (kernel != 0 && kernel != 1) return NVFP4_ERR_INVALID_ARG;
+    debug_state().single_cta_gemm = kernel;
+    return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_debug_capture_fused_operand(int on) {
+    if (on != 0 && on != 1) return NVFP4_ERR_INVALID_ARG;
+    debug_state().capture_fused_operand = on;
+    return NVFP4_OK;
 }
 
 nvfp4_status nvfp4_debug_set_fault_injection(int mode, uint32_t timeout_us) {

@@ -79,7 +79,7 @@ struct Params {
     int64_t ldy;
     int M, N, K;
     int num_m_tiles, num_n_tiles;
-    int num_ctiles;      // cluster tiles: CM consecutive M-tiles sharing one N-tile
+    int num_tiles;
     int y_vec;           // rows of Y start 16-byte aligned: 16-byte stores
     int inject;          // 1: the producer issues nothing (bounded-wait test)
     uint64_t timeout_ns;
@@ -140,19 +140,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
     return __shfl_sync(kAll, ok, 0) != 0;
 }
 
-// M-tile of this CTA in cluster tile `ct` (CTA `rank` of a cluster of CM).
-template <int CM>
-__device__ __forceinline__ void cta_tile(int ct, int rank, const Params &p, int &mt, int &nt) {
-    const int num_cm = (p.num_m_tiles + CM - 1) / CM;
-    int cm;
-    tile_coords(ct, num_cm, p.num_n_tiles, GROUP_M / CM, cm, nt);
-    mt = cm * CM + rank;
-}
-
-// CM > 1: the CM CTAs of a cluster work on CM consecutive M-tiles of the same
-// N-tile in lockstep; each loads 1/CM of the shared B tile (and of its
-// scales) and multicasts it to all, so B is read from L2 once per cluster.
-template <int CM>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const Params p) {
@@ -166,15 +153,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int num_k = p.K / BK;
     const int kb4 = p.K / 64;  // 512-byte scale tiles per 128-row group
     const int n_sf_groups = (p.N + 127) / 128;
-    const int rank = CM > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-    const int cluster_id = blockIdx.x / CM;
-    const int num_clusters = gridDim.x / CM;
-    constexpr uint16_t kMask = static_cast<uint16_t>((1u << CM) - 1u);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&sh.full[s], 1);
-            mbar_init(&sh.empty[s], CM);  // one release per CTA of the cluster
+            mbar_init(&sh.empty[s], 1);
         }
         mbar_init(&sh.acc_full, 1);
         mbar_init(&sh.acc_empty, kEpiWarps);
@@ -190,7 +173,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (CM > 1) cluster_sync_all();  // peers' barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
     // The set-up above overlaps the previous kernel when launched as a
@@ -203,13 +185,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t pol = policy_evict_last();
         int g = 0;  // stage counter over this CTA's tiles
         bool ok = !p.inject;
-        for (int ct = cluster_id; ok && ct < p.num_ctiles; ct += num_clusters) {
+        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
             int mt, nt;
-            cta_tile<CM>(ct, rank, p, mt, nt);
-            const bool mt_valid = mt < p.num_m_tiles;  // a cluster's tail tile may be empty
+            tile_coords(t, p.num_m_tiles, p.num_n_tiles, GROUP_M, mt, nt);
             const bool two_groups = (nt * 2 + 1) < n_sf_groups;
-            const uint32_t tx = A_BYTES + B_BYTES + (mt_valid ? SFA_BYTES : 0) +
-                                (two_groups ? 2 : 1) * (SFB_BYTES / 2);
+            const uint32_t tx = A_BYTES + B_BYTES + SFA_BYTES + (two_groups ? 2 : 1) * (SFB_BYTES / 2);
             for (int kt = 0; kt < num_k; ++kt, ++g) {
                 const int s = g % STAGES;
                 if (!warp_wait(&sh.empty[s], ((g / STAGES) & 1) ^ 1, p, sh)) {
@@ -220,37 +200,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(&sh.full[s], tx);
                     tma_load_2d(smem + SMEM_A + s * A_BYTES, &tmA, &sh.full[s], kt * (BK / 2),
                                 mt * BM, pol);
-                    uint8_t *bdst = smem + SMEM_B + s * B_BYTES + rank * (B_BYTES / CM);
-                    if (CM == 1)
-                        tma_load_2d(bdst, &tmB, &sh.full[s], kt * (BK / 2), nt * BN, pol);
-                    else
-                        tma_load_2d_mc(bdst, &tmB, &sh.full[s], kt * (BK / 2),
-                                       nt * BN + rank * (BN / CM), kMask, pol);
-                    if (mt_valid) {
-                        const uint8_t *sa =
-                            p.As + (static_cast<int64_t>(mt) * kb4 + kt * 4) * SF_TILE;
-                        bulk_load(smem + SMEM_SFA + s * SFA_BYTES, sa, SFA_BYTES, &sh.full[s], pol);
-                    }
-                    // B scales: two 128-row groups of 2 KiB; CTA `rank` loads
-                    // bytes [rank * 4K / CM, +4K / CM) of the pair
-                    constexpr int piece = SFB_BYTES / CM;
-                    const int grp = (rank * piece) / (SFB_BYTES / 2);
-                    const int off = (rank * piece) % (SFB_BYTES / 2);
-                    if (grp == 0 || two_groups) {
-                        const uint8_t *sb =
-                            p.Bs + (static_cast<int64_t>(nt * 2 + grp) * kb4 + kt * 4) * SF_TILE +
-                            off;
-                        uint8_t *sdst = smem + SMEM_SFB + s * SFB_BYTES + rank * piece;
-                        if (CM == 1) {
-                            bulk_load(sdst, sb, SFB_BYTES / 2, &sh.full[s], pol);
-                            if (two_groups)
-                                bulk_load(sdst + SFB_BYTES / 2,
-                                          sb + static_cast<int64_t>(kb4) * SF_TILE,
-                                          SFB_BYTES / 2, &sh.full[s], pol);
-                        } else {
-                            bulk_load_mc(sdst, sb, piece, &sh.full[s], kMask, pol);
-                        }
-                    }
+                    tma_load_2d(smem + SMEM_B + s * B_BYTES, &tmB, &sh.full[s], kt * (BK / 2),
+                                nt * BN, pol);
+                    const uint8_t *sa = p.As + (static_cast<int64_t>(mt) * kb4 + kt * 4) * SF_TILE;
+                    bulk_load(smem + SMEM_SFA + s * SFA_BYTES, sa, SFA_BYTES, &sh.full[s], pol);
+                    // B scales: two 128-row groups of 2 KiB (the second only
+                    // when the tile reaches past the first 128 rows of B)
+                    const uint8_t *sb = p.Bs + (static_cast<int64_t>(nt * 2) * kb4 + kt * 4) * SF_TILE;
+                    uint8_t *sdst = smem + SMEM_SFB + s * SFB_BYTES;
+                    bulk_load(sdst, sb, SFB_BYTES / 2, &sh.full[s], pol);
+                    if (two_groups)
+                        bulk_load(sdst + SFB_BYTES / 2, sb + static_cast<int64_t>(kb4) * SF_TILE,
+                                  SFB_BYTES / 2, &sh.full[s], pol);
                 }
                 __syncwarp();
             }
@@ -263,22 +224,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(&sh.full[s], (fills - 1) & 1, p.timeout_ns);
             }
         }
-        if (CM > 1 && lane == 0 && !p.inject) {
-            // every CTA of the cluster releases every stage to every CTA:
-            // wait until the last releases addressed to this CTA have
-            // landed, so none arrives after it exits
-            for (int s = 0; s < STAGES && s < g; ++s) {
-                const int fills = (g - s + STAGES - 1) / STAGES;
-                mbar_wait(&sh.empty[s], (fills - 1) & 1, p.timeout_ns);
-            }
-        }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         constexpr uint32_t idesc = idesc_mxf4nvf4(BM, BN);
         int g = 0, it = 0;
         bool ok = true;
-        for (int ct = cluster_id; ok && ct < p.num_ctiles; ct += num_clusters, ++it) {
+        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++it) {
             if (!warp_wait(&sh.acc_empty, (it & 1) ^ 1, p, sh)) {
                 ok = false;
                 break;
@@ -311,10 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_mxf4nvf4_elect(tmem + ACC_COL, sdesc_sw128(a_smem + j * 32),
                                        sdesc_sw128(b_smem + j * 32), idesc, sf_a + j * 4,
                                        sf_b + j * 8, (kt | j) != 0);
-                if (CM == 1)
-                    tc_commit_elect(&sh.empty[s]);
-                else
-                    tc_commit_mc_elect(&sh.empty[s], kMask);
+                tc_commit_elect(&sh.empty[s]);
             }
             if (ok) tc_commit_elect(&sh.acc_full);
         }
@@ -332,11 +281,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = (warp - kFirstEpiWarp) >> 2;  // which 128 columns
         const float alpha = __fmul_rn(*p.g_a, *p.g_b);
         int it = 0;
-        for (int ct = cluster_id; ct < p.num_ctiles; ct += num_clusters, ++it) {
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
             if (!warp_wait(&sh.acc_full, it & 1, p, sh)) break;
             tc_fence_after();
             int mt, nt;
-            cta_tile<CM>(ct, rank, p, mt, nt);
+            tile_coords(t, p.num_m_tiles, p.num_n_tiles, GROUP_M, mt, nt);
             const uint32_t t_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + ACC_COL +
                                     static_cast<uint32_t>(half * 128);
             uint32_t packed[64];
@@ -380,7 +329,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (CM > 1) cluster_sync_all();  // no CTA leaves while a peer may still address it
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
@@ -397,70 +345,21 @@ bool make_operand_map(CUtensorMap *map, const uint8_t *ptr, int64_t rows, int64_
                        box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int CM>
-cudaError_t launch_cm(const CUtensorMap &tmA, const CUtensorMap &tmB, Params p, cudaStream_t st) {
-    static int max_clusters_of[kMaxDevices + 1] = {};  // 0: not yet queried
-    int &max_clusters = max_clusters_of[device_slot()];
-    if (max_clusters <= 0) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<CM>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
-        if (e != cudaSuccess) return e;
-        max_clusters = launch_cfg().num_sms / CM;
-        if (CM > 1) {
-            cudaLaunchConfig_t cfg = {};
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = CM;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.gridDim = dim3(CM * max_clusters, 1, 1);
-            cfg.blockDim = dim3(kThreads, 1, 1);
-            cfg.dynamicSmemBytes = SMEM_ALLOC;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<CM>, &cfg) == cudaSuccess && n > 0 &&
-                n < max_clusters)
-                max_clusters = n;
-        }
-    }
-    p.num_ctiles = ((p.num_m_tiles + CM - 1) / CM) * p.num_n_tiles;
-    const int clusters = p.num_ctiles < max_clusters ? p.num_ctiles : max_clusters;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CM;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1] = pdl_attribute();
-    cfg.gridDim = dim3(CM * clusters, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = SMEM_ALLOC;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<CM>, tmA, tmB, p);
-}
-
-int cluster_m() {
-    static int cm = 0;
-    if (cm == 0) {
-        cm = 1;
-        const char *env = getenv("NVFP4_GEMM_CLUSTER_M");  // tuning knob: 1, 2 or 4
-        if (env && (env[0] == '1' || env[0] == '2' || env[0] == '4') && env[1] == 0)
-            cm = env[0] - '0';
-    }
-    return cm;
-}
-
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
-    const int CM = cluster_m();
+    static int max_ctas_of[kMaxDevices + 1] = {};  // 0: not yet set up
+    int &max_ctas = max_ctas_of[device_slot()];
+    if (max_ctas <= 0) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
+        max_ctas = launch_cfg().num_sms;
+    }
     CUtensorMap tmA, tmB;
     if (!make_operand_map(&tmA, a.Aq, a.M, a.K, BM)) return cudaErrorInvalidValue;
-    if (!make_operand_map(&tmB, a.Bq, a.N, a.K, BN / CM)) return cudaErrorInvalidValue;
+    if (!make_operand_map(&tmB, a.Bq, a.N, a.K, BN)) return cudaErrorInvalidValue;
     Params p;
     p.As = a.As;
     p.Bs = a.Bs;
@@ -473,19 +372,22 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st) {
     p.K = static_cast<int>(a.K);
     p.num_m_tiles = static_cast<int>((a.M + BM - 1) / BM);
     p.num_n_tiles = static_cast<int>((a.N + BN - 1) / BN);
-    p.num_ctiles = 0;
+    p.num_tiles = p.num_m_tiles * p.num_n_tiles;
     p.y_vec = (a.ldy % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.Y) & 15) == 0);
     p.inject = debug_state().inject;
     p.timeout_ns = debug_state().timeout_ns;
     p.err = device_error_word();
     if (p.err == nullptr) return cudaErrorInvalidSymbol;
-    cudaError_t e;
-    if (CM == 4)
-        e = launch_cm<4>(tmA, tmB, p, st);
-    else if (CM == 2)
-        e = launch_cm<2>(tmA, tmB, p, st);
-    else
-        e = launch_cm<1>(tmA, tmB, p, st);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0] = pdl_attribute();
+    cfg.gridDim = dim3(p.num_tiles < max_ctas ? p.num_tiles : max_ctas, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_ALLOC;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel, tmA, tmB, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

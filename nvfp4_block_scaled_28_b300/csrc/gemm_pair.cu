@@ -573,14 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int gemm_use_pair() {
-    static int use = -1;
-    if (use < 0) {
-        const char *env = getenv("NVFP4_GEMM_PAIR");
-        use = (env && env[0] == '0' && env[1] == 0) ? 0 : 1;
-    }
-    return use;
-}
+int gemm_use_pair() { return debug_state().single_cta_gemm ? 0 : 1; }
 
 cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;

@@ -110,6 +110,11 @@ struct SkParams {
     int64_t ldy;
     int M, N, K;
     int n_tiles;
+    // testing hook (fused): CTA 0 copies the activation operand it quantized
+    // into shared memory out to these buffers (codes M x K/2, tile-layout
+    // scales with the padding rows of the first 128-row group zeroed)
+    uint8_t *dbg_xq;
+    uint8_t *dbg_xs;
     int inject;
     uint64_t timeout_ns;
     unsigned int *err;
@@ -390,6 +395,25 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
         // fused: the epilogue warps first help quantize X (idle until the
         // first accumulator is complete anyway)
         if (FUSED) quantize_x_resident<C, S>(p, sh, xres, sfxres);
+        if (FUSED && p.dbg_xq != nullptr && blockIdx.x == 0 && warp == 3 &&
+            sk_wait<S>(&sh.xready, 0, p, sh)) {
+            // testing hook: the resident operand, un-swizzled, to global
+            const int kbpr = p.K / 16;
+            for (int b = lane; b < p.M * kbpr; b += 32) {
+                const int r = b / kbpr, kb = b - r * kbpr;
+                const int chunk = kb >> 4, kbc = kb & 15, piece = kbc >> 1;
+                *reinterpret_cast<uint2 *>(p.dbg_xq + static_cast<int64_t>(r) * (p.K / 2) +
+                                           kb * 8) =
+                    *reinterpret_cast<const uint2 *>(xres + chunk * C::X_CHUNK + r * 128 +
+                                                     ((piece ^ (r & 7)) << 4) + (kbc & 1) * 8);
+            }
+            for (int i = lane; i < 128 * kbpr; i += 32) {
+                const int r = i / kbpr, kb = i - r * kbpr;
+                const int off = (kb >> 2) * SK_SF_TILE + (r & 31) * 16 + (r >> 5) * 4 + (kb & 3);
+                p.dbg_xs[off] = r < p.M ? sfxres[off] : 0;
+            }
+            __syncwarp();
+        }
         // -------------------------------------------------------- epilogue
         const int quarter = warp & 3;
         int it = 0;
@@ -474,6 +498,8 @@ cudaError_t launch_sk(const SkinnyArgs &a, cudaStream_t st) {
     p.N = static_cast<int>(a.N);
     p.K = static_cast<int>(a.K);
     p.n_tiles = static_cast<int>((a.N + SK_BM - 1) / SK_BM);
+    p.dbg_xq = FUSED ? a.dbg_xq : nullptr;
+    p.dbg_xs = FUSED ? a.dbg_xs : nullptr;
     p.inject = debug_state().inject;
     p.timeout_ns = debug_state().timeout_ns;
     p.err = device_error_word();

@@ -136,7 +136,7 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st);
 // The same GEMM on CTA pairs (tcgen05 cta_group::2), 256 x 256 tiles.
 cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st);
 // Kernel for M > 128: 1 = CTA pairs (default), 0 = single-CTA tiles
-// (NVFP4_GEMM_PAIR=0 selects it, for comparison).
+// (selected by nvfp4_debug_select_gemm_kernel, for comparison).
 int gemm_use_pair();
 
 // Skinny-M GEMM (Y^T = W X^T, weights as the 128-row MMA operand).
@@ -155,11 +155,11 @@ struct SkinnyArgs {
     int64_t ldy;
     int fused;
     WeightGroups groups = {};  // g_w then points at groups.count floats
+    // fused, testing hook: where CTA 0 writes the operand it quantized
+    uint8_t *dbg_xq = nullptr;
+    uint8_t *dbg_xs = nullptr;
 };
 cudaError_t launch_gemm_skinny(const SkinnyArgs &a, cudaStream_t st);
-
-cudaError_t launch_mma_peak(int ctas, int iters, int variant, unsigned long long *cycles,
-                            cudaStream_t st);
 
 // Device address of the library's error word on the current device.
 unsigned int *device_error_word();
@@ -168,6 +168,8 @@ unsigned int *device_error_word();
 struct DebugState {
     int inject = 0;
     uint64_t timeout_ns = 2000000000ull;
+    int single_cta_gemm = 0;  // 1: the single-CTA GEMM kernel for M > 128
+    int capture_fused_operand = 0;  // 1: the fused decode kernel writes its operand out
 };
 DebugState &debug_state();
 

@@ -17,7 +17,9 @@
 // only sees a host-side stand-in under the array's name, so the device
 // address is looked up once per device with cudaGetSymbolAddress (on the
 // first call made while that device is current) and then passed to the
-// kernels as an ordinary pointer.
+// kernels as an ordinary pointer. The kept address belongs to the device's
+// primary context: after a cudaDeviceReset it is stale, so the entry point
+// is not to be called on that device again in the same process.
 #include <cuda_runtime.h>
 
 #include <cstddef>

@@ -133,31 +133,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
-// 2-D tiled load multicast to the CTAs of this cluster named in `mask`: the
-// data lands at the same shared offset in each, and each CTA's mbarrier at
-// `bar`'s offset counts the bytes.
-__device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                               int32_t x, int32_t y, uint16_t mask,
-                                               uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(
-            smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y), "h"(mask),
-        "l"(policy)
-        : "memory");
-}
-
-// Contiguous bulk copy multicast to the CTAs named in `mask`.
-__device__ __forceinline__ void bulk_load_mc(void *dst, const void *src, uint32_t bytes,
-                                             uint64_t *bar, uint16_t mask, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".L2::cache_hint [%0], [%1], %2, [%3], %4, %5;" ::"r"(smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "h"(mask), "l"(policy)
-        : "memory");
-}
-
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -420,18 +395,6 @@ __device__ __forceinline__ void tmem_cp_32x128b_x4_elect(uint32_t taddr, uint64_
         "elect.sync _|e, 0xffffffff;\n\t"
         "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
         "l"(sdesc)
-        : "memory");
-}
-
-// Arrive on the mbarrier at `bar`'s offset in every CTA of `mask` once all
-// previously issued tcgen05 operations of this thread have completed.
-__device__ __forceinline__ void tc_commit_mc_elect(uint64_t *bar, uint16_t mask) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;\n\t}" ::"r"(smem_addr(bar)),
-        "h"(mask)
         : "memory");
 }
 

@@ -1,19 +1,47 @@
-// Dense FP4 tensor-core peak probe: every CTA issues back-to-back
-// tcgen05.mma kind::mxf4nvf4 (128 x N x 64, E4M3 block scales) on
-// operands that stay in shared memory, so no global traffic limits the
-// rate. The measured FLOP/s is the ceiling the GEMM is compared against.
+// Dense FP4 tensor-core peak probe (measurement library libnvfp4_probe.so,
+// declared in include/nvfp4_probe.h; not part of the linear-layer library):
+// every CTA issues back-to-back tcgen05.mma kind::mxf4nvf4 (128 x N x 64,
+// E4M3 block scales) on operands that stay in shared memory, so no global
+// traffic limits the rate. The measured FLOP/s is the ceiling the GEMM is
+// compared against.
 //
 // The issuing loop is specialised at compile time per variant and unrolled
 // by 4 with constant descriptor offsets: with run-time variant tests inside
 // the loop the warp's own scalar work, not the tensor core, set the rate.
 #include <cuda_runtime.h>
 
-#include "internal.h"
+#include <cstdint>
+
+#include "nvfp4_probe.h"
 #include "ptx.cuh"
 
 namespace nvfp4 {
 
 namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // bounded waits: 2 s
+
+// The probe's own error word (bounded waits that ran out).
+__device__ unsigned int g_probe_error = 0;
+
+int device_slot() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return kMaxDevices;
+    return dev;
+}
+
+unsigned int *device_error_word() {
+    static unsigned int *addr[kMaxDevices] = {};
+    const int dev = device_slot();
+    if (dev == kMaxDevices) return nullptr;
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_probe_error) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<unsigned int *>(p);
+    }
+    return addr[dev];
+}
 
 constexpr int kPeakThreads = 128;
 constexpr int kSmem = 16384 + 32768 + 1024 + 1024 + 1024;
@@ -264,7 +292,7 @@ cudaError_t launch_pair(int ctas, int iters, unsigned long long *cycles, cudaStr
     cfg.stream = st;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mma_peak_pair_kernel, iters, debug_state().timeout_ns, err,
+    return cudaLaunchKernelEx(&cfg, mma_peak_pair_kernel, iters, kTimeoutNs, err,
                               cycles);
 }
 
@@ -280,12 +308,10 @@ cudaError_t launch_v(int ctas, int iters, unsigned long long *cycles, cudaStream
     }
     unsigned int *err = device_error_word();
     if (err == nullptr) return cudaErrorInvalidSymbol;
-    mma_peak_kernel<V><<<ctas, kPeakThreads, kSmem, st>>>(iters, debug_state().timeout_ns, err,
+    mma_peak_kernel<V><<<ctas, kPeakThreads, kSmem, st>>>(iters, kTimeoutNs, err,
                                                           cycles);
     return cudaGetLastError();
 }
-
-}  // namespace
 
 cudaError_t launch_mma_peak(int ctas, int iters, int variant, unsigned long long *cycles,
                             cudaStream_t st) {
@@ -302,4 +328,34 @@ cudaError_t launch_mma_peak(int ctas, int iters, int variant, unsigned long long
     }
 }
 
+}  // namespace
 }  // namespace nvfp4
+
+extern "C" {
+
+NVFP4_PROBE_API int nvfp4_mma_peak_probe(int ctas, int iters, int variant, unsigned long long *cycles,
+                         void *stream) {
+    if (ctas <= 0 || iters <= 0 || cycles == nullptr) return 1;
+    if (variant < 0 || variant > 7) return 1;
+    if (variant == 7 && ctas < 2) return 1;  // clusters of 2
+    // unrolled by 4 MMAs per warp; variant 2 splits them over two warps
+    if (iters % (variant == 2 ? 8 : 4) != 0) return 1;
+    if ((reinterpret_cast<uintptr_t>(cycles) & 7) != 0) return 2;
+    return nvfp4::launch_mma_peak(ctas, iters, variant, cycles, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? 0
+               : 5;
+}
+
+NVFP4_PROBE_API int nvfp4_probe_error(int clear) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return 5;
+    unsigned int word = 0;
+    if (cudaMemcpyFromSymbol(&word, nvfp4::g_probe_error, sizeof(word)) != cudaSuccess) return 5;
+    if (clear) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(nvfp4::g_probe_error, &zero, sizeof(zero)) != cudaSuccess) return 5;
+    }
+    return word ? 6 : 0;
+}
+
+}  // extern "C"

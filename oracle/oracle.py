@@ -7,6 +7,7 @@ patterns, packed codes and E4M3 scales as uint8.
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
 import subprocess
 import threading
@@ -31,18 +32,36 @@ def lib_path() -> str:
     return _LIB
 
 
+_CFLAGS = ["-O2", "-std=c11", "-D_DEFAULT_SOURCE", "-fPIC", "-shared", "-fopenmp",
+           "-ffp-contract=off", "-fno-fast-math", "-Wall"]
+
+
+def _digest() -> str:
+    """SHA-256 of the oracle source and the compiler flags."""
+    h = hashlib.sha256()
+    with open(_SRC, "rb") as f:
+        h.update(f.read())
+    h.update(" ".join(_CFLAGS).encode())
+    return h.hexdigest()
+
+
 def build(force: bool = False) -> str:
     """Compile ``liboracle.so`` next to its source (gcc, OpenMP, no FMA
-    contraction, no fast-math). Rebuilds whenever the source is newer."""
-    if (not force and os.path.exists(_LIB)
-            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
-        return _LIB
+    contraction, no fast-math). Rebuilds whenever the SHA-256 of the source
+    and flags differs from the one recorded at the last build (file times
+    are not consulted)."""
+    stamp = _LIB + ".sha256"
+    digest = _digest()
+    if not force and os.path.exists(_LIB) and os.path.exists(stamp):
+        with open(stamp) as f:
+            if f.read().strip() == digest:
+                return _LIB
     tmp = _LIB + ".tmp.%d" % os.getpid()
-    cmd = ["gcc", "-O2", "-std=c11", "-D_DEFAULT_SOURCE", "-fPIC", "-shared",
-           "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-Wall",
-           "-o", tmp, _SRC, "-lm"]
+    cmd = ["gcc"] + _CFLAGS + ["-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
+    with open(stamp, "w") as f:
+        f.write(digest + "\n")
     return _LIB
 
 

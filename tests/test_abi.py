@@ -1,6 +1,7 @@
 """The C-ABI library loads, exports every entry point include/nvfp4.h
-declares, and rejects bad arguments before launching anything (no GPU
-needed: every case here fails the host-side checks)."""
+declares (and the measurement library every entry point of
+include/nvfp4_probe.h), and rejects bad arguments before launching anything
+(no GPU needed: every case here fails the host-side checks)."""
 import ctypes
 import os
 import re
@@ -13,12 +14,13 @@ from nvfp4_block_scaled_28_b300 import _native as N
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "nvfp4.h")
+PROBE_HEADER = os.path.join(ROOT, "include", "nvfp4_probe.h")
 
 
-def declared_functions():
-    text = open(HEADER).read()
+def declared_functions(path=HEADER, macro="NVFP4_API"):
+    text = open(path).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"NVFP4_API\s+[\w\s\*]+?\b(nvfp4_\w+)\s*\(", text)))
+    return sorted(set(re.findall(macro + r"\s+[\w\s\*]+?\b(nvfp4_\w+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")
@@ -41,6 +43,27 @@ def test_library_exports_every_declared_symbol(lib):
     for name in names:
         assert hasattr(lib, name), name
     assert set(names) == set(N.SIGNATURES), "binding and header disagree"
+
+
+def test_probe_library_is_separate_and_exports_its_header():
+    from nvfp4_block_scaled_28_b300 import build
+    build.build_probe()
+    probe = N.load_probe()
+    names = declared_functions(PROBE_HEADER, "NVFP4_PROBE_API")
+    assert names == sorted(N.PROBE_SIGNATURES)
+    for name in names:
+        assert hasattr(probe, name), name
+    # the product library carries no measurement probe
+    product = N.load()
+    for name in names:
+        assert not hasattr(product, name), name
+    assert "nvfp4_mma_peak_probe" not in declared_functions()
+
+
+def test_every_header_is_checked():
+    import glob
+    assert sorted(os.path.basename(h) for h in glob.glob(os.path.join(ROOT, "include", "*.h"))) \
+        == ["nvfp4.h", "nvfp4_probe.h"]
 
 
 def test_status_strings(lib):
@@ -127,8 +150,8 @@ def test_python_binding_rejects_packed_fp4_as_bf16():
                         torch.zeros(128, 16, dtype=torch.uint8), g)
 
 
-def test_mma_peak_probe_argument_checks(lib):
-    p = lib.nvfp4_mma_peak_probe
+def test_mma_peak_probe_argument_checks():
+    p = N.load_probe().nvfp4_mma_peak_probe
     assert p(1, 8, 8, A16, None) == N.ERR_INVALID_ARG   # no such variant
     assert p(1, 8, 7, A16, None) == N.ERR_INVALID_ARG   # pair variant needs 2 CTAs
     assert p(1, 8, -1, A16, None) == N.ERR_INVALID_ARG
@@ -137,6 +160,12 @@ def test_mma_peak_probe_argument_checks(lib):
     assert p(0, 8, 0, A16, None) == N.ERR_INVALID_ARG
     assert p(1, 8, 0, None, None) == N.ERR_INVALID_ARG
     assert p(1, 8, 0, A16 + 4, None) == N.ERR_MISALIGNED
+
+
+def test_select_gemm_kernel_checks(lib):
+    assert lib.nvfp4_debug_select_gemm_kernel(2) == N.ERR_INVALID_ARG
+    assert lib.nvfp4_debug_select_gemm_kernel(-1) == N.ERR_INVALID_ARG
+    assert lib.nvfp4_debug_select_gemm_kernel(0) == N.OK
 
 
 def test_linear_bias_requant_argument_checks(lib):
@@ -215,3 +244,25 @@ def test_library_is_built_from_the_current_sources():
     artifact's own time stamp is compared with every source (no stamp files)."""
     from nvfp4_block_scaled_28_b300 import build
     assert build.up_to_date(), "the library is older than its sources: rebuild it"
+
+
+def test_block_count_limit_keeps_indices_32_bit(lib):
+    """Tensors of 2^28 or more 16-element blocks are rejected before any
+    launch (the kernels' 32-bit block and vector indices, plus the grid
+    strides added ahead of their bounds tests, stay below 2^32). Just below
+    the limit the shape passes and the next check (a null global scale)
+    fails instead."""
+    limit = 1 << 28
+    rows, cols = 1 << 14, (limit // (1 << 14)) * 16   # exactly 2^28 blocks
+    q = lib.nvfp4_quantize
+    assert q(A16, rows, cols, cols, A16, A16, A16, 0, None) == N.ERR_UNSUPPORTED_SHAPE
+    assert q(A16, rows - 1, cols, cols, None, A16, A16, 0, None) == N.ERR_INVALID_ARG
+    assert lib.nvfp4_global_scale(A16, rows, cols, cols, A16, None) == N.ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_global_scale(A16, rows - 1, cols, cols, None, None) == N.ERR_INVALID_ARG
+    lin = lib.nvfp4_linear
+    K = cols
+    assert lin(A16, rows, K, K, A16, A16, A16, 256, A16, 256, None, 0, A16 * 16, 1 << 62,
+               None) == N.ERR_UNSUPPORTED_SHAPE
+    # M x N beyond the output limit
+    assert lib.nvfp4_gemm(A16, A16, A16, A16, A16, A16, 1 << 21, 1 << 21, 256, A16, 1 << 21,
+                          None, 0, None) == N.ERR_UNSUPPORTED_SHAPE

@@ -151,16 +151,28 @@ def test_fused_skinny_strided_x_and_given_scale(nv, oracle_mod):
     check_gemm_tolerance(bf16_bits(y_f), oracle_mod.gemm(xq, xs, gx, wq, ws, gw), "strided")
 
 
-def _full_size_case(nv, oracle_mod, name, M, Nn, n_rows):
+def tile_covering_rows(M: int, step: int, seed: int = 1) -> np.ndarray:
+    """One random row in every `step`-row band of [0, M), plus the first and
+    last row. With step dividing 128 every CTA's 128 accumulator rows of
+    every output tile (whole tiles and the column halves of the partial last
+    wave alike, since each sampled row is checked across all N columns) are
+    sampled; the offset within a band cycles through the four 32-lane TMEM
+    quarters from band to band."""
+    rng = np.random.default_rng(seed)
+    starts = np.arange(0, M, step)
+    quarter = (np.arange(len(starts)) % 4) * 32 if step == 128 else 0
+    within = quarter + rng.integers(0, min(step, 32), len(starts))
+    rows = np.minimum(starts + within, M - 1)
+    return np.unique(np.concatenate([[0, M - 1], rows]))
+
+
+def _full_size_case(nv, oracle_mod, name, M, Nn, step):
     w_ = workloads.WORKLOADS[name]
     x = workloads.make_x(w_.x_kind, M, w_.K, workloads.x_seed(w_))
     w = workloads.make_w(Nn, w_.K, workloads.w_seed(w_))
     (xq, xs, gx), (wq, ws, gw) = _oracle_operands(oracle_mod, x, w)
     y, (Wq, Ws, _) = _run_linear(nv, x, w, nv.LINEAR_UNFUSED)
-    rng = np.random.default_rng(1)
-    rows = np.arange(M) if M <= n_rows else np.sort(rng.choice(M, n_rows, replace=False))
-    if M > n_rows:
-        rows = np.unique(np.concatenate([[0, M - 1], rows]))
+    rows = np.arange(M) if M <= 64 else tile_covering_rows(M, step)
     y_ref = oracle_mod.gemm_rows(xq, xs, gx, wq, ws, gw, rows)
     y_rows = y.index_select(0, torch.from_numpy(rows).cuda())
     max_rel, floor_only = check_gemm_tolerance(bf16_bits(y_rows), y_ref, name)
@@ -173,7 +185,7 @@ def _full_size_case(nv, oracle_mod, name, M, Nn, n_rows):
 
 
 def test_full_size_prefill(nv, oracle_mod):
-    _full_size_case(nv, oracle_mod, "prefill", 4096, 5120, 48)
+    _full_size_case(nv, oracle_mod, "prefill", 4096, 5120, 32)   # 128 rows, every 32-row band
 
 
 @pytest.mark.parametrize("Nn", [9216, 12288])
@@ -183,11 +195,18 @@ def test_full_size_dit(nv, oracle_mod, Nn):
 
 @pytest.mark.parametrize("M", [1, 8, 32])
 def test_full_size_decode(nv, oracle_mod, M):
-    _full_size_case(nv, oracle_mod, "decode", M, 27648, 32)
+    _full_size_case(nv, oracle_mod, "decode", M, 27648, 32)      # every row
 
 
 def test_full_size_square(nv, oracle_mod):
-    _full_size_case(nv, oracle_mod, "square", 16384, 16384, 12)
+    _full_size_case(nv, oracle_mod, "square", 16384, 16384, 128)  # 128 rows, every CTA tile
+
+
+def test_tile_covering_rows_reach_every_tile():
+    for M, step in ((4096, 32), (16384, 128), (300, 32), (16384 + 77, 128)):
+        rows = tile_covering_rows(M, step)
+        assert rows.min() == 0 and rows.max() == M - 1
+        assert set(np.unique(rows // 128)) == set(range((M + 127) // 128))
 
 
 def test_bounded_wait_timeout_is_reported(nv, oracle_mod):

@@ -1,12 +1,8 @@
 """GPU parity of the single-CTA GEMM kernel (128 x 256 tiles), the
-alternative to the CTA-pair kernel selected by NVFP4_GEMM_PAIR=0. The
-selection is read once per process, so the GPU work runs in a child
-process; its outputs are checked here against the oracle within
-|y - y_ref| <= 2^-7 |y_ref| + 1e-3 ||Y_ref[m,:]||_2."""
-import os
-import subprocess
-import sys
-
+alternative to the CTA-pair kernel selected by
+nvfp4_debug_select_gemm_kernel(1). Its outputs are checked against the
+oracle within |y - y_ref| <= 2^-7 |y_ref| + 1e-3 ||Y_ref[m,:]||_2, with at
+least one sampled row in every 128-row tile of the large shape."""
 import numpy as np
 import pytest
 import torch
@@ -16,43 +12,39 @@ from nvfp4_block_scaled_28_b300 import workloads
 
 pytestmark = pytest.mark.gpu
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+@pytest.fixture(scope="module")
+def nv():
+    import nvfp4_block_scaled_28_b300 as nv
+    nv.load_library()
+    assert torch.cuda.is_available(), "CUDA device required"
+    return nv
+
+
 SHAPES = [(129, 257, 512), (300, 520, 768), (513, 1000, 1024), (4096, 5120, 5120)]
 
-CHILD = r"""
-import sys, numpy as np, torch
-sys.path.insert(0, %(root)r)
-import nvfp4_block_scaled_28_b300 as nv
-from nvfp4_block_scaled_28_b300 import workloads
-out = {}
-for (M, N, K) in %(shapes)r:
-    x = workloads.make_x("outlier", M, K, seed=M + 7 * K)
-    w = workloads.make_w(N, K, seed=N + 11 * K)
-    Wq, Ws, gw = nv.nvfp4_quantize_weight(w.cuda(), nv.SF_MMA_128x4)
-    y = nv.nvfp4_linear(x.cuda(), Wq, Ws, gw)
-    out["%%d_%%d_%%d" %% (M, N, K)] = y.cpu().view(torch.int16).numpy()
-assert nv.nvfp4_device_error() == 0
-np.savez(%(path)r, **out)
-"""
 
-
-def test_single_cta_kernel_matches_oracle(oracle_mod, tmp_path):
-    path = str(tmp_path / "y.npz")
-    env = dict(os.environ, NVFP4_GEMM_PAIR="0")
-    r = subprocess.run([sys.executable, "-c", CHILD % {"root": ROOT, "shapes": SHAPES,
-                                                       "path": path}],
-                       env=env, capture_output=True, text=True, timeout=600)
-    assert r.returncode == 0, r.stderr[-2000:]
-    got = np.load(path)
-    for (M, N, K) in SHAPES:
-        x = workloads.make_x("outlier", M, K, seed=M + 7 * K)
-        w = workloads.make_w(N, K, seed=N + 11 * K)
-        xb, wb = bf16_bits(x), bf16_bits(w)
-        gx, gw = oracle_mod.global_scale(xb), oracle_mod.global_scale(wb)
-        xq, xs = oracle_mod.quantize(xb, gx)
-        wq, ws = oracle_mod.quantize(wb, gw)
-        y = got["%d_%d_%d" % (M, N, K)].view(np.uint16)
-        rows = np.arange(M) if M <= 600 else np.unique(
-            np.concatenate([[0, M - 1], np.random.default_rng(M).choice(M, 30, replace=False)]))
-        y_ref = oracle_mod.gemm_rows(xq, xs, gx, wq, ws, gw, rows)
-        check_gemm_tolerance(y[rows], y_ref, "single-CTA %dx%dx%d" % (M, N, K))
+def test_single_cta_kernel_matches_oracle(nv, oracle_mod):
+    lib = nv.load_library()
+    assert lib.nvfp4_debug_select_gemm_kernel(1) == 0
+    try:
+        for (M, N, K) in SHAPES:
+            x = workloads.make_x("outlier", M, K, seed=M + 7 * K)
+            w = workloads.make_w(N, K, seed=N + 11 * K)
+            Wq, Ws, gw = nv.nvfp4_quantize_weight(w.cuda(), nv.SF_MMA_128x4)
+            y = bf16_bits(nv.nvfp4_linear(x.cuda(), Wq, Ws, gw))
+            assert nv.nvfp4_device_error() == 0
+            xb, wb = bf16_bits(x), bf16_bits(w)
+            gx, gwo = oracle_mod.global_scale(xb), oracle_mod.global_scale(wb)
+            xq, xs = oracle_mod.quantize(xb, gx)
+            wq, ws = oracle_mod.quantize(wb, gwo)
+            if M <= 600:
+                rows = np.arange(M)
+            else:
+                rng = np.random.default_rng(M)
+                rows = np.unique(np.concatenate([
+                    [0, M - 1], np.arange(0, M, 128) + rng.integers(0, 128, (M + 127) // 128)]))
+                rows = rows[rows < M]
+            y_ref = oracle_mod.gemm_rows(xq, xs, gx, wq, ws, gwo, rows)
+            check_gemm_tolerance(y[rows], y_ref, "single-CTA %dx%dx%d" % (M, N, K))
+    finally:
+        assert lib.nvfp4_debug_select_gemm_kernel(0) == 0

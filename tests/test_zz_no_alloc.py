@@ -4,7 +4,9 @@ device memory (it keeps its scratch in a fixed array inside the library).
 Called through the C ABI twice in a row -- a larger problem, then a smaller
 one that lands on the stale contents the first call left in the shared
 array -- and checked against nvfp4_linear, the entry point with a
-caller-provided workspace, within the GEMM tolerance the other tests use.
+caller-provided workspace. Both run the same kernels on the same inputs, so
+the outputs must be bitwise equal (which is also within the GEMM tolerance
+the other tests use).
 This file is collected last so that a run stopping at the first failure has
 already run every other test.
 """
@@ -45,6 +47,8 @@ def test_noalloc_matches_linear_on_two_calls(nv, shapes):
         Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
         assert _call_noalloc(lib, X, Wq, Ws, gw, Y) == 0
         torch.cuda.synchronize()
+        assert torch.equal(Y.view(torch.int16), y_ref.view(torch.int16)), \
+            "noalloc call %d differs from nvfp4_linear" % (i + 1)
         check_gemm_tolerance(bf16_bits(Y), bf16_bits(y_ref), "noalloc call %d" % (i + 1))
     assert nv.nvfp4_device_error() == 0
 
