@@ -769,6 +769,8 @@ def run_single_op(args):
                           "clocks": clocks}))
         return
     M, Nn, K = (int(v) for v in args.shape.split(","))
+    _ok(lib.nvfp4_debug_select_gemm_kernel({"pair": 0, "single": 1}[args.kernel]),
+        "select kernel")
     X = workloads.make_x("outlier", M, K, 1, device="cuda")
     g = nv.nvfp4_global_scale(X)
     if args.op == "quantize":
@@ -814,7 +816,7 @@ def run_single_op(args):
         fn(i)
     ms = time_region(torch, fn, args.steps)
     assert nv.nvfp4_device_error() == 0
-    print(json.dumps({"op": args.op, "shape": [M, Nn, K], "ms": ms,
+    print(json.dumps({"op": args.op, "shape": [M, Nn, K], "kernel": args.kernel, "ms": ms,
                       "rate": work / (ms * 1e-3), "unit": unit + "/s"}))
 
 
@@ -836,6 +838,9 @@ def main():
                     default=None,
                     help="time a single kernel on --shape instead of the benchmark step")
     ap.add_argument("--shape", default="8192,8192,8192", help="M,N,K for --op")
+    ap.add_argument("--kernel", choices=["pair", "single"], default="pair",
+                    help="--op: the GEMM kernel for M > 128 (CTA pairs on 256x256 tiles, or "
+                         "the single-CTA kernel)")
     ap.add_argument("--iters", type=int, default=200000, help="--op mma_peak: MMAs per CTA")
     ap.add_argument("--variant", type=int, default=0,
                     help="--op mma_peak: N / accumulator-count / scale-copy variant")

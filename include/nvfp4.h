@@ -388,12 +388,14 @@ NVFP4_API nvfp4_status nvfp4_debug_set_fault_injection(int mode, uint32_t timeou
 
 /*
  * Testing and comparison hook: the GEMM kernel used for M > 128 by
- * nvfp4_gemm and nvfp4_linear from the next call on (process-wide, all
- * devices). kernel = 0: the CTA-pair kernel (default); kernel = 1: the
- * single-CTA kernel (128 x 256 tiles, one SM per tile). The entry points
- * whose epilogues live only in the CTA-pair kernel (bias / re-quantization,
- * LoRA, grouped projections above 128 rows) return UNSUPPORTED_SHAPE while
- * kernel = 1. Errors: INVALID_ARG (kernel not 0 or 1).
+ * nvfp4_gemm, nvfp4_linear and nvfp4_linear_grouped from the next call on
+ * (process-wide, all devices). kernel = 0: CTA pairs on 256 x 256 tiles
+ * (default); kernel = 1: the single-CTA kernel (128 x 256 tiles, one SM per
+ * tile). Both issue the same K = 64 MMAs in K order, so they give the same
+ * bits. While kernel = 1, the entry points whose epilogues live in the
+ * CTA-pair kernel (bias / re-quantization, LoRA, grouped projections above
+ * 128 rows) return UNSUPPORTED_SHAPE. Errors: INVALID_ARG (kernel not 0 or
+ * 1).
  */
 NVFP4_API nvfp4_status nvfp4_debug_select_gemm_kernel(int kernel);
 

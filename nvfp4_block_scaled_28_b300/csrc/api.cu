@@ -236,8 +236,7 @@ nvfp4_status nvfp4_gemm(const uint8_t *Aq, const uint8_t *As, const float *g_a, 
         return from_cuda(launch_gemm_skinny(sa, static_cast<cudaStream_t>(stream)));
     }
     GemmArgs a{Aq, As, g_a, Bq, Bs, g_b, M, N, K, static_cast<uint16_t *>(Y), ldy};
-    return from_cuda(gemm_use_pair() ? launch_gemm_pair(a, static_cast<cudaStream_t>(stream))
-                                     : launch_gemm(a, static_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_gemm_plain(a, static_cast<cudaStream_t>(stream)));
 }
 
 // nvfp4_linear workspace: [g_x, barrier counter | amax partials] header,
@@ -299,7 +298,8 @@ nvfp4_status linear_impl(const void *X, int64_t M, int64_t K, int64_t ldx, const
     if (s != NVFP4_OK) return s;
     if (M == 0 || N == 0) return NVFP4_OK;
     // per-group scales live in the CTA-pair kernel's extended epilogue
-    if (wg.count > 1 && M > kSkinnyMaxM && !gemm_use_pair()) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (wg.count > 1 && M > kSkinnyMaxM && gemm_kernel_choice() == kGemmSingle)
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (g_x != nullptr && !aligned(g_x, 4)) return NVFP4_ERR_MISALIGNED;
     const size_t need = nvfp4_linear_workspace_bytes(M, N, K, mode);
     if (workspace_bytes < need) return NVFP4_ERR_WORKSPACE_TOO_SMALL;
@@ -335,7 +335,7 @@ nvfp4_status linear_impl(const void *X, int64_t M, int64_t K, int64_t ldx, const
     }
     GemmArgs a{xq, xs, g_x, Wq, Ws, g_w, M, N, K, static_cast<uint16_t *>(Y), ldy};
     a.groups = wg;
-    return from_cuda(gemm_use_pair() ? launch_gemm_pair(a, st) : launch_gemm(a, st));
+    return from_cuda(launch_gemm_plain(a, st));
 }
 
 }  // namespace
@@ -390,7 +390,8 @@ nvfp4_status nvfp4_linear_lora(const void *X, int64_t M, int64_t K, int64_t ldx,
     if (!std::isfinite(lora_scale)) return NVFP4_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return NVFP4_OK;
     // the up projection rides in the CTA-pair kernel, the one used above 128 rows
-    if (M <= kSkinnyMaxM || !gemm_use_pair()) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (M <= kSkinnyMaxM || gemm_kernel_choice() == kGemmSingle)
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (M * (K / 16) >= kMaxBlocks) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (lora_A == nullptr || lora_B == nullptr) return NVFP4_ERR_INVALID_ARG;
     if (!aligned(lora_A, 16) || !aligned(lora_B, 16)) return NVFP4_ERR_MISALIGNED;
@@ -444,7 +445,8 @@ nvfp4_status nvfp4_linear_bias_requant(const void *X, int64_t M, int64_t K, int6
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (M == 0 || N == 0) return NVFP4_OK;
     // the epilogue lives in the CTA-pair kernel, the one used above 128 rows
-    if (M <= kSkinnyMaxM || !gemm_use_pair()) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (M <= kSkinnyMaxM || gemm_kernel_choice() == kGemmSingle)
+        return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (M * (K / 16) >= kMaxBlocks || M * (N / 16) >= kMaxBlocks)
         return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (!Wq || !Ws || !g_w) return NVFP4_ERR_INVALID_ARG;
@@ -487,8 +489,8 @@ nvfp4_status nvfp4_device_error(int clear) {
 }
 
 nvfp4_status nvfp4_debug_select_gemm_kernel(int kernel) {
-    if (kernel != 0 && kernel != 1) return NVFP4_ERR_INVALID_ARG;
-    debug_state().single_cta_gemm = kernel;
+    if (kernel != kGemmPair && kernel != kGemmSingle) return NVFP4_ERR_INVALID_ARG;
+    debug_state().gemm_kernel = kernel;
     return NVFP4_OK;
 }
 

@@ -573,7 +573,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int gemm_use_pair() { return debug_state().single_cta_gemm ? 0 : 1; }
+int gemm_kernel_choice() { return debug_state().gemm_kernel; }
+
+cudaError_t launch_gemm_plain(const GemmArgs &a, cudaStream_t st) {
+    return gemm_kernel_choice() == kGemmSingle ? launch_gemm(a, st) : launch_gemm_pair(a, st);
+}
 
 cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;

@@ -132,12 +132,16 @@ cudaError_t launch_quantize_lora(const uint16_t *X, int64_t rows, int64_t K, int
                                  float *part, uint16_t *Lp, cudaStream_t st);
 size_t lora_partial_bytes(int64_t rows, int64_t r);
 
+// Single-CTA kernel, 128 x 256 tiles (plain epilogue only).
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st);
-// The same GEMM on CTA pairs (tcgen05 cta_group::2), 256 x 256 tiles.
+// CTA pairs (tcgen05 cta_group::2), 256 x 256 tiles: every epilogue
+// extension (bias, re-quantization, LoRA stage, weight groups).
 cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st);
-// Kernel for M > 128: 1 = CTA pairs (default), 0 = single-CTA tiles
-// (selected by nvfp4_debug_select_gemm_kernel, for comparison).
-int gemm_use_pair();
+// Kernel for plain and grouped GEMMs with M > 128 (nvfp4_debug_select_gemm_kernel).
+enum GemmKernel { kGemmPair = 0, kGemmSingle = 1 };
+int gemm_kernel_choice();
+// The plain / grouped GEMM through the selected kernel.
+cudaError_t launch_gemm_plain(const GemmArgs &a, cudaStream_t st);
 
 // Skinny-M GEMM (Y^T = W X^T, weights as the 128-row MMA operand).
 constexpr int64_t kSkinnyMaxM = 128;       // activation rows it handles
@@ -168,7 +172,7 @@ unsigned int *device_error_word();
 struct DebugState {
     int inject = 0;
     uint64_t timeout_ns = 2000000000ull;
-    int single_cta_gemm = 0;  // 1: the single-CTA GEMM kernel for M > 128
+    int gemm_kernel = 0;  // GemmKernel for plain and grouped GEMMs with M > 128
     int capture_fused_operand = 0;  // 1: the fused decode kernel writes its operand out
 };
 DebugState &debug_state();

@@ -57,3 +57,18 @@ def check_gemm_tolerance(y_bits: np.ndarray, yref_bits: np.ndarray, label: str =
     nz = np.abs(yr) > 0
     max_rel = float(np.max(err[nz] / np.abs(yr[nz]))) if np.any(nz) else 0.0
     return max_rel, floor_only
+
+
+def tile_covering_rows(M: int, step: int, seed: int = 1) -> np.ndarray:
+    """One random row in every `step`-row band of [0, M), plus the first and
+    last row. With step dividing 128 every CTA's 128 accumulator rows of
+    every output tile (whole tiles and the column halves of the partial last
+    wave alike, since each sampled row is checked across all N columns) are
+    sampled; the offset within a band cycles through the four 32-lane TMEM
+    quarters from band to band."""
+    rng = np.random.default_rng(seed)
+    starts = np.arange(0, M, step)
+    quarter = (np.arange(len(starts)) % 4) * 32 if step == 128 else 0
+    within = quarter + rng.integers(0, min(step, 32), len(starts))
+    rows = np.minimum(starts + within, M - 1)
+    return np.unique(np.concatenate([[0, M - 1], rows]))

@@ -165,7 +165,10 @@ def test_mma_peak_probe_argument_checks():
 def test_select_gemm_kernel_checks(lib):
     assert lib.nvfp4_debug_select_gemm_kernel(2) == N.ERR_INVALID_ARG
     assert lib.nvfp4_debug_select_gemm_kernel(-1) == N.ERR_INVALID_ARG
-    assert lib.nvfp4_debug_select_gemm_kernel(0) == N.OK
+    for k in (1, 0):
+        assert lib.nvfp4_debug_select_gemm_kernel(k) == N.OK
+    assert lib.nvfp4_debug_capture_fused_operand(2) == N.ERR_INVALID_ARG
+    assert lib.nvfp4_debug_capture_fused_operand(0) == N.OK
 
 
 def test_linear_bias_requant_argument_checks(lib):

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import bf16_bits, check_gemm_tolerance, sf_rowmajor_to_mma, to_np_u8
+from helpers import bf16_bits, check_gemm_tolerance, sf_rowmajor_to_mma, tile_covering_rows, to_np_u8
 from nvfp4_block_scaled_28_b300 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -149,21 +149,6 @@ def test_fused_skinny_strided_x_and_given_scale(nv, oracle_mod):
     y_u = nv.nvfp4_linear(xd, Wq, Ws, g_w, mode=nv.LINEAR_UNFUSED)
     assert torch.equal(y_f.view(torch.int16), y_u.view(torch.int16))
     check_gemm_tolerance(bf16_bits(y_f), oracle_mod.gemm(xq, xs, gx, wq, ws, gw), "strided")
-
-
-def tile_covering_rows(M: int, step: int, seed: int = 1) -> np.ndarray:
-    """One random row in every `step`-row band of [0, M), plus the first and
-    last row. With step dividing 128 every CTA's 128 accumulator rows of
-    every output tile (whole tiles and the column halves of the partial last
-    wave alike, since each sampled row is checked across all N columns) are
-    sampled; the offset within a band cycles through the four 32-lane TMEM
-    quarters from band to band."""
-    rng = np.random.default_rng(seed)
-    starts = np.arange(0, M, step)
-    quarter = (np.arange(len(starts)) % 4) * 32 if step == 128 else 0
-    within = quarter + rng.integers(0, min(step, 32), len(starts))
-    rows = np.minimum(starts + within, M - 1)
-    return np.unique(np.concatenate([[0, M - 1], rows]))
 
 
 def _full_size_case(nv, oracle_mod, name, M, Nn, step):

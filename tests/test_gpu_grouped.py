@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import bf16_bits, check_gemm_tolerance
+from helpers import bf16_bits, check_gemm_tolerance, tile_covering_rows
 from nvfp4_block_scaled_28_b300 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -80,6 +80,5 @@ def test_grouped_eight_groups(nv, oracle_mod):
 def test_full_size_dit_qkv(nv, oracle_mod):
     """The DiT attention projections: 4096 tokens, 3072 -> 3 x 3072."""
     M = 4096
-    rows = np.unique(np.concatenate([[0, M - 1],
-                                     np.random.default_rng(5).choice(M, 14, replace=False)]))
+    rows = tile_covering_rows(M, 128, seed=5)
     _check(nv, oracle_mod, M, (3072, 3072, 3072), 3072, 0, seed=31, rows=rows)
