@@ -10,21 +10,39 @@
 // Same arithmetic as the large-M kernel (the "nvfp4-difusion" page's block-
 // scaled matmul, section 2); only the roles of the operands are swapped. The
 // regime is bound by streaming the weights from HBM once (N K / 2 bytes of
-// codes plus N K / 16 of scales), so each CTA owns 128 weight rows and
-// streams them through a ring of stages (two 256-deep K chunks per stage
-// when K allows; 3 to 8 stages, as many as fit), X's chunk riding along.
+// codes plus N K / 16 of scales): each 128-row weight tile streams through a
+// ring of stages (two 256-deep K chunks per stage when K allows; 3 to 8
+// stages, as many as fit), X's chunk riding along.
 //
-// FUSED (M <= kSkinnyFusedMaxM, K <= kSkinnyFusedMaxK): no codes of X ever reach
-// HBM. At the
-// start, four quantizer warps read the bfloat16 X, compute g_x when it is not
-// given (the same integer amax and IEEE division as nvfp4_global_scale) and
-// quantize all of X (quant_math.cuh, the bytes of nvfp4_quantize) into a
-// resident shared-memory copy: E2M1 codes in 128-byte-swizzled chunks and
-// E4M3 scales in the tensor-core tile layout. The ring then streams only
-// weights. Every CTA quantizes the same small X (M K / 16 blocks), which
-// overlaps the weight ring filling up while M is a few rows; at M = 8 the
-// 148 CTAs reading and quantizing the same rows already cost more than one
-// small quantize launch, hence the row limit.
+// The weights do not depend on the kernel this one follows (the activation
+// quantizer, launched as its programmatic predecessor), so the producer
+// issues the first stages' weight loads before it waits for that kernel,
+// and the first bytes' HBM latency overlaps the quantizer.
+//
+// Balance (SPLIT = 2, up to 8 activation rows): the 27648 x 5120 FFN-up
+// weight is 216 tiles, one round of 148 plus a partial round of 68, in which
+// 80 SMs would idle and the 68 busy ones cannot draw the HBM bandwidth that
+// 148 do (measured: ~6.1 TB/s in the full round, ~4 TB/s in the partial
+// one). Launched as
+// clusters of two CTAs, every CTA streams whole tiles round robin, and the
+// tiles of the partial last round (when they fit on half the CTAs) are
+// split by K: CTA r of cluster c streams K half r of tail tile c. CTA 1
+// sends its FP32 partial accumulator (128 weight rows x the loaded
+// activation rows) into CTA 0's shared memory (st.shared::cluster +
+// release arrive); CTA 0 adds it to its own (one IEEE addition per
+// element, so the result does not depend on which half finishes first),
+// scales and stores Y.
+//
+// FUSED (M <= kSkinnyFusedMaxM, K <= kSkinnyFusedMaxK): no codes of X ever
+// reach HBM. At the start, the epilogue and quantizer warps read the
+// bfloat16 X, compute g_x when it is not given (the same integer amax and
+// IEEE division as nvfp4_global_scale) and quantize all of X
+// (quant_math.cuh, the bytes of nvfp4_quantize) into a resident
+// shared-memory copy: E2M1 codes in 128-byte-swizzled chunks and E4M3
+// scales in the tensor-core tile layout. The ring then streams only
+// weights. Every CTA quantizes the same small X, which overlaps the ring
+// filling up while M is a few rows; beyond that, one small quantize launch
+// costs less, hence the row limit.
 //
 // Warps: 0 TMA producer, 1 MMA issuer (per K = 64 step its two scale copies
 // to TMEM and the MMA under one elect.sync), 2 TMEM allocator, 3-6
@@ -46,14 +64,16 @@ namespace nvfp4 {
 namespace {
 
 constexpr int SK_BM = 128;                 // weight rows per tile
-constexpr int SK_BK = 256;                 // K per stage
+constexpr int SK_BK = 256;                 // K per chunk
 constexpr int SK_SF_TILE = 512;
 constexpr unsigned kAllLanes = 0xFFFFFFFFu;
 
 // NX: MMA N (64 or 128); XR <= NX: rows of X loaded (or quantized);
-// KC: 256-deep K chunks per pipeline stage (2 when K % 512 == 0: two weight
-// boxes per stage halve the per-stage costs of the ring).
-template <int NX, int XR, bool FUSED, int KC>
+// KC: 256-deep K chunks per pipeline stage (2 when the K range allows: two
+// weight boxes per stage halve the per-stage costs of the ring);
+// SPLIT: 2 = clusters of two CTAs that split the partial last round's
+// tiles by K.
+template <int NX, int XR, bool FUSED, int KC, int SPLIT>
 struct SkCfg {
     static constexpr int W_CHUNK = SK_BM * SK_BK / 2;             // 16 KiB per K chunk
     // X chunks sit XR rows apart; the MMA reads NX >= XR rows from each, so
@@ -64,7 +84,13 @@ struct SkCfg {
     static constexpr int RES_CHUNKS = FUSED ? static_cast<int>(kSkinnyFusedMaxK / SK_BK) : 0;
     static constexpr int XRES_BYTES = RES_CHUNKS * X_CHUNK;
     static constexpr int SFXRES_BYTES = RES_CHUNKS * 2048;       // 4 scale tiles per chunk
-    static constexpr int RING = XRES_BYTES + SFXRES_BYTES;        // ring after the resident X
+    // SPLIT: receive buffer of the partner's partial accumulator of a tail
+    // tile (CTA 0), FP32 [activation row][weight row]
+    static constexpr int NBUF = SPLIT == 1 ? 0 : 1;
+    static constexpr int RECV_ONE = SK_BM * XR * 4;
+    static constexpr int RECV_BYTES = NBUF * RECV_ONE;
+    static constexpr int OFF_RECV = XRES_BYTES + SFXRES_BYTES;
+    static constexpr int RING = OFF_RECV + RECV_BYTES;            // ring after these
     // one stage: weights (KC chunks) and their scales; unfused: X's chunks
     // and scales too
     static constexpr int W_BYTES = KC * W_CHUNK;
@@ -90,11 +116,12 @@ struct SkCfg {
     static constexpr uint32_t SF_COLS = 32 * KC;
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(!FUSED || XR == 8, "the resident X holds 8 rows");
+    static_assert(SPLIT == 1 || SPLIT == 2, "one or two K ranges");
     static_assert(SF_COL + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
     static_assert(STAGES >= 3, "pipeline depth");
     static_assert(SMEM <= 232448, "shared memory budget");
     static_assert(RING % 1024 == 0 && OFF_X % 1024 == 0 && X_CHUNK % 1024 == 0 &&
-                      STAGE % 1024 == 0,
+                      STAGE % 1024 == 0 && OFF_RECV % 1024 == 0,
                   "swizzled tiles need 1024-B alignment");
 };
 
@@ -110,6 +137,7 @@ struct SkParams {
     int64_t ldy;
     int M, N, K;
     int n_tiles;
+    int n_tail;          // SPLIT: tiles of the partial last round split by K (the last n_tail)
     // testing hook (fused): CTA 0 copies the activation operand it quantized
     // into shared memory out to these buffers (codes M x K/2, tile-layout
     // scales with the padding rows of the first 128-row group zeroed)
@@ -128,15 +156,65 @@ struct SkShared {
     uint64_t acc_full;
     uint64_t acc_empty;
     uint64_t drain;
+    uint64_t recv_full;        // SPLIT, CTA 0: the partner's partial has landed
     uint32_t tmem_base;
     volatile uint32_t abort_flag;
     float g_x;                 // fused: activation global scale used by this CTA
     uint32_t amax_part[8];     // fused: per-warp amax of X (bfloat16 bits)
 };
 
+// A CTA's work: whole tiles round robin over the grid, then (SPLIT) one K
+// half of a tail tile. Unit u covers stages kc0 / KC .. + nk of tile nt
+// (kc0 in 256-deep chunks).
+struct SkUnit {
+    int nt, kc0, nk;
+    bool half;
+};
+
+struct SkWork {
+    int n_whole;     // whole tiles of this CTA
+    int nk_whole;    // stages per whole tile
+    int tail;        // tail tile of this CTA's cluster, or -1
+    int tail_kc0;    // its first chunk (this CTA's K half)
+
+    __device__ __forceinline__ int units() const { return n_whole + (tail >= 0 ? 1 : 0); }
+    __device__ __forceinline__ SkUnit unit(int u) const {
+        if (u < n_whole)
+            return {static_cast<int>(blockIdx.x + u * gridDim.x), 0, nk_whole, false};
+        return {tail, tail_kc0, nk_whole / 2, true};
+    }
+};
+
+template <int KC, int SPLIT>
+__device__ __forceinline__ SkWork sk_work(const SkParams &p, int rank) {
+    SkWork w;
+    const int n_full = p.n_tiles - (SPLIT == 2 ? p.n_tail : 0);
+    const int b = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
+    w.n_whole = b < n_full ? (n_full - b + G - 1) / G : 0;
+    w.nk_whole = p.K / (SK_BK * KC);
+    const int cid = b / SPLIT;
+    w.tail = (SPLIT == 2 && cid < p.n_tail) ? n_full + cid : -1;
+    w.tail_kc0 = rank * (p.K / SK_BK / 2);
+    return w;
+}
+
+// Stage g of this CTA's work -> (tile, first 256-deep chunk); false past the end.
+__device__ __forceinline__ bool sk_stage(const SkWork &w, int g, int &nt, int &k0, int kc) {
+    for (int u = 0; u < w.units(); ++u) {
+        const SkUnit un = w.unit(u);
+        if (g < un.nk) {
+            nt = un.nt;
+            k0 = un.kc0 + g * kc;
+            return true;
+        }
+        g -= un.nk;
+    }
+    return false;
+}
+
 template <int STAGES>
 __device__ __forceinline__ bool sk_wait(uint64_t *bar, uint32_t parity, const SkParams &p,
-                                        SkShared<STAGES> &sh) {
+                                        SkShared<STAGES> &sh, bool cluster_acquire = false) {
     int ok = 1;
     if ((threadIdx.x & 31) == 0) {
         const uint32_t a = smem_addr(bar);
@@ -157,7 +235,11 @@ __device__ __forceinline__ bool sk_wait(uint64_t *bar, uint32_t parity, const Sk
             }
         }
     }
-    return __shfl_sync(kAllLanes, ok, 0) != 0;
+    ok = __shfl_sync(kAllLanes, ok, 0);
+    // every lane acquires what the partner CTA released (the phase has
+    // completed, so this probe returns at once)
+    if (ok && cluster_acquire) (void)mbar_try_wait_cluster(smem_addr(bar), parity);
+    return ok != 0;
 }
 
 // Fused path, run by the epilogue and quantizer warps (warps 3 .. 3 + 8,
@@ -251,11 +333,11 @@ __device__ __forceinline__ void quantize_x_resident(const SkParams &p, SkShared<
     __syncwarp();
 }
 
-template <int NX, int XR, bool FUSED, int KC>
-__global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
+template <int NX, int XR, bool FUSED, int KC, int SPLIT>
+__global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC, SPLIT>::THREADS, 1)
     skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                   const SkParams p) {
-    using C = SkCfg<NX, XR, FUSED, KC>;
+    using C = SkCfg<NX, XR, FUSED, KC, SPLIT>;
     constexpr int S = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem_base = reinterpret_cast<uint8_t *>(
@@ -263,11 +345,13 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
     uint8_t *smem = smem_base + C::RING;      // the stage ring
     uint8_t *xres = smem_base;                // fused: resident X codes
     uint8_t *sfxres = smem_base + C::XRES_BYTES;  // fused: resident X scales
+    float *recv = reinterpret_cast<float *>(smem_base + C::OFF_RECV);  // SPLIT, CTA 0
     SkShared<S> &sh = *reinterpret_cast<SkShared<S> *>(smem_base + C::BAR_OFF);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int num_k = p.K / (SK_BK * KC);  // pipeline stages per tile
+    const int rank = SPLIT == 2 ? static_cast<int>(cluster_ctarank()) : 0;
+    const SkWork work = sk_work<KC, SPLIT>(p, rank);
     const int kb4 = p.K / 64;
 
     if (threadIdx.x == 0) {
@@ -279,6 +363,7 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
         mbar_init(&sh.acc_full, 1);
         mbar_init(&sh.acc_empty, C::EPI_WARPS);
         mbar_init(&sh.drain, 1);
+        mbar_init(&sh.recv_full, 32 * C::EPI_WARPS);  // every lane of CTA 1's epilogue
         sh.abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmW);
@@ -290,50 +375,80 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (SPLIT == 2) cluster_sync_all();  // the partner's barriers exist before any remote use
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
-    // set-up overlaps the previous kernel (programmatic dependent launch)
+    // the next kernel may start its own set-up; every role that reads what
+    // the previous kernel wrote (X, its codes and scales, g_x) or writes Y
+    // waits for that kernel first (pdl_wait)
     pdl_launch_dependents();
-    pdl_wait();
 
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
         const uint64_t pol_w = policy_evict_first();  // weights stream through once
         const uint64_t pol_x = policy_evict_last();   // X is re-read by every CTA
         constexpr uint32_t tx = C::W_BYTES + C::SFW_BYTES + C::X_LOAD + C::SFX_BYTES;
-        int g = 0;
-        bool ok = !p.inject;
-        for (int nt = blockIdx.x; ok && nt < p.n_tiles; nt += gridDim.x) {
-            for (int kt = 0; kt < num_k; ++kt, ++g) {
-                const int s = g % S;
-                if (!sk_wait<S>(&sh.empty[s], ((g / S) & 1) ^ 1, p, sh)) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) {
-                    uint8_t *st = smem + s * C::STAGE;
-                    const int k0 = kt * KC;  // first 256-deep chunk of the stage
-                    mbar_arrive_expect_tx(&sh.full[s], tx);
+        int total = 0;
+        for (int u = 0; u < work.units(); ++u) total += work.unit(u).nk;
+        const bool issue = !p.inject;
+        auto load_w = [&](int s, int nt, int k0) {
+            uint8_t *st = smem + s * C::STAGE;
 #pragma unroll
-                    for (int c = 0; c < KC; ++c)
-                        tma_load_2d(st + C::OFF_W + c * C::W_CHUNK, &tmW, &sh.full[s],
-                                    (k0 + c) * (SK_BK / 2), nt * SK_BM, pol_w);
-                    bulk_load(st + C::OFF_SFW,
-                              p.Ws + (static_cast<int64_t>(nt) * kb4 + k0 * 4) * SK_SF_TILE,
-                              C::SFW_BYTES, &sh.full[s], pol_w);
-                    if (!FUSED) {
+            for (int c = 0; c < KC; ++c)
+                tma_load_2d(st + C::OFF_W + c * C::W_CHUNK, &tmW, &sh.full[s],
+                            (k0 + c) * (SK_BK / 2), nt * SK_BM, pol_w);
+            bulk_load(st + C::OFF_SFW, p.Ws + (static_cast<int64_t>(nt) * kb4 + k0 * 4) * SK_SF_TILE,
+                      C::SFW_BYTES, &sh.full[s], pol_w);
+        };
+        auto load_x = [&](int s, int k0) {
+            uint8_t *st = smem + s * C::STAGE;
 #pragma unroll
-                        for (int c = 0; c < KC; ++c)
-                            tma_load_2d(st + C::OFF_X + c * C::X_CHUNK, &tmX, &sh.full[s],
-                                        (k0 + c) * (SK_BK / 2), 0, pol_x);
-                        bulk_load(st + C::OFF_SFX, p.Xs + static_cast<int64_t>(k0) * 4 * SK_SF_TILE,
-                                  C::SFX_BYTES, &sh.full[s], pol_x);
-                    }
-                }
-                __syncwarp();
+            for (int c = 0; c < KC; ++c)
+                tma_load_2d(st + C::OFF_X + c * C::X_CHUNK, &tmX, &sh.full[s],
+                            (k0 + c) * (SK_BK / 2), 0, pol_x);
+            bulk_load(st + C::OFF_SFX, p.Xs + static_cast<int64_t>(k0) * 4 * SK_SF_TILE,
+                      C::SFX_BYTES, &sh.full[s], pol_x);
+        };
+        // the first S stages' weights before waiting for the previous kernel
+        // (the slots are fresh), X's codes and scales after
+        const int pre = issue ? (total < S ? total : S) : 0;
+        if (lane == 0) {
+            for (int g = 0; g < pre; ++g) {
+                int nt, k0;
+                sk_stage(work, g, nt, k0, KC);
+                mbar_arrive_expect_tx(&sh.full[g], tx);
+                load_w(g, nt, k0);
             }
         }
-        if (!ok && !p.inject && lane == 0) {
+        __syncwarp();
+        pdl_wait();
+        if (!FUSED && lane == 0) {
+            for (int g = 0; g < pre; ++g) {
+                int nt, k0;
+                sk_stage(work, g, nt, k0, KC);
+                load_x(g, k0);
+            }
+        }
+        __syncwarp();
+        int g = pre;
+        bool ok = issue;
+        for (; ok && g < total; ++g) {
+            const int s = g % S;
+            if (!sk_wait<S>(&sh.empty[s], ((g / S) & 1) ^ 1, p, sh)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                int nt, k0;
+                sk_stage(work, g, nt, k0, KC);
+                mbar_arrive_expect_tx(&sh.full[s], tx);
+                load_w(s, nt, k0);
+                if (!FUSED) load_x(s, k0);
+            }
+            __syncwarp();
+        }
+        if (!ok && issue && lane == 0) {
+            // let the loads already issued land before the CTA exits
             for (int s = 0; s < S && s < g; ++s) {
                 const int fills = (g - s + S - 1) / S;
                 mbar_wait(&sh.full[s], (fills - 1) & 1, p.timeout_ns);
@@ -342,16 +457,18 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
+        // (reads only shared memory and TMEM, gated by the full barriers)
         constexpr uint32_t idesc = idesc_mxf4nvf4(SK_BM, NX);
-        int g = 0, it = 0;
+        int g = 0;
         bool ok = !FUSED || sk_wait<S>(&sh.xready, 0, p, sh);
-        for (int nt = blockIdx.x; ok && nt < p.n_tiles; nt += gridDim.x, ++it) {
-            if (!sk_wait<S>(&sh.acc_empty, (it & 1) ^ 1, p, sh)) {
+        for (int u = 0; ok && u < work.units(); ++u) {
+            const SkUnit un = work.unit(u);
+            if (!sk_wait<S>(&sh.acc_empty, (u & 1) ^ 1, p, sh)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            for (int kt = 0; kt < num_k; ++kt, ++g) {
+            for (int kt = 0; kt < un.nk; ++kt, ++g) {
                 const int s = g % S;
                 if (!sk_wait<S>(&sh.full[s], (g / S) & 1, p, sh)) {
                     ok = false;
@@ -364,10 +481,11 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
                 const uint32_t sfw_smem = smem_addr(st + C::OFF_SFW);
                 const uint32_t w_smem = smem_addr(st + C::OFF_W);
                 // X and its scales: this stage's chunks, or (fused) the
-                // resident chunks kt * KC ..
-                const uint32_t x_smem = FUSED ? smem_addr(xres + kt * KC * C::X_CHUNK)
+                // resident chunks of the stage's K range
+                const int xc = un.kc0 + kt * KC;
+                const uint32_t x_smem = FUSED ? smem_addr(xres + xc * C::X_CHUNK)
                                               : smem_addr(st + C::OFF_X);
-                const uint32_t sfx_smem = FUSED ? smem_addr(sfxres + kt * KC * 2048)
+                const uint32_t sfx_smem = FUSED ? smem_addr(sfxres + xc * 2048)
                                                 : smem_addr(st + C::OFF_SFX);
                 // per K = 64 step: its two scale tiles, then the MMA, one elect
 #pragma unroll
@@ -392,6 +510,7 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
     } else if (warp == 2) {
         // TMEM allocator only
     } else if (warp < 3 + C::EPI_WARPS) {
+        pdl_wait();  // g_x and X come from the previous kernel; Y may be its input
         // fused: the epilogue warps first help quantize X (idle until the
         // first accumulator is complete anyway)
         if (FUSED) quantize_x_resident<C, S>(p, sh, xres, sfxres);
@@ -416,14 +535,11 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
         }
         // -------------------------------------------------------- epilogue
         const int quarter = warp & 3;
-        int it = 0;
-        for (int nt = blockIdx.x; nt < p.n_tiles; nt += gridDim.x, ++it) {
-            if (!sk_wait<S>(&sh.acc_full, it & 1, p, sh)) break;
+        const int row = quarter * 32 + lane;  // weight row within the tile
+        for (int u = 0; u < work.units(); ++u) {
+            const SkUnit un = work.unit(u);
+            if (!sk_wait<S>(&sh.acc_full, u & 1, p, sh)) break;
             tc_fence_after();
-            // fused: the quantizer warps published g_x in shared memory before
-            // the MMAs this accumulator completion follows
-            const float gx = FUSED ? sh.g_x : *p.g_x;
-            const float alpha = __fmul_rn(gx, p.g_w[weight_group_of(p.groups, nt * SK_BM)]);
             const uint32_t t_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + C::ACC_COL;
             // D[n, m]: lane = weight row n, column = activation row m
             float acc[NX];
@@ -438,7 +554,26 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.acc_empty);
-            const int n = nt * SK_BM + quarter * 32 + lane;
+            if (SPLIT == 2 && un.half) {
+                // a tail tile: CTA 1 hands its K half's partial to CTA 0
+                // ([m][row] in CTA 0's buffer; the buffer is used once)
+                if (rank == 1) {
+                    const uint32_t dst = mapa_shared(smem_addr(recv + row), 0);
+#pragma unroll
+                    for (int m = 0; m < XR; ++m)
+                        st_cluster_u32(dst + m * SK_BM * 4, __float_as_uint(acc[m]));
+                    mbar_arrive_cluster(mapa_shared(smem_addr(&sh.recv_full), 0));
+                    continue;
+                }
+                if (!sk_wait<S>(&sh.recv_full, 0, p, sh, true)) break;
+#pragma unroll
+                for (int m = 0; m < XR; ++m) acc[m] = __fadd_rn(acc[m], recv[m * SK_BM + row]);
+            }
+            // fused: the quantizer warps published g_x in shared memory before
+            // the MMAs this accumulator completion follows
+            const float gx = FUSED ? sh.g_x : *p.g_x;
+            const float alpha = __fmul_rn(gx, p.g_w[weight_group_of(p.groups, un.nt * SK_BM)]);
+            const int n = un.nt * SK_BM + row;
             if (n < p.N) {
 #pragma unroll
                 for (int m = 0; m < XR; ++m) {
@@ -451,24 +586,34 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC>::THREADS, 1)
         }
         __syncwarp();
     } else if (FUSED) {
+        pdl_wait();
         quantize_x_resident<C, S>(p, sh, xres, sfxres);
     }
 
     tc_fence_before();
     __syncthreads();
+    if (SPLIT == 2) cluster_sync_all();  // neither CTA leaves while the other may address it
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
 }
 
-template <int NX, int XR, bool FUSED, int KC>
+// Tiles of the partial last round that a cluster launch splits by K: all of
+// them when they fit on half the SMs, else none.
+int tail_tiles(int64_t n_tiles) {
+    const int64_t G = launch_cfg().num_sms & ~1;
+    const int64_t rem = n_tiles % G;
+    return (rem > 0 && 2 * rem <= G) ? static_cast<int>(rem) : 0;
+}
+
+template <int NX, int XR, bool FUSED, int KC, int SPLIT>
 cudaError_t launch_sk(const SkinnyArgs &a, cudaStream_t st) {
-    using C = SkCfg<NX, XR, FUSED, KC>;
+    using C = SkCfg<NX, XR, FUSED, KC, SPLIT>;
     static bool attr_of[kMaxDevices + 1] = {};
     bool &attr = attr_of[device_slot()];
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(skinny_kernel<NX, XR, FUSED, KC>,
+        cudaError_t e = cudaFuncSetAttribute(skinny_kernel<NX, XR, FUSED, KC, SPLIT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         attr = true;
@@ -498,23 +643,41 @@ cudaError_t launch_sk(const SkinnyArgs &a, cudaStream_t st) {
     p.N = static_cast<int>(a.N);
     p.K = static_cast<int>(a.K);
     p.n_tiles = static_cast<int>((a.N + SK_BM - 1) / SK_BM);
+    p.n_tail = SPLIT == 2 ? tail_tiles(p.n_tiles) : 0;
     p.dbg_xq = FUSED ? a.dbg_xq : nullptr;
     p.dbg_xs = FUSED ? a.dbg_xs : nullptr;
     p.inject = debug_state().inject;
     p.timeout_ns = debug_state().timeout_ns;
     p.err = device_error_word();
     if (p.err == nullptr) return cudaErrorInvalidSymbol;
-    const int slots = launch_cfg().num_sms;
-    const int grid = p.n_tiles < slots ? p.n_tiles : slots;
-    cudaLaunchAttribute pdl = pdl_attribute();
+    // whole tiles round robin over the grid; with SPLIT, one cluster per
+    // tail tile as well
+    const int G = launch_cfg().num_sms & ~(SPLIT - 1);
+    const int n_full = p.n_tiles - p.n_tail;
+    int ctas = n_full < G ? n_full : G;
+    if (2 * p.n_tail > ctas) ctas = 2 * p.n_tail;
+    ctas = (ctas + SPLIT - 1) / SPLIT * SPLIT;
+    cudaLaunchAttribute attrs[2];
+    attrs[0] = pdl_attribute();
+    attrs[1].id = cudaLaunchAttributeClusterDimension;
+    attrs[1].val.clusterDim.x = SPLIT;
+    attrs[1].val.clusterDim.y = 1;
+    attrs[1].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.gridDim = dim3(ctas, 1, 1);
     cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
-    cfg.attrs = &pdl;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, skinny_kernel<NX, XR, FUSED, KC>, tmW, tmX, p);
+    cfg.attrs = attrs;
+    cfg.numAttrs = SPLIT == 2 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, skinny_kernel<NX, XR, FUSED, KC, SPLIT>, tmW, tmX, p);
+}
+
+// Unfused: the activation rows loaded (XR) follow M.
+template <int KC, int SPLIT>
+cudaError_t launch_unfused(const SkinnyArgs &a, cudaStream_t st) {
+    if (a.M <= 32) return launch_sk<64, 32, false, KC, SPLIT>(a, st);
+    return launch_sk<64, 64, false, KC, SPLIT>(a, st);
 }
 
 }  // namespace
@@ -522,18 +685,25 @@ cudaError_t launch_sk(const SkinnyArgs &a, cudaStream_t st) {
 cudaError_t launch_gemm_skinny(const SkinnyArgs &a, cudaStream_t st) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
     if (a.M > kSkinnyMaxM) return cudaErrorInvalidValue;
+    // a tail to split, whose K halves are whole stages of two chunks. Only
+    // for up to 8 activation rows: measured on the 27648 x 5120 weight, the
+    // split saves 1.2 us at M = 1 and 2.7 us at M = 8 but costs 2.5 us at
+    // M = 16 and 32, where a full-grid quantizer precedes the GEMM and the
+    // cluster launch waits for it
+    const bool split = a.M <= 8 && a.K % 1024 == 0 && tail_tiles((a.N + SK_BM - 1) / SK_BM) > 0;
     if (a.fused) {
         if (a.M > kSkinnyFusedMaxM || a.K > kSkinnyFusedMaxK) return cudaErrorInvalidValue;
-        return a.K % 512 == 0 ? launch_sk<64, 8, true, 2>(a, st) : launch_sk<64, 8, true, 1>(a, st);
+        if (split) return launch_sk<64, 8, true, 2, 2>(a, st);
+        return a.K % 512 == 0 ? launch_sk<64, 8, true, 2, 1>(a, st)
+                              : launch_sk<64, 8, true, 1, 1>(a, st);
     }
-    if (a.K % 512 == 0) {
-        if (a.M <= 32) return launch_sk<64, 32, false, 2>(a, st);
-        if (a.M <= 64) return launch_sk<64, 64, false, 2>(a, st);
-        return launch_sk<128, 128, false, 2>(a, st);
+    if (a.M > 64) {
+        // 128 activation rows: a receive buffer would crowd out the ring
+        return a.K % 512 == 0 ? launch_sk<128, 128, false, 2, 1>(a, st)
+                              : launch_sk<128, 128, false, 1, 1>(a, st);
     }
-    if (a.M <= 32) return launch_sk<64, 32, false, 1>(a, st);
-    if (a.M <= 64) return launch_sk<64, 64, false, 1>(a, st);
-    return launch_sk<128, 128, false, 1>(a, st);
+    if (split) return launch_unfused<2, 2>(a, st);
+    return a.K % 512 == 0 ? launch_unfused<2, 1>(a, st) : launch_unfused<1, 1>(a, st);
 }
 
 }  // namespace nvfp4

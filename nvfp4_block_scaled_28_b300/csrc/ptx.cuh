@@ -468,6 +468,26 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                  : "memory");
 }
 
+// Probe of a phase with acquire semantics at cluster scope: data that
+// another CTA of the cluster wrote before its release-arrive is visible.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// 32-bit store into the shared memory of a CTA of the cluster
+// (shared::cluster address from mapa_shared).
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
 // 2-D tiled load into this CTA's shared memory whose bytes are counted on an
 // mbarrier of either CTA of the pair (shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map,
