@@ -60,7 +60,8 @@ typedef enum nvfp4_status {
     NVFP4_ERR_UNSUPPORTED_SHAPE = 3, /* K (or cols) is not a multiple the entry point needs */
     NVFP4_ERR_WORKSPACE_TOO_SMALL = 4,
     NVFP4_ERR_CUDA = 5,              /* a CUDA runtime or driver call failed */
-    NVFP4_ERR_TIMEOUT = 6            /* a bounded wait inside a kernel ran out */
+    NVFP4_ERR_TIMEOUT = 6,           /* a bounded wait inside a kernel ran out */
+    NVFP4_ERR_BOUNDS = 7             /* debug build only: a kernel's bounds check failed */
 } nvfp4_status;
 
 /* Layout of an E4M3 scale tensor of `rows` rows and K/16 scales per row. */
@@ -370,8 +371,12 @@ NVFP4_API nvfp4_status nvfp4_linear_lora(const void *X, int64_t M, int64_t K, in
 NVFP4_API size_t nvfp4_linear_lora_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r);
 
 /*
- * Synchronize the current device, then return NVFP4_ERR_TIMEOUT if any
- * kernel of this library recorded a bounded-wait timeout since the last
+ * Synchronize the current device, then return NVFP4_ERR_BOUNDS if a kernel
+ * of the debug build (libnvfp4_b300_debug.so, compiled with
+ * NVFP4_DEBUG_CHECKS: every index a kernel forms for a global or shared
+ * access is checked against its buffer, and an access that fails is
+ * recorded and skipped) found an index out of bounds, NVFP4_ERR_TIMEOUT if
+ * a kernel recorded a bounded-wait timeout, in both cases since the last
  * clear, NVFP4_ERR_CUDA if the synchronization failed, else NVFP4_OK.
  * clear != 0 resets the device-side word.
  */

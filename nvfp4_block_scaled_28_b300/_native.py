@@ -9,7 +9,11 @@ import ctypes
 import os
 import threading
 
-LIB_NAME = "libnvfp4_b300.so"
+# NVFP4_B300_DEBUG=1 in the environment loads the debug build instead: the same
+# kernels with device-side bounds checks (nvfp4_device_error reports a failed
+# one as ERR_BOUNDS); build.build() compiles both.
+DEBUG = os.environ.get("NVFP4_B300_DEBUG") == "1"
+LIB_NAME = "libnvfp4_b300_debug.so" if DEBUG else "libnvfp4_b300.so"
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), LIB_NAME)
 
 # nvfp4_status
@@ -20,6 +24,7 @@ ERR_UNSUPPORTED_SHAPE = 3
 ERR_WORKSPACE_TOO_SMALL = 4
 ERR_CUDA = 5
 ERR_TIMEOUT = 6
+ERR_BOUNDS = 7
 
 # nvfp4_sf_layout
 SF_ROW_MAJOR = 0

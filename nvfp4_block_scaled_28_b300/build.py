@@ -4,9 +4,15 @@
                        invocation over every ``csrc/*.cu``;
 ``libnvfp4_probe.so``  the measurement library of include/nvfp4_probe.h
                        (the dense FP4 tensor-core peak probe, ``probe/``);
-                       it is not part of the product library.
+                       it is not part of the product library;
+``libnvfp4_b300_debug.so``  the same C ABI and kernels compiled with
+                       NVFP4_DEBUG_CHECKS (and relocatable device code):
+                       every index a kernel forms for a global or shared
+                       access is checked, a failure recorded in the device
+                       error word and the access skipped. Loaded instead of
+                       the product library when NVFP4_B300_DEBUG=1.
 
-Both link the CUDA runtime statically; the driver API is reached at run time
+All link the CUDA runtime statically; the driver API is reached at run time
 through cudaGetDriverEntryPointByVersion, so the libraries load on machines
 without a GPU driver. No fast-math: the quantizer's bytes depend on IEEE
 binary32 division, reciprocal and multiplication.
@@ -34,6 +40,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libnvfp4_b300.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 PROBE_LIB_PATH = os.path.join(PKG_DIR, "libnvfp4_probe.so")
+DEBUG_LIB_PATH = os.path.join(PKG_DIR, "libnvfp4_b300_debug.so")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -101,6 +108,10 @@ def probe_target():
     return Target(PROBE_LIB_PATH, probe_sources())
 
 
+def debug_target():
+    return Target(DEBUG_LIB_PATH, sources(), ["-DNVFP4_DEBUG_CHECKS", "-rdc=true"])
+
+
 def up_to_date() -> bool:
     return product_target().up_to_date()
 
@@ -127,9 +138,10 @@ def _build(t: Target, force: bool, verbose: bool) -> str:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Build the product library (and the probe library beside it)."""
+    """Build the product library, and beside it the probe and debug ones."""
     path = _build(product_target(), force, verbose)
     _build(probe_target(), force, verbose)
+    _build(debug_target(), force, verbose)
     return path
 
 

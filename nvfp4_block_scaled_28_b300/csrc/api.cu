@@ -137,6 +137,7 @@ const char *nvfp4_status_string(int status) {
         case NVFP4_ERR_WORKSPACE_TOO_SMALL: return "NVFP4_ERR_WORKSPACE_TOO_SMALL";
         case NVFP4_ERR_CUDA: return "NVFP4_ERR_CUDA";
         case NVFP4_ERR_TIMEOUT: return "NVFP4_ERR_TIMEOUT";
+        case NVFP4_ERR_BOUNDS: return "NVFP4_ERR_BOUNDS";
         default: return "NVFP4_ERR_UNKNOWN";
     }
 }
@@ -485,6 +486,7 @@ nvfp4_status nvfp4_device_error(int clear) {
         if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess)
             return NVFP4_ERR_CUDA;
     }
+    if (word & kDevErrBounds) return NVFP4_ERR_BOUNDS;
     return (word & kDevErrTimeout) ? NVFP4_ERR_TIMEOUT : NVFP4_OK;
 }
 

@@ -90,7 +90,8 @@ constexpr int EPI_CHUNK = 64;              // output columns per TMA store (128 
 constexpr int EPI_BYTES = 32 * EPI_CHUNK * 2;  // one warp's 32 rows x 64 columns of bfloat16
 constexpr int SMEM_EPI = SMEM_SFB + STAGES * SFB_BYTES;  // 1024-aligned staging, one per warp
 constexpr int SMEM_BAR = SMEM_EPI + kEpiWarps * EPI_BYTES;
-constexpr int SMEM_USED = SMEM_BAR + 256;
+constexpr int SMEM_RTAB = SMEM_BAR + 256;  // re-quantization: 1 / (e4m3(S) g_y) for the 128 S
+constexpr int SMEM_USED = SMEM_RTAB + 128 * 4;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // room to align the base to 1024
 
 static_assert(SF_COL + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
@@ -408,6 +409,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float g_a = *p.g_a;
         const float alpha0 = __fmul_rn(g_a, *p.g_b);
         const uint32_t acc_empty0 = mapa_shared(smem_addr(&sh.acc_empty), 0);
+        // re-quantization: the block multiplier for each of the 128 scale
+        // bytes, filled once by the epilogue warps (the standalone
+        // quantizer's table, the same IEEE operations)
+        float *rtab = reinterpret_cast<float *>(smem + SMEM_RTAB);
+        const float gy = (kEpi && p.Yq != nullptr) ? *p.g_y : 1.0f;
+        if (kEpi && p.Yq != nullptr) {
+            for (int i = threadIdx.x - 32 * kFirstEpiWarp; i < 128; i += 32 * kEpiWarps)
+                rtab[i] = scale_recip(static_cast<uint32_t>(i), gy);
+            asm volatile("bar.sync 2, %0;" ::"n"(32 * kEpiWarps) : "memory");
+        }
         int it = 0;
         for (int t = 0; t < my_units; ++t, ++it) {
             const Unit un = unit_of(pair + t * num_pairs, p);
@@ -482,9 +493,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        *reinterpret_cast<uint4 *>(stage + lane * 128 + ((k ^ (lane & 7)) * 16)) =
-                            make_uint4(packed[c * 32 + 4 * k], packed[c * 32 + 4 * k + 1],
-                                       packed[c * 32 + 4 * k + 2], packed[c * 32 + 4 * k + 3]);
+                        if (NVFP4_CHECK(lane * 128 + ((k ^ (lane & 7)) * 16) + 16 <= EPI_BYTES))
+                            *reinterpret_cast<uint4 *>(stage + lane * 128 +
+                                                       ((k ^ (lane & 7)) * 16)) =
+                                make_uint4(packed[c * 32 + 4 * k], packed[c * 32 + 4 * k + 1],
+                                           packed[c * 32 + 4 * k + 2], packed[c * 32 + 4 * k + 3]);
                     fence_proxy_async_shared();
                     __syncwarp();
                     if (lane == 0) {
@@ -494,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else if (row < p.M) {
                 uint16_t *yrow = p.Y + static_cast<int64_t>(row) * p.ldy;
-                if (p.y_vec && n0 + 128 <= p.N) {
+                if (p.y_vec && n0 + 128 <= p.N && NVFP4_CHECK(n0 >= 0)) {
                     uint4 *dst = reinterpret_cast<uint4 *>(yrow + n0);
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
@@ -518,17 +531,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // scales go straight to the tile layout (4 consecutive blocks
                 // = one aligned 32-bit word), 0 on padding rows M .. M
                 // rounded to 128
-                const float gy = *p.g_y;
                 uint32_t code[16];
                 uint32_t sw[2] = {0u, 0u};
 #pragma unroll
                 for (int b = 0; b < 8; ++b) {
-                    const uint32_t S = quantize16(
+                    const uint32_t S = quantize16_tab(
                         make_uint4(packed[8 * b], packed[8 * b + 1], packed[8 * b + 2],
                                    packed[8 * b + 3]),
                         make_uint4(packed[8 * b + 4], packed[8 * b + 5], packed[8 * b + 6],
                                    packed[8 * b + 7]),
-                        gy, code[2 * b], code[2 * b + 1]);
+                        gy, rtab, code[2 * b], code[2 * b + 1]);
                     sw[b >> 2] |= S << (8 * (b & 3));
                 }
                 uint8_t *stage = smem + SMEM_EPI + (warp - kFirstEpiWarp) * EPI_BYTES;
@@ -536,8 +548,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4 *>(stage + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) =
-                        make_uint4(code[4 * j], code[4 * j + 1], code[4 * j + 2], code[4 * j + 3]);
+                    if (NVFP4_CHECK(lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16) + 16 <= EPI_BYTES))
+                        *reinterpret_cast<uint4 *>(stage + lane * 64 +
+                                                   ((j ^ ((lane >> 1) & 3)) * 16)) =
+                            make_uint4(code[4 * j], code[4 * j + 1], code[4 * j + 2],
+                                       code[4 * j + 3]);
                 fence_proxy_async_shared();
                 __syncwarp();
                 if (lane == 0) {
@@ -553,7 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int64_t off =
                             ((static_cast<int64_t>(row >> 7) * kb4y + (kb >> 2)) << 9) +
                             ((row & 31) << 4) + (((row & 127) >> 5) << 2);
-                        *reinterpret_cast<uint32_t *>(p.Ys + off) = row < p.M ? sw[h2] : 0u;
+                        if (NVFP4_CHECK(off + 4 <= rows_pad * (p.N / 16)))
+                            *reinterpret_cast<uint32_t *>(p.Ys + off) = row < p.M ? sw[h2] : 0u;
                     }
                 }
             }

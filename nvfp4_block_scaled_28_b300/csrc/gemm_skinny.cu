@@ -320,11 +320,11 @@ __device__ __forceinline__ void quantize_x_resident(const SkParams &p, SkShared<
             uint32_t lo, hi;
             const uint32_t Sb = quantize16(v0[u], v1[u], gx, lo, hi);
             const int chunk = kb >> 4, kbc = kb & 15, piece = kbc >> 1;
-            *reinterpret_cast<uint2 *>(xres + chunk * C::X_CHUNK + r * 128 +
-                                       ((piece ^ (r & 7)) << 4) + (kbc & 1) * 8) =
-                make_uint2(lo, hi);
-            sfxres[(kb >> 2) * SK_SF_TILE + (r & 31) * 16 + (r >> 5) * 4 + (kb & 3)] =
-                static_cast<uint8_t>(Sb);
+            const int xoff = chunk * C::X_CHUNK + r * 128 + ((piece ^ (r & 7)) << 4) + (kbc & 1) * 8;
+            const int soff = (kb >> 2) * SK_SF_TILE + (r & 31) * 16 + (r >> 5) * 4 + (kb & 3);
+            if (NVFP4_CHECK(xoff + 8 <= C::XRES_BYTES && r * 128 < C::X_CHUNK))
+                *reinterpret_cast<uint2 *>(xres + xoff) = make_uint2(lo, hi);
+            if (NVFP4_CHECK(soff < C::SFXRES_BYTES)) sfxres[soff] = static_cast<uint8_t>(Sb);
         }
     }
     fence_proxy_async_shared();  // generic-proxy writes -> tensor core reads
@@ -561,13 +561,16 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC, SPLIT>::THREADS, 1)
                     const uint32_t dst = mapa_shared(smem_addr(recv + row), 0);
 #pragma unroll
                     for (int m = 0; m < XR; ++m)
-                        st_cluster_u32(dst + m * SK_BM * 4, __float_as_uint(acc[m]));
+                        if (NVFP4_CHECK((m * SK_BM + row + 1) * 4 <= C::RECV_BYTES))
+                            st_cluster_u32(dst + m * SK_BM * 4, __float_as_uint(acc[m]));
                     mbar_arrive_cluster(mapa_shared(smem_addr(&sh.recv_full), 0));
                     continue;
                 }
                 if (!sk_wait<S>(&sh.recv_full, 0, p, sh, true)) break;
 #pragma unroll
-                for (int m = 0; m < XR; ++m) acc[m] = __fadd_rn(acc[m], recv[m * SK_BM + row]);
+                for (int m = 0; m < XR; ++m)
+                    if (NVFP4_CHECK((m * SK_BM + row + 1) * 4 <= C::RECV_BYTES))
+                        acc[m] = __fadd_rn(acc[m], recv[m * SK_BM + row]);
             }
             // fused: the quantizer warps published g_x in shared memory before
             // the MMAs this accumulator completion follows

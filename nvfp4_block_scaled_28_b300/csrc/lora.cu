@@ -119,12 +119,14 @@ __global__ void __launch_bounds__(32 * kWarps)
             const uint32_t r = p >> 3, piece = p & 7u;
             const bool ok = row0 + r < rows;
             const uint16_t *src = X + (ok ? (row0 + r) * ldx : 0) + ch * 64u + piece * 8u;
-            cp_async16(xs0 + s * C::X_TILE + swz(r, piece), src, ok ? 16u : 0u);
+            if (NVFP4_CHECK(swz(r, piece) + 16u <= C::X_TILE && ch * 64u + piece * 8u + 8u <= K))
+                cp_async16(xs0 + s * C::X_TILE + swz(r, piece), src, ok ? 16u : 0u);
         }
         for (uint32_t p = tid; p < R * 8u; p += 32 * kWarps) {
             const uint32_t j = p >> 3, piece = p & 7u;
-            cp_async16(as0 + s * C::A_TILE + swz(j, piece),
-                       A + static_cast<uint64_t>(j) * K + ch * 64u + piece * 8u, 16u);
+            if (NVFP4_CHECK(swz(j, piece) + 16u <= C::A_TILE && ch * 64u + piece * 8u + 8u <= K))
+                cp_async16(as0 + s * C::A_TILE + swz(j, piece),
+                           A + static_cast<uint64_t>(j) * K + ch * 64u + piece * 8u, 16u);
         }
     };
 #pragma unroll
@@ -159,13 +161,15 @@ __global__ void __launch_bounds__(32 * kWarps)
             uint32_t lo, hi;
             const uint32_t S = quantize16_tab(a, b, g, rtab, lo, hi);
             const uint32_t row = row0 + r;
-            if (row < rows)
+            if (row < rows && NVFP4_CHECK(ch * 32u + blk * 8u + 8u <= K / 2))
                 *reinterpret_cast<uint2 *>(q + static_cast<uint64_t>(row) * (K / 2) + ch * 32u +
                                            blk * 8u) = make_uint2(lo, hi);
             uint32_t w = S << (8u * blk);
             w |= __shfl_xor_sync(0xFFFFFFFFu, w, 1);
             w |= __shfl_xor_sync(0xFFFFFFFFu, w, 2);
-            if (blk == 0) *reinterpret_cast<uint32_t *>(sf + sf_mma_offset(row, ch * 4u, kb4)) = w;
+            const uint64_t soff = sf_mma_offset(row, ch * 4u, kb4);
+            if (blk == 0 && NVFP4_CHECK(soff + 4 <= static_cast<uint64_t>(rows_pad) * (K / 16)))
+                *reinterpret_cast<uint32_t *>(sf + soff) = w;
         }
         // down projection: this warp's 16 rows times the chunk of A
 #pragma unroll
@@ -186,10 +190,12 @@ __global__ void __launch_bounds__(32 * kWarps)
     // this K range's partial down projection, rows ra and rb
     float *pa = part + (static_cast<uint64_t>(blockIdx.y) * rows_pad + ra) * R;
     float *pb = pa + 8 * R;
+    if (NVFP4_CHECK(ra + 8 < rows_pad)) {  // rows ra and ra + 8 of this range's partials
 #pragma unroll
-    for (int n = 0; n < R / 8; ++n) {
-        *reinterpret_cast<float2 *>(pa + n * 8 + 2 * c) = make_float2(acc[n][0], acc[n][1]);
-        *reinterpret_cast<float2 *>(pb + n * 8 + 2 * c) = make_float2(acc[n][2], acc[n][3]);
+        for (int n = 0; n < R / 8; ++n) {
+            *reinterpret_cast<float2 *>(pa + n * 8 + 2 * c) = make_float2(acc[n][0], acc[n][1]);
+            *reinterpret_cast<float2 *>(pb + n * 8 + 2 * c) = make_float2(acc[n][2], acc[n][3]);
+        }
     }
 }
 

@@ -10,8 +10,27 @@
 
 namespace nvfp4 {
 
-// Bit of the device-side error word: a bounded wait ran out.
+// Bits of the device-side error word: a bounded wait ran out; (debug
+// build) an index failed its bounds check.
 constexpr unsigned int kDevErrTimeout = 1u;
+constexpr unsigned int kDevErrBounds = 2u;
+
+// Bounds checks of the debug build (NVFP4_DEBUG_CHECKS, compiled with
+// relocatable device code so that every kernel reaches the library's error
+// word): NVFP4_CHECK(cond) is true when cond holds; otherwise it records
+// kDevErrBounds and is false, and the caller skips the access it guards
+// (never a trap: the kernel runs on, its waits stay bounded). In the
+// product build it is the constant true and cond is not evaluated.
+#ifdef NVFP4_DEBUG_CHECKS
+extern __device__ unsigned int g_device_error;
+__device__ __forceinline__ bool debug_in_bounds(bool ok) {
+    if (!ok) atomicOr(&g_device_error, kDevErrBounds);
+    return ok;
+}
+#define NVFP4_CHECK(cond) (::nvfp4::debug_in_bounds(static_cast<bool>(cond)))
+#else
+#define NVFP4_CHECK(cond) true
+#endif
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

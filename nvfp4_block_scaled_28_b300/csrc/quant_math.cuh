@@ -123,7 +123,7 @@ __device__ __forceinline__ uint32_t quantize16_tab(uint4 a, uint4 b, float g,
                                                    const float *rtab, uint32_t &lo,
                                                    uint32_t &hi) {
     const uint32_t S = block_scale(a, b, g);
-    block_codes16(a, b, rtab[S], lo, hi);
+    block_codes16(a, b, NVFP4_CHECK(S < 128u) ? rtab[S] : 0.0f, lo, hi);
     return S;
 }
 

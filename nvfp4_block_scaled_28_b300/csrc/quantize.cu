@@ -49,7 +49,7 @@ __device__ __forceinline__ void quantize_round(const uint16_t *__restrict__ X, u
         kb[u] = i - row[u] * kbpr;
         va[u] = make_uint4(0, 0, 0, 0);
         vb[u] = va[u];
-        if (i < total) {
+        if (i < total && NVFP4_CHECK(row[u] < total / kbpr && kb[u] < kbpr)) {
             const uint4 *src = reinterpret_cast<const uint4 *>(X + row[u] * ldx + kb[u] * 16ull);
             va[u] = ld_stream(src);
             vb[u] = ld_stream(src + 1);
@@ -63,6 +63,11 @@ __device__ __forceinline__ void quantize_round(const uint16_t *__restrict__ X, u
             S = quantize16_tab(va[u], vb[u], g, rtab, lo, hi);
             *reinterpret_cast<uint2 *>(q + static_cast<uint64_t>(i) * 8) = make_uint2(lo, hi);
         }
+        // the scale buffer holds `total` bytes (row-major) or the tiles of
+        // the rows padded to 128 (tile layout)
+        [[maybe_unused]] const uint64_t sf_end = kLayout == NVFP4_SF_ROW_MAJOR
+                                    ? static_cast<uint64_t>(total)
+                                    : static_cast<uint64_t>((total / kbpr + 127) / 128 * 128) * kbpr;
         const uint32_t end = kLayout == NVFP4_SF_ROW_MAJOR ? total : total_pad;
         const uint64_t off = kLayout == NVFP4_SF_ROW_MAJOR
                                  ? static_cast<uint64_t>(i)
@@ -70,7 +75,7 @@ __device__ __forceinline__ void quantize_round(const uint16_t *__restrict__ X, u
                                        ((row[u] & 31u) << 4) + (((row[u] & 127u) >> 5) << 2) +
                                        (kb[u] & 3u);
         if (!kGather) {
-            if (i < end) sf[off] = static_cast<uint8_t>(S);
+            if (i < end && NVFP4_CHECK(off < sf_end)) sf[off] = static_cast<uint8_t>(S);
             continue;
         }
         const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, S, 1);
@@ -79,14 +84,16 @@ __device__ __forceinline__ void quantize_round(const uint16_t *__restrict__ X, u
         const bool whole = (i & 3u) == 0 && i + 3 < end &&
                            ((reinterpret_cast<uintptr_t>(sf) + off) & 3u) == 0;
         if (whole) {
-            *reinterpret_cast<uint32_t *>(sf + off) = S | (s1 << 8) | (s2 << 16) | (s3 << 24);
+            if (NVFP4_CHECK(off + 3 < sf_end))
+                *reinterpret_cast<uint32_t *>(sf + off) = S | (s1 << 8) | (s2 << 16) | (s3 << 24);
         } else if (i < end) {
             // the lane leading a whole group stored this byte already
             const uint32_t lead = i & ~3u;
             const uint64_t lead_off = off - (i - lead);
             const bool lead_whole = lead + 3 < end &&
                                     ((reinterpret_cast<uintptr_t>(sf) + lead_off) & 3u) == 0;
-            if (!lead_whole || (i & 3u) == 0) sf[off] = static_cast<uint8_t>(S);
+            if ((!lead_whole || (i & 3u) == 0) && NVFP4_CHECK(off < sf_end))
+                sf[off] = static_cast<uint8_t>(S);
         }
     }
 }
@@ -129,7 +136,9 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t *__restri
         for (int u = 0; u < 4; ++u) {
             const uint32_t j = i + u * stride;
             const uint32_t r = div_vpr.div(j), c = j - r * vpr;
-            v[u] = ld_stream(reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull));
+            v[u] = (NVFP4_CHECK(r < rows && c < vpr)
+                        ? ld_stream(reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull))
+                        : make_uint4(0, 0, 0, 0));
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -139,7 +148,9 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t *__restri
     }
     for (; i < total; i += stride) {
         const uint32_t r = div_vpr.div(i), c = i - r * vpr;
-        const uint4 v = ld_stream(reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull));
+        const uint4 v = (NVFP4_CHECK(r < rows && c < vpr)
+                        ? ld_stream(reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull))
+                        : make_uint4(0, 0, 0, 0));
         acc = max_u16x2(acc, max_u16x2(max_u16x2(v.x & m, v.y & m), max_u16x2(v.z & m, v.w & m)));
     }
     uint32_t a = max(acc & 0xFFFFu, acc >> 16);
@@ -181,7 +192,9 @@ __global__ void __launch_bounds__(kThreads) quantize_fused_kernel(
             for (int u = 0; u < 8; ++u) {
                 const uint32_t j = i + u * stride;
                 const uint32_t r = div_vpr.div(j), c = j - r * vpr;
-                v[u] = ld_stream(reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull));
+                v[u] = (NVFP4_CHECK(r < rows && c < vpr)
+                        ? ld_stream(reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull))
+                        : make_uint4(0, 0, 0, 0));
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u)
@@ -190,7 +203,9 @@ __global__ void __launch_bounds__(kThreads) quantize_fused_kernel(
         }
         for (; i < total; i += stride) {
             const uint32_t r = div_vpr.div(i), c = i - r * vpr;
-            const uint4 v = ld_stream(reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull));
+            const uint4 v = (NVFP4_CHECK(r < rows && c < vpr)
+                        ? ld_stream(reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull))
+                        : make_uint4(0, 0, 0, 0));
             acc = max_u16x2(acc,
                             max_u16x2(max_u16x2(v.x & m, v.y & m), max_u16x2(v.z & m, v.w & m)));
         }
@@ -272,7 +287,9 @@ __global__ void __launch_bounds__(kThreads) quantize_small_kernel(
             for (int u = 0; u < 8; ++u) {
                 const uint32_t j = i + u * blockDim.x;
                 const uint32_t r = div_vpr.div(j), c = j - r * vpr;
-                v[u] = *reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull);
+                v[u] = NVFP4_CHECK(r < rows && c < vpr)
+                         ? *reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull)
+                         : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u)
@@ -281,7 +298,9 @@ __global__ void __launch_bounds__(kThreads) quantize_small_kernel(
         }
         for (; i < total; i += blockDim.x) {
             const uint32_t r = div_vpr.div(i), c = i - r * vpr;
-            const uint4 v = *reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull);
+            const uint4 v = NVFP4_CHECK(r < rows && c < vpr)
+                         ? *reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull)
+                         : make_uint4(0, 0, 0, 0);
             acc = max_u16x2(acc,
                             max_u16x2(max_u16x2(v.x & m, v.y & m), max_u16x2(v.z & m, v.w & m)));
         }
@@ -332,8 +351,11 @@ __global__ void __launch_bounds__(kThreads) sf_to_mma_kernel(const uint8_t *__re
          i += gridDim.x * blockDim.x) {
         const uint32_t row = div_kb4.div(i), G = i - row * kb4;
         uint32_t v = 0;
-        if (row < rows) v = *reinterpret_cast<const uint32_t *>(src + static_cast<uint64_t>(i) * 4);
-        *reinterpret_cast<uint32_t *>(dst + sf_mma_offset(row, G * 4, kb4)) = v;
+        if (row < rows && NVFP4_CHECK(static_cast<uint64_t>(i) * 4 + 4 <= uint64_t(rows) * kb4 * 4))
+            v = *reinterpret_cast<const uint32_t *>(src + static_cast<uint64_t>(i) * 4);
+        const uint64_t off = sf_mma_offset(row, G * 4, kb4);
+        if (NVFP4_CHECK(off + 4 <= static_cast<uint64_t>(total) * 4))
+            *reinterpret_cast<uint32_t *>(dst + off) = v;
     }
 }
 

@@ -120,22 +120,27 @@ __global__ void __launch_bounds__(kThreads)
     const uint64_t total = static_cast<uint64_t>(kLayout == NVFP4_SF_ROW_MAJOR ? rows : rows_pad) *
                            kbpr;
     const uint32_t kb4 = kbpr >> 2;
+    const uint64_t sf_end = static_cast<uint64_t>(kLayout == NVFP4_SF_ROW_MAJOR ? rows : rows_pad) *
+                            kbpr;  // bytes of the scale buffer
+    (void)sf_end;
     for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<uint64_t>(gridDim.x) * blockDim.x) {
         const uint32_t row = static_cast<uint32_t>(i / kbpr);
         const uint32_t kb = static_cast<uint32_t>(i - static_cast<uint64_t>(row) * kbpr);
         if (row >= rows) {  // padding rows of the tile layout
-            sf[sf_mma_offset(row, kb, kb4)] = 0;
+            const uint64_t off = sf_mma_offset(row, kb, kb4);
+            if (NVFP4_CHECK(off < sf_end)) sf[off] = 0;
             continue;
         }
+        if (!NVFP4_CHECK(kb < kbpr)) continue;
         const uint4 *src = reinterpret_cast<const uint4 *>(X + row * ldx + kb * 16u);
         const uint4 a = __ldg(src), b = __ldg(src + 1);
         uint32_t lo, hi;
         const uint32_t S = quantize16_select<kRule>(a, b, g, lo, hi);
         *reinterpret_cast<uint2 *>(q + static_cast<uint64_t>(row) * (kbpr * 8u) + kb * 8u) =
             make_uint2(lo, hi);
-        sf[kLayout == NVFP4_SF_ROW_MAJOR ? i : sf_mma_offset(row, kb, kb4)] =
-            static_cast<uint8_t>(S);
+        const uint64_t off = kLayout == NVFP4_SF_ROW_MAJOR ? i : sf_mma_offset(row, kb, kb4);
+        if (NVFP4_CHECK(off < sf_end)) sf[off] = static_cast<uint8_t>(S);
     }
 }
 

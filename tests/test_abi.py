@@ -60,6 +60,19 @@ def test_probe_library_is_separate_and_exports_its_header():
     assert "nvfp4_mma_peak_probe" not in declared_functions()
 
 
+def test_debug_library_exports_the_same_abi():
+    """The bounds-checking debug build (loaded with NVFP4_B300_DEBUG=1) is a
+    separate file with every entry point of include/nvfp4.h."""
+    from nvfp4_block_scaled_28_b300 import build
+    build.build()
+    dbg = ctypes.CDLL(build.DEBUG_LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(dbg, name), name
+    dbg.nvfp4_status_string.restype = ctypes.c_char_p
+    assert dbg.nvfp4_status_string(7).decode() == "NVFP4_ERR_BOUNDS"
+    assert build.DEBUG_LIB_PATH != build.LIB_PATH
+
+
 def test_every_header_is_checked():
     import glob
     assert sorted(os.path.basename(h) for h in glob.glob(os.path.join(ROOT, "include", "*.h"))) \
@@ -69,7 +82,8 @@ def test_every_header_is_checked():
 def test_status_strings(lib):
     for code, name in [(0, "NVFP4_OK"), (1, "NVFP4_ERR_INVALID_ARG"), (2, "NVFP4_ERR_MISALIGNED"),
                        (3, "NVFP4_ERR_UNSUPPORTED_SHAPE"), (4, "NVFP4_ERR_WORKSPACE_TOO_SMALL"),
-                       (5, "NVFP4_ERR_CUDA"), (6, "NVFP4_ERR_TIMEOUT"), (99, "NVFP4_ERR_UNKNOWN")]:
+                       (5, "NVFP4_ERR_CUDA"), (6, "NVFP4_ERR_TIMEOUT"), (7, "NVFP4_ERR_BOUNDS"),
+                       (99, "NVFP4_ERR_UNKNOWN")]:
         assert lib.nvfp4_status_string(code).decode() == name
 
 
