@@ -126,6 +126,7 @@ struct SkCfg {
 };
 
 struct SkParams {
+    const uint8_t *Wq;   // weight codes, N x K/2 (row-major: a tile is one contiguous range)
     const uint8_t *Ws;   // weight scales, 128x4 tile layout
     const uint8_t *Xs;   // activation scales, 128x4 tile layout (unfused)
     const uint16_t *X;   // bfloat16 activation (fused; read for amax when g_x is null)
@@ -419,6 +420,25 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC, SPLIT>::THREADS, 1)
                 mbar_arrive_expect_tx(&sh.full[g], tx);
                 load_w(g, nt, k0);
             }
+            // Then every weight byte of this CTA's units into L2: the ring
+            // holds only S stages, and until the previous kernel completes
+            // (and X is known) no slot is freed; the prefetch keeps HBM busy
+            // across that boundary. A tile's codes (128 rows x K/2) and its
+            // scales are contiguous ranges; a split tile's is fetched by the
+            // cluster's CTA 0. The weights are inputs no kernel writes, so
+            // they may be read before the wait.
+            if (issue) {
+                for (int u = 0; u < work.units(); ++u) {
+                    const SkUnit un = work.unit(u);
+                    if (un.half && rank != 0) continue;
+                    const int64_t row0 = static_cast<int64_t>(un.nt) * SK_BM;
+                    const int64_t rows = p.N - row0 < SK_BM ? p.N - row0 : SK_BM;
+                    bulk_prefetch_l2(p.Wq + row0 * (p.K / 2),
+                                     static_cast<uint32_t>(rows * (p.K / 2)));
+                    bulk_prefetch_l2(p.Ws + static_cast<int64_t>(un.nt) * kb4 * SK_SF_TILE,
+                                     static_cast<uint32_t>(kb4 * SK_SF_TILE));
+                }
+            }
         }
         __syncwarp();
         pdl_wait();
@@ -633,6 +653,7 @@ cudaError_t launch_sk(const SkinnyArgs &a, cudaStream_t st) {
             return cudaErrorInvalidValue;
     }
     SkParams p;
+    p.Wq = a.Wq;
     p.Ws = a.Ws;
     p.Xs = a.Xs;
     p.X = a.X;
