@@ -639,8 +639,8 @@ def extra_rows(torch, nv, D, workloads, peaks):
                    "frac_of_hbm": wbytes / ms / 1e6 / hbm,
                    "TFLOP/s": 2.0 * m * n * dec.K / ms / 1e9}
             if mode_id == 1:
-                row["path"] = ("one kernel, X quantized in shared memory" if m <= 4 else
-                               "unfused sequence (fused mode covers M <= 4)")
+                row["path"] = ("one kernel, X quantized in shared memory" if m <= 8 else
+                               "unfused sequence (fused mode covers M <= 8)")
             out["decode_linear_M%d_%s" % (m, mode_name)] = row
     torch.cuda.synchronize()
     return out

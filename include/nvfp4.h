@@ -200,12 +200,12 @@ NVFP4_API size_t nvfp4_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 typedef enum nvfp4_linear_mode {
     /* nvfp4_quantize into the workspace, then nvfp4_gemm. */
     NVFP4_LINEAR_UNFUSED = 0,
-    /* For M <= 4 and K <= 6144 one kernel does it all: every CTA reads the
+    /* For M <= 8 and K <= 6144 one kernel does it all: every CTA reads the
      * bfloat16 X, computes g_x when it is not given, and quantizes X once
      * into shared memory (same arithmetic, bit-identical output), so X's
      * codes never travel through HBM and no separate quantize launch is
-     * needed. Beyond that every CTA re-quantizing the same rows costs more
-     * than one quantize pass, so this mode runs the unfused sequence. */
+     * needed. Beyond that (the resident operand holds 8 rows of up to 6144
+     * K) this mode runs the unfused sequence. */
     NVFP4_LINEAR_FUSED = 1
 } nvfp4_linear_mode;
 
@@ -225,7 +225,7 @@ typedef enum nvfp4_linear_mode {
  * read (to reuse it, or to check it): the global scale used (fp32 at byte
  * 0; written when g_x is NULL), X's codes (M x K/2 bytes at byte 8448) and
  * their NVFP4_SF_MMA_128x4 scales (at byte 8448 + M*K/2 rounded up to a
- * multiple of 256). The fused mode for M <= 4 leaves nothing there (its
+ * multiple of 256). The fused mode for M <= 8 leaves nothing there (its
  * operand stays in shared memory).
  * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_SHAPE,
  * WORKSPACE_TOO_SMALL, CUDA.
@@ -405,7 +405,7 @@ NVFP4_API nvfp4_status nvfp4_debug_set_fault_injection(int mode, uint32_t timeou
 NVFP4_API nvfp4_status nvfp4_debug_select_gemm_kernel(int kernel);
 
 /*
- * Testing hook for the fused decode mode (NVFP4_LINEAR_FUSED with M <= 4,
+ * Testing hook for the fused decode mode (NVFP4_LINEAR_FUSED with M <= 8,
  * K <= 6144), whose quantized activation otherwise never leaves shared
  * memory: with on = 1, CTA 0 of the fused kernel also writes the codes and
  * tile-layout scales it produced into the workspace, at the offsets where

@@ -326,8 +326,8 @@ nvfp4_status linear_impl(const void *X, int64_t M, int64_t K, int64_t ldx, const
         }
         return from_cuda(launch_gemm_skinny(sa, st));
     }
-    // unfused (and fused beyond 4 rows or K = 6144, where every CTA
-    // re-quantizing X costs more than one quantize pass)
+    // unfused (and fused beyond 8 rows or K = 6144: the resident operand
+    // holds 8 rows of up to 6144 K)
     if (quantize_activation(Xh, M, K, ldx, &g_x, ws, st) != cudaSuccess) return NVFP4_ERR_CUDA;
     if (M <= kSkinnyMaxM) {
         SkinnyArgs sa{Wq, Ws, g_w, xq, xs, nullptr, 0, g_x, M, N, K,

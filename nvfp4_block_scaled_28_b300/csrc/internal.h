@@ -145,7 +145,7 @@ cudaError_t launch_gemm_plain(const GemmArgs &a, cudaStream_t st);
 
 // Skinny-M GEMM (Y^T = W X^T, weights as the 128-row MMA operand).
 constexpr int64_t kSkinnyMaxM = 128;       // activation rows it handles
-constexpr int64_t kSkinnyFusedMaxM = 4;    // ... with in-kernel quantization of X
+constexpr int64_t kSkinnyFusedMaxM = 8;    // ... with in-kernel quantization of X
 constexpr int64_t kSkinnyFusedMaxK = 6144; // ... held resident in shared memory
 struct SkinnyArgs {
     const uint8_t *Wq, *Ws;  // weights: codes (N x K/2), scales (128x4 tile layout)

@@ -177,7 +177,7 @@ def test_lora_pass_workspace(nv, oracle_mod, M, K, r):
     assert nv.nvfp4_device_error() == 0
 
 
-@pytest.mark.parametrize("M,K", [(1, 5120), (4, 5120), (3, 1280), (2, 6144)])
+@pytest.mark.parametrize("M,K", [(1, 5120), (4, 5120), (3, 1280), (2, 6144), (8, 5120), (6, 6144)])
 @pytest.mark.parametrize("given", [False, True])
 def test_fused_decode_operand(nv, oracle_mod, M, K, given):
     """The fused decode kernel quantizes X in shared memory; the testing hook
