@@ -263,9 +263,12 @@ cudaError_t quantize_activation(const uint16_t *Xh, int64_t M, int64_t K, int64_
     if (*g_x != nullptr) return launch_quantize(Xh, M, K, ldx, *g_x, xq, xs, NVFP4_SF_MMA_128x4, st);
     unsigned int *counter = reinterpret_cast<unsigned int *>(ws + 64);
     *g_x = gx_slot;
-    return M * K <= kQuantizeSmallElems
-               ? launch_quantize_small(Xh, M, K, ldx, gx_slot, xq, xs, st)
-               : launch_quantize_fused(Xh, M, K, ldx, partials, counter, gx_slot, xq, xs, st);
+    if (M * K <= kQuantizeSmallElems) return launch_quantize_small(Xh, M, K, ldx, gx_slot, xq, xs, st);
+    if (M * K <= kQuantizeClusterElems) {
+        const cudaError_t e = launch_quantize_cluster(Xh, M, K, ldx, gx_slot, xq, xs, st);
+        if (e != cudaErrorNotSupported) return e;
+    }
+    return launch_quantize_fused(Xh, M, K, ldx, partials, counter, gx_slot, xq, xs, st);
 }
 
 }  // namespace

@@ -66,6 +66,15 @@ constexpr int64_t kQuantizeSmallElems = 64 * 1024;
 cudaError_t launch_quantize_small(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
                                   float *g_out, uint8_t *q, uint8_t *sf, cudaStream_t st);
 
+// The same for a medium X (at most kQuantizeClusterElems elements) in one
+// cluster of kQuantizeClusterCtas CTAs that exchange their partial amax
+// through distributed shared memory. cudaErrorNotSupported (nothing
+// launched) where such a cluster does not fit on the device.
+constexpr int64_t kQuantizeClusterElems = 512 * 1024;
+constexpr int kQuantizeClusterCtas = 16;
+cudaError_t launch_quantize_cluster(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
+                                    float *g_out, uint8_t *q, uint8_t *sf, cudaStream_t st);
+
 // Launch configuration for kernels that take part in programmatic
 // dependent launch chains.
 cudaLaunchAttribute pdl_attribute();

@@ -334,6 +334,92 @@ __global__ void __launch_bounds__(kThreads) quantize_small_kernel(
                                                      div_kbpr, g, rtab, q, sf);
 }
 
+// Dynamic quantization of a medium activation (decode rows beyond the small
+// kernel's reach) by one thread-block cluster: each CTA reduces the amax of
+// its share of X, writes it into slot `rank` of every CTA's shared array
+// (distributed shared memory), and after one cluster barrier every CTA
+// holds all partials, hence the same g (integer max, one IEEE division),
+// without a grid barrier or a zeroed counter. CTA 0 stores g; each CTA then
+// quantizes its share of the blocks (the second read of X hits L2).
+__global__ void __launch_bounds__(kThreads) quantize_cluster_kernel(
+    const uint16_t *__restrict__ X, uint32_t rows, uint32_t rows_pad, uint32_t kbpr, uint64_t ldx,
+    FastDiv div_kbpr, uint32_t vpr, FastDiv div_vpr, float *g_out, uint8_t *__restrict__ q,
+    uint8_t *__restrict__ sf) {
+    __shared__ uint32_t part[kQuantizeClusterCtas];
+    __shared__ float g_sh;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t csize = gridDim.x;  // one cluster
+    pdl_launch_dependents();
+    pdl_wait();  // X may come from the previous kernel
+    {
+        const uint32_t total = rows * vpr;
+        const uint32_t per = (total + csize - 1) / csize;
+        const uint32_t lo = rank * per;
+        const uint32_t hi = lo + per < total ? lo + per : total;
+        const uint32_t m = 0x7FFF7FFFu;
+        uint32_t acc = 0;
+        uint32_t i = lo + threadIdx.x;
+        for (; i + 7 * blockDim.x < hi; i += 8 * blockDim.x) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t j = i + u * blockDim.x;
+                const uint32_t r = div_vpr.div(j), c = j - r * vpr;
+                v[u] = NVFP4_CHECK(r < rows && c < vpr)
+                         ? *reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull)
+                         : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                acc = max_u16x2(acc, max_u16x2(max_u16x2(v[u].x & m, v[u].y & m),
+                                               max_u16x2(v[u].z & m, v[u].w & m)));
+        }
+        for (; i < hi; i += blockDim.x) {
+            const uint32_t r = div_vpr.div(i), c = i - r * vpr;
+            const uint4 v = NVFP4_CHECK(r < rows && c < vpr)
+                         ? *reinterpret_cast<const uint4 *>(X + r * ldx + c * 8ull)
+                         : make_uint4(0, 0, 0, 0);
+            acc = max_u16x2(acc,
+                            max_u16x2(max_u16x2(v.x & m, v.y & m), max_u16x2(v.z & m, v.w & m)));
+        }
+        uint32_t a = max(acc & 0xFFFFu, acc >> 16);
+        a = __reduce_max_sync(0xFFFFFFFFu, a);
+        __shared__ uint32_t warp_max[kThreads / 32];
+        if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = a;
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            uint32_t b = threadIdx.x < kThreads / 32 ? warp_max[threadIdx.x] : 0u;
+            b = __reduce_max_sync(0xFFFFFFFFu, b);
+            // this CTA's partial into slot `rank` of every CTA of the cluster
+            if (threadIdx.x < csize && NVFP4_CHECK(rank < kQuantizeClusterCtas))
+                st_cluster_u32(mapa_shared(smem_addr(&part[rank]), threadIdx.x), b);
+        }
+    }
+    cluster_sync_all();  // every partial is in every CTA's array
+    if (threadIdx.x < 32) {
+        uint32_t b = threadIdx.x < csize ? part[threadIdx.x] : 0u;
+        b = __reduce_max_sync(0xFFFFFFFFu, b);
+        if (threadIdx.x == 0) {
+            const float amax = __uint_as_float(b << 16);
+            g_sh = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+        }
+    }
+    __syncthreads();
+    const float g = g_sh;
+    if (rank == 0 && threadIdx.x == 0) *g_out = g;
+    __shared__ float rtab[128];
+    fill_recip_table(rtab, g);
+    __syncthreads();
+    const uint32_t total = rows * kbpr;
+    const uint32_t total_pad = rows_pad * kbpr;
+    const uint32_t stride = csize * blockDim.x;
+    constexpr int U = 4;
+    for (uint32_t base = rank * blockDim.x + (threadIdx.x & ~31u); base < total_pad;
+         base += U * stride)
+        quantize_round<NVFP4_SF_MMA_128x4, U, false>(X, base, stride, total, total_pad, kbpr, ldx,
+                                                     div_kbpr, g, rtab, q, sf);
+}
+
 // g = amax / (6 * 448), or 1 for an all-zero tensor; in place over the cell.
 __global__ void global_scale_finalize(uint32_t *cell) {
     const float amax = __uint_as_float(*cell << 16);
@@ -435,6 +521,45 @@ cudaError_t launch_quantize_small(const uint16_t *X, int64_t rows, int64_t cols,
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, quantize_small_kernel, X, static_cast<uint32_t>(rows),
+                              rows_pad, kbpr, static_cast<uint64_t>(ldx), FastDiv(kbpr), vpr,
+                              FastDiv(vpr), g_out, q, sf);
+}
+
+cudaError_t launch_quantize_cluster(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
+                                    float *g_out, uint8_t *q, uint8_t *sf, cudaStream_t st) {
+    const uint32_t vpr = static_cast<uint32_t>(cols / 8);
+    const uint32_t kbpr = static_cast<uint32_t>(cols / 16);
+    const uint32_t rows_pad = static_cast<uint32_t>((rows + 127) / 128 * 128);
+    cudaLaunchAttribute attr[2];
+    attr[0] = pdl_attribute();
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = kQuantizeClusterCtas;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.gridDim = dim3(kQuantizeClusterCtas, 1, 1);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    // 0: not yet known; 1: a cluster of 16 fits on this device; -1: it does
+    // not (the cooperative quantizer is used instead)
+    static int fits_of[kMaxDevices + 1] = {};
+    int &fits = fits_of[device_slot()];
+    if (fits == 0) {
+        // 16 CTAs per cluster is beyond the portable 8
+        cudaError_t e = cudaFuncSetAttribute(quantize_cluster_kernel,
+                                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        cudaLaunchConfig_t occ = cfg;  // the cluster shape alone
+        occ.attrs = &attr[1];
+        occ.numAttrs = 1;
+        int n = 0;
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, quantize_cluster_kernel, &occ);
+        if (e != cudaSuccess) (void)cudaGetLastError();
+        fits = (e == cudaSuccess && n >= 1) ? 1 : -1;
+    }
+    if (fits < 0) return cudaErrorNotSupported;
+    return cudaLaunchKernelEx(&cfg, quantize_cluster_kernel, X, static_cast<uint32_t>(rows),
                               rows_pad, kbpr, static_cast<uint64_t>(ldx), FastDiv(kbpr), vpr,
                               FastDiv(vpr), g_out, q, sf);
 }

@@ -7,7 +7,8 @@ leaves in the workspace the global scale it used (fp32 at byte 0), X's codes
 256-byte aligned). Y alone cannot show that these bytes are right: a code of
 -0 and +0, or errors whose products cancel, leave Y unchanged. Each kernel
 that writes them is covered here: the cooperative dynamic quantizer
-(prefill-sized X), the small-X quantizer (decode rows), the quantizer with a
+(prefill-sized X), the one-cluster quantizer (medium X), the small-X
+quantizer (decode rows), the quantizer with a
 given global scale, the LoRA pass, and, through a testing hook, the fused
 decode kernel whose operand otherwise stays in shared memory. Every X
 carries blocks of signed zeros and of tiny negatives that round to code 0x8.
@@ -90,11 +91,13 @@ def _weights(nv, N, K, seed):
     return nv.nvfp4_quantize_weight(workloads.make_w(N, K, seed=seed).cuda(), nv.SF_MMA_128x4)
 
 
-# (M, K): the cooperative dynamic quantizer for X above 64K elements (prefill
-# size included), the small-X quantizer at or below it (decode rows)
+# (M, K): the cooperative dynamic quantizer for X above 512K elements
+# (prefill size included), the one-cluster quantizer from 64K to 512K
+# elements (both ends), the small-X quantizer at or below 64K (decode rows)
 @pytest.mark.parametrize("M,K,kind", [
     (4096, 5120, "outlier"), (300, 768, "token_scaled"), (1000, 1024, "normal"),
     (32, 5120, "outlier"), (8, 5120, "outlier"), (1, 5120, "outlier"), (64, 1024, "normal"),
+    (512, 1024, "outlier"), (513, 1024, "token_scaled"), (65, 1024, "outlier"),
 ])
 def test_linear_workspace_dynamic_scale(nv, oracle_mod, M, K, kind):
     N = 256
