@@ -633,8 +633,9 @@ def extra_rows(torch, nv, D, workloads, peaks):
                 Wq, Ws, gw = wsets[i % 3]
                 _ok(D.linear(Xm, Wq, Ws, gw, Y, None, mode_id, ws), "lin")
 
-            f(0)
-            ms = time_region(torch, f, 30)
+            for i in range(20):  # steady state: the dependent-launch chain primed
+                f(i)
+            ms = time_region(torch, f, 200)
             row = {"ms": ms, "weight_GB/s": wbytes / ms / 1e6,
                    "frac_of_hbm": wbytes / ms / 1e6 / hbm,
                    "TFLOP/s": 2.0 * m * n * dec.K / ms / 1e9}

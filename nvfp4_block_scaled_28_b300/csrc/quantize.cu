@@ -341,7 +341,9 @@ __global__ void __launch_bounds__(kThreads) quantize_small_kernel(
 // holds all partials, hence the same g (integer max, one IEEE division),
 // without a grid barrier or a zeroed counter. CTA 0 stores g; each CTA then
 // quantizes its share of the blocks (the second read of X hits L2).
-__global__ void __launch_bounds__(kThreads) quantize_cluster_kernel(
+constexpr int kClusterThreads = 1024;  // one round of loads per phase at decode sizes
+
+__global__ void __launch_bounds__(kClusterThreads) quantize_cluster_kernel(
     const uint16_t *__restrict__ X, uint32_t rows, uint32_t rows_pad, uint32_t kbpr, uint64_t ldx,
     FastDiv div_kbpr, uint32_t vpr, FastDiv div_vpr, float *g_out, uint8_t *__restrict__ q,
     uint8_t *__restrict__ sf) {
@@ -384,11 +386,11 @@ __global__ void __launch_bounds__(kThreads) quantize_cluster_kernel(
         }
         uint32_t a = max(acc & 0xFFFFu, acc >> 16);
         a = __reduce_max_sync(0xFFFFFFFFu, a);
-        __shared__ uint32_t warp_max[kThreads / 32];
+        __shared__ uint32_t warp_max[kClusterThreads / 32];
         if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = a;
         __syncthreads();
         if (threadIdx.x < 32) {
-            uint32_t b = threadIdx.x < kThreads / 32 ? warp_max[threadIdx.x] : 0u;
+            uint32_t b = threadIdx.x < kClusterThreads / 32 ? warp_max[threadIdx.x] : 0u;
             b = __reduce_max_sync(0xFFFFFFFFu, b);
             // this CTA's partial into slot `rank` of every CTA of the cluster
             if (threadIdx.x < csize && NVFP4_CHECK(rank < kQuantizeClusterCtas))
@@ -537,7 +539,7 @@ cudaError_t launch_quantize_cluster(const uint16_t *X, int64_t rows, int64_t col
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(kClusterThreads, 1, 1);
     cfg.gridDim = dim3(kQuantizeClusterCtas, 1, 1);
     cfg.stream = st;
     cfg.attrs = attr;
