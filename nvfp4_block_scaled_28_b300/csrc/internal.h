@@ -54,8 +54,10 @@ constexpr int kMaxAmaxPartials = 2048;
 
 // Activation quantization with a dynamic global scale g = amax / (6 * 448)
 // in one cooperative launch: amax partials, a grid-wide barrier on
-// `counter` (zeroed by the launcher), then quantization; the second read
-// of X comes from L2 when X fits there.
+// `counter`, then quantization; the second read of X comes from L2 when X
+// fits there. The counter is zeroed by a one-thread kernel launched before
+// it as a programmatic dependent of the preceding kernel (no memset, which
+// would break the launch chain).
 cudaError_t launch_quantize_fused(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
                                   uint32_t *partials, unsigned int *counter, float *g_out,
                                   uint8_t *q, uint8_t *sf, cudaStream_t st);

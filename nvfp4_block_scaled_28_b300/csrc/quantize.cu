@@ -422,6 +422,17 @@ __global__ void __launch_bounds__(kClusterThreads) quantize_cluster_kernel(
                                                      div_kbpr, g, rtab, q, sf);
 }
 
+// Zeroes the cooperative quantizer's barrier counter, as a programmatic
+// dependent of the kernel before it: it may be resident early, and it
+// writes only once that kernel has completed. In the linear layer's launch
+// sequence that kernel is the GEMM, which itself waited for the previous
+// quantizer that used the counter.
+__global__ void counter_reset_kernel(unsigned int *counter) {
+    pdl_launch_dependents();
+    pdl_wait();
+    *counter = 0u;
+}
+
 // g = amax / (6 * 448), or 1 for an all-zero tensor; in place over the cell.
 __global__ void global_scale_finalize(uint32_t *cell) {
     const float amax = __uint_as_float(*cell << 16);
@@ -585,19 +596,23 @@ cudaError_t launch_quantize_fused(const uint16_t *X, int64_t rows, int64_t cols,
     const int need = grid_for(static_cast<uint64_t>(rows_pad) * kbpr, 4);
     if (need < grid) grid = need;
     if (grid > kMaxAmaxPartials) grid = kMaxAmaxPartials;
-    cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(unsigned int), st);
-    if (e != cudaSuccess) return e;
     unsigned int *err = device_error_word();
     if (err == nullptr) return cudaErrorInvalidSymbol;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0] = pdl_attribute();
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(1, 1, 1);
+    cfg.gridDim = dim3(1, 1, 1);
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, counter_reset_kernel, counter);
+    if (e != cudaSuccess) return e;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, quantize_fused_kernel, X, static_cast<uint32_t>(rows),
                               rows_pad, kbpr, static_cast<uint64_t>(ldx), FastDiv(kbpr), vpr,
                               FastDiv(vpr), partials, counter, g_out, q, sf,
