@@ -8,6 +8,8 @@ X -> global scale, dynamic NVFP4 quantization of X, tcgen05 block-scaled
 FP4 GEMM against the NVFP4 weights, bfloat16 out.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+    python bench.py --config tiny|prefill|decode|dit|square [--mode fused] [--steps K]
+    python bench.py --op gemm|quantize|linear|... --shape M,N,K
 
 Prints one JSON line (rank 0). ``value`` is the whole-job TFLOP/s
 (2 M N K per step, summed over ranks, divided by the max-over-ranks time).
@@ -15,7 +17,8 @@ The step's operands are ten times the size of L2. ``roofline`` times the
 GEMM kernel alone; ``rows`` hold the other workloads (standalone quantize,
 prefill, DiT, decode, the extension rows). The ``reference`` arm times the
 CPU oracle (test infrastructure) on a bounded row sample of the same
-workload.
+workload. ``--config`` times nvfp4_linear on every shape of one named
+workload (one JSON line per shape); ``--op`` times one kernel on one shape.
 """
 from __future__ import annotations
 
@@ -821,6 +824,55 @@ def run_single_op(args):
                       "rate": work / (ms * 1e-3), "unit": unit + "/s"}))
 
 
+def run_config(args):
+    """nvfp4_linear (dynamic activation global scale, --mode) on every shape
+    of one named workload (--config tiny|prefill|decode|dit|square), its own
+    activation recipe and seeds; three rotating input sets where they fit in
+    a few GB. One JSON line per shape."""
+    import torch
+
+    import nvfp4_block_scaled_28_b300 as nv
+    from nvfp4_block_scaled_28_b300 import workloads
+
+    lib = nv.load_library()
+    D = Direct(lib, torch.cuda.current_stream().cuda_stream)
+    wl = workloads.WORKLOADS[args.config]
+    mode = nv.LINEAR_FUSED if args.mode == "fused" else nv.LINEAR_UNFUSED
+    peaks = measured_peaks()
+    for n in wl.N:
+        for m in wl.M:
+            K = wl.K
+            nsets = 3 if (m * K * 2 + n * K // 2) * 3 < (4 << 30) else 1
+            sets = []
+            for r in range(nsets):
+                X = workloads.make_x(wl.x_kind, m, K, workloads.x_seed(wl) + 1000 * r + m,
+                                     device="cuda")
+                W = workloads.make_w(n, K, workloads.w_seed(wl) + 1000 * r + n, device="cuda")
+                Wq, Ws, gw = nv.nvfp4_quantize_weight(W, nv.SF_MMA_128x4)
+                del W
+                sets.append((X, Wq, Ws, gw, torch.empty((m, n), dtype=torch.bfloat16,
+                                                        device="cuda")))
+            ws = torch.empty(nv.linear_workspace_bytes(m, n, K, mode), dtype=torch.uint8,
+                             device="cuda")
+
+            def fn(i, sets=sets, ws=ws):
+                X, Wq, Ws, gw, Y = sets[i % len(sets)]
+                _ok(D.linear(X, Wq, Ws, gw, Y, None, mode, ws), "linear")
+
+            for i in range(max(args.warmup, 3)):
+                fn(i)
+            ms = time_region(torch, fn, args.steps)
+            assert nv.nvfp4_device_error() == 0
+            wbytes = n * K // 2 + n * K // 16
+            print(json.dumps({"config": wl.name, "workload": wl.description, "M": m, "N": n,
+                              "K": K, "mode": args.mode, "inputs": "%d rotating sets" % nsets,
+                              "ms": ms, "TFLOP/s": 2.0 * m * n * K / ms / 1e9,
+                              "weight_GB/s": wbytes / ms / 1e6,
+                              "weight_frac_of_hbm": wbytes / ms / 1e6 / peaks["hbm_gbs"]}))
+            del sets, ws
+            torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -839,6 +891,10 @@ def main():
                     default=None,
                     help="time a single kernel on --shape instead of the benchmark step")
     ap.add_argument("--shape", default="8192,8192,8192", help="M,N,K for --op")
+    ap.add_argument("--config", choices=["tiny", "prefill", "decode", "dit", "square"],
+                    default=None,
+                    help="time nvfp4_linear on every shape of one named workload instead of "
+                         "the benchmark step")
     ap.add_argument("--kernel", choices=["pair", "single"], default="pair",
                     help="--op: the GEMM kernel for M > 128 (CTA pairs on 256x256 tiles, or "
                          "the single-CTA kernel)")
@@ -846,10 +902,12 @@ def main():
     ap.add_argument("--variant", type=int, default=0,
                     help="--op mma_peak: N / accumulator-count / scale-copy variant")
     args = ap.parse_args()
-    if args.warmup < 3 and args.op is None:
+    if args.warmup < 3 and args.op is None and args.config is None:
         ap.error("--warmup must be >= 3")
     if args.op is not None:
         run_single_op(args)
+    elif args.config is not None:
+        run_config(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
