@@ -114,7 +114,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // Bounded wait by lane 0 of a converged warp, also giving up once another
-// role has aborted; the verdict is broadcast to the warp.
+// role has aborted; the outcome is broadcast to the warp.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const Params &p,
                                           Shared &sh) {
     int ok = 1;
