@@ -233,6 +233,14 @@ class Direct:
             Wq.shape[0], la.data_ptr(), lb.data_ptr(), r, scale, Y.data_ptr(), Y.stride(0), None,
             ws.data_ptr(), ws.numel(), self.stream)
 
+    def linear_bias_requant_dynamic(self, X, Wq, Ws, gw, bias, Y, gy, Yq, Ys, ws):
+        M, K = X.shape
+        n = Wq.shape[0]
+        return self.lib.nvfp4_linear_bias_requant_dynamic(
+            X.data_ptr(), M, K, X.stride(0), Wq.data_ptr(), Ws.data_ptr(), gw.data_ptr(), n,
+            None if bias is None else bias.data_ptr(), Y.data_ptr(), Y.stride(0), gy.data_ptr(),
+            Yq.data_ptr(), Ys.data_ptr(), None, ws.data_ptr(), ws.numel(), self.stream)
+
     def linear_bias_requant(self, X, Wq, Ws, gw, bias, Y, gy, Yq, Ys, ws):
         M, K = X.shape
         n = Wq.shape[0]
@@ -599,6 +607,21 @@ def extra_rows(torch, nv, D, workloads, peaks):
                                                                     Yq, Ys, ws), "epi"), 20)
     ms_q = time_region(torch, lambda i: _ok(D.linear_bias_requant(Xp, Wq, Ws, gw, bias, None, gy,
                                                                   Yq, Ys, ws), "epi"), 20)
+    # the output's global scale computed from the output: epilogue amax +
+    # quantize of Y, against the unfused dynamic sequence (bias linear, the
+    # global scale of Y, quantize)
+    gyd = torch.empty(1, dtype=torch.float32, device="cuda")
+    _ok(D.linear_bias_requant_dynamic(Xp, Wq, Ws, gw, bias, Y, gyd, Yq, Ys, ws), "dyn")
+    ms_dyn = time_region(torch, lambda i: _ok(D.linear_bias_requant_dynamic(
+        Xp, Wq, Ws, gw, bias, Y, gyd, Yq, Ys, ws), "dyn"), 20)
+
+    def dyn_seq(i):
+        _ok(D.linear_bias_requant(Xp, Wq, Ws, gw, bias, Y, None, None, None, ws), "bias")
+        _ok(D.global_scale(Y, gyd), "g")
+        _ok(D.quantize(Y, gyd, Yq, Ys, nv.SF_MMA_128x4), "q")
+
+    dyn_seq(0)
+    ms_dyn_seq = time_region(torch, dyn_seq, 20)
     out["prefill_linear_4096x5120x5120_epilogue"] = {
         "linear_ms": ms_lin,
         "linear_then_quantize_ms": ms_seq,
@@ -606,6 +629,8 @@ def extra_rows(torch, nv, D, workloads, peaks):
         "bias_requant_fused_no_bf16_y_ms": ms_q,
         "TFLOP/s_fused": fl / ms_epi / 1e9,
         "TFLOP/s_fused_no_bf16_y": fl / ms_q / 1e9,
+        "bias_requant_dynamic_g_y_ms": ms_dyn,
+        "bias_then_global_scale_then_quantize_ms": ms_dyn_seq,
     }
     # F3: the same layer with a rank-32 LoRA correction (down projection in
     # the quantization pass, up projection as bfloat16 steps in the GEMM)

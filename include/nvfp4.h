@@ -338,6 +338,37 @@ NVFP4_API nvfp4_status nvfp4_linear_bias_requant(const void *X, int64_t M, int64
                                                 void *stream);
 
 /*
+ * nvfp4_linear_bias_requant with the output's global scale computed from
+ * the output itself, as the next linear would compute it for its own
+ * activation (the pages' dynamic activation quantization, "nvfp4-difusion"
+ * page, section 2, carried across the chained linears):
+ *   Y   = bf16( acc * g_x * g_w + bias[n] )
+ *   g_y = amax(|Y|) / (6 * 448), or 1 for an all-zero Y     -> *g_y_out
+ *   Yq, Ys = nvfp4_quantize(Y, g_y, NVFP4_SF_MMA_128x4)
+ * All bytes equal nvfp4_linear_bias_requant (Y only, same bias) followed by
+ * nvfp4_global_scale(Y) and nvfp4_quantize(Y, ...). The GEMM epilogue folds
+ * each tile's largest |y| into *g_y_out (used as the amax cell) with atomic
+ * maxima, so no pass over Y computes the amax; a small kernel turns it into
+ * g_y and the quantizer then reads Y back (from L2 when Y fits there).
+ * X, Wq, Ws, g_w, g_x, bias, workspace: as nvfp4_linear_bias_requant.
+ * Y: required, M x N bfloat16 (ldy >= N, ldy % 8 == 0, 16-byte aligned).
+ * g_y_out: device float (4-byte aligned) that receives g_y; its previous
+ * value does not matter.
+ * Yq, Ys: as nvfp4_linear_bias_requant.
+ * Shapes: K % 256 == 0, N % 256 == 0, M > 128.
+ * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_SHAPE,
+ * WORKSPACE_TOO_SMALL, CUDA.
+ */
+NVFP4_API nvfp4_status nvfp4_linear_bias_requant_dynamic(const void *X, int64_t M, int64_t K,
+                                                        int64_t ldx, const uint8_t *Wq,
+                                                        const uint8_t *Ws, const float *g_w,
+                                                        int64_t N, const void *bias, void *Y,
+                                                        int64_t ldy, float *g_y_out, uint8_t *Yq,
+                                                        uint8_t *Ys, const float *g_x,
+                                                        void *workspace, size_t workspace_bytes,
+                                                        void *stream);
+
+/*
  * NVFP4 linear layer with a run-time low-rank (LoRA) correction, the LoRA
  * kept beside the quantized weight ("nvfp4-difusion" page, section 3: a LoRA
  * cannot be merged into NVFP4 codes; its computation is fused with the

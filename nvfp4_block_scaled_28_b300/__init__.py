@@ -25,6 +25,7 @@ from .ops import (  # noqa: F401
     nvfp4_linear,
     nvfp4_linear_noalloc,
     nvfp4_linear_bias_requant,
+    nvfp4_linear_bias_requant_dynamic,
     nvfp4_linear_grouped,
     nvfp4_linear_lora,
     pack_weight_groups,

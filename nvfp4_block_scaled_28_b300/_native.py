@@ -63,6 +63,8 @@ SIGNATURES = {
     "nvfp4_linear_noalloc": (_INT, [_P, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _I64, _P, _P]),
     "nvfp4_linear_bias_requant": (_INT, [_P, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _P, _I64,
                                          _P, _P, _P, _P, _P, _SZ, _P]),
+    "nvfp4_linear_bias_requant_dynamic": (_INT, [_P, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _P,
+                                                 _I64, _P, _P, _P, _P, _P, _SZ, _P]),
     "nvfp4_linear_lora": (_INT, [_P, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _P, _I64,
                                  ctypes.c_float, _P, _I64, _P, _P, _SZ, _P]),
     "nvfp4_linear_lora_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64]),

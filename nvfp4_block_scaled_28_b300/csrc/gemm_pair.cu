@@ -125,6 +125,7 @@ struct Params {
     // bits per element).
     int num_full;
     int num_units;
+    uint32_t *y_amax;    // kMode 2: max |y| of the stored output (rows < M), atomically
     int inject;          // 1: the producers issue nothing (bounded-wait test)
     uint64_t timeout_ns;
     unsigned int *err;   // device error word
@@ -193,9 +194,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
     return __shfl_sync(kAll, ok, 0) != 0;
 }
 
-// kEpi: the bias / re-quantization epilogue (a separate instantiation, so
-// the plain kernel's registers are not spent on it).
-template <bool kEpi>
+// kMode 0: the plain epilogue; 1: the bias / re-quantization / grouped /
+// LoRA epilogue; 2: that, plus the largest |y| of the output folded into
+// p.y_amax. Separate instantiations, so the plainer kernels' registers are
+// not spent on what they do not do.
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
@@ -206,6 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tmL,
                      const __grid_constant__ CUtensorMap tmLB,
                      const __grid_constant__ CUtensorMap tmB64, const Params p) {
+    constexpr bool kEpi = kMode >= 1;
+    constexpr bool kAmax = kMode == 2;
     // tmSA: A scales as rows of 256 B (8 rows per stage); tmSB: B scales as
     // {256 B, rows of a 128-row group, group} (8 rows x 2 groups per stage)
     extern __shared__ uint8_t smem_raw[];
@@ -522,6 +527,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            if (kAmax && p.y_amax != nullptr) {
+                // the largest |y| of this thread's row (bfloat16 magnitude
+                // bits, which order like the values), one atomic per warp;
+                // rows >= M hold the bias only and are not part of Y
+                uint32_t m2 = 0;
+                if (row < p.M) {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) m2 = max_u16x2(m2, packed[i] & 0x7FFF7FFFu);
+                }
+                uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+                m = __reduce_max_sync(kAll, m);
+                if (lane == 0 && m != 0u) atomicMax(p.y_amax, m);
+            }
             if (kEpi && p.Yq != nullptr) {
                 // re-quantize this thread's 128 bfloat16 values (8 blocks of
                 // 16) for the next layer, after the Y stores are in flight.
@@ -600,10 +618,13 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     static int max_clusters_of[kMaxDevices + 1] = {};  // 0: not yet queried
     int &max_clusters = max_clusters_of[device_slot()];
     if (max_clusters <= 0) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<false>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<0>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(gemm_pair_kernel<true>,
+        e = cudaFuncSetAttribute(gemm_pair_kernel<1>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(gemm_pair_kernel<2>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
         if (e != cudaSuccess) return e;
         max_clusters = launch_cfg().num_sms / 2;
@@ -619,7 +640,7 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<false>, &cfg) == cudaSuccess && n > 0 &&
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<0>, &cfg) == cudaSuccess && n > 0 &&
             n < max_clusters)
             max_clusters = n;
     }
@@ -685,7 +706,7 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     // the partial last wave's tiles as column halves, when they then fit in
     // one wave (plain epilogue only)
     const bool epi = !store_y || a.bias != nullptr || a.Yq != nullptr || a.groups.count > 1 ||
-                     a.lora_Lp != nullptr;
+                     a.lora_Lp != nullptr || a.y_amax != nullptr;
     p.num_full = p.num_tiles;
     {
         const int R = p.num_tiles % max_clusters;
@@ -693,6 +714,7 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     }
     p.num_units = p.num_full + 2 * (p.num_tiles - p.num_full);
     p.lora_r = a.lora_Lp != nullptr ? static_cast<int>(a.lora_r) : 0;
+    p.y_amax = a.y_amax;
     p.inject = debug_state().inject;
     p.timeout_ns = debug_state().timeout_ns;
     p.err = device_error_word();
@@ -711,10 +733,14 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = epi ? cudaLaunchKernelEx(&cfg, gemm_pair_kernel<true>, tmA, tmB, tmSA, tmSB,
-                                             tmY, tmYq, tmL, tmLB, tmB64, p)
-                        : cudaLaunchKernelEx(&cfg, gemm_pair_kernel<false>, tmA, tmB, tmSA, tmSB,
-                                             tmY, tmYq, tmL, tmLB, tmB64, p);
+    cudaError_t e =
+        a.y_amax != nullptr
+            ? cudaLaunchKernelEx(&cfg, gemm_pair_kernel<2>, tmA, tmB, tmSA, tmSB, tmY, tmYq, tmL,
+                                 tmLB, tmB64, p)
+        : epi ? cudaLaunchKernelEx(&cfg, gemm_pair_kernel<1>, tmA, tmB, tmSA, tmSB, tmY, tmYq, tmL,
+                                   tmLB, tmB64, p)
+              : cudaLaunchKernelEx(&cfg, gemm_pair_kernel<0>, tmA, tmB, tmSA, tmSB, tmY, tmYq, tmL,
+                                   tmLB, tmB64, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

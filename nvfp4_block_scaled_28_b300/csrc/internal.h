@@ -77,6 +77,16 @@ constexpr int kQuantizeClusterCtas = 16;
 cudaError_t launch_quantize_cluster(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
                                     float *g_out, uint8_t *q, uint8_t *sf, cudaStream_t st);
 
+// A 32-bit cell zeroed once the preceding kernel has completed (a
+// programmatic dependent launch: the chain of dependent launches stays
+// unbroken, as a memset would break it).
+cudaError_t launch_cell_reset(uint32_t *cell, cudaStream_t st);
+
+// The amax cell (bfloat16 magnitude bits) turned in place into the global
+// scale g = amax / (6 * 448), or 1 for 0, once the preceding kernel has
+// completed (a programmatic dependent launch).
+cudaError_t launch_amax_cell_to_scale(uint32_t *cell, cudaStream_t st);
+
 // Launch configuration for kernels that take part in programmatic
 // dependent launch chains.
 cudaLaunchAttribute pdl_attribute();
@@ -131,6 +141,9 @@ struct GemmArgs {
     const uint16_t *lora_Lp = nullptr;
     const uint16_t *lora_B = nullptr;
     int64_t lora_r = 0;
+    // The largest |y| of the stored bfloat16 output (rows < M), folded into
+    // *y_amax (bfloat16 magnitude bits, zeroed beforehand) by atomic maxima
+    uint32_t *y_amax = nullptr;
 };
 
 // The fused pass for a LoRA linear: NVFP4 codes + tile-layout scales of X

@@ -422,15 +422,25 @@ __global__ void __launch_bounds__(kClusterThreads) quantize_cluster_kernel(
                                                      div_kbpr, g, rtab, q, sf);
 }
 
-// Zeroes the cooperative quantizer's barrier counter, as a programmatic
-// dependent of the kernel before it: it may be resident early, and it
-// writes only once that kernel has completed. In the linear layer's launch
-// sequence that kernel is the GEMM, which itself waited for the previous
-// quantizer that used the counter.
+// Zeroes a 32-bit cell (the cooperative quantizer's barrier counter, an
+// amax cell), as a programmatic dependent of the kernel before it: it may
+// be resident early, and it writes only once that kernel has completed. In
+// the linear layer's launch sequence that kernel is the one before this
+// call's first use of the cell, which itself waited for the previous use.
 __global__ void counter_reset_kernel(unsigned int *counter) {
     pdl_launch_dependents();
     pdl_wait();
     *counter = 0u;
+}
+
+// An amax cell (bfloat16 magnitude bits) into the global scale, in place,
+// once the kernel that accumulated it has completed.
+__global__ void amax_cell_to_scale_kernel(uint32_t *cell) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const float amax = __uint_as_float(*cell << 16);
+    const float g = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+    *reinterpret_cast<float *>(cell) = g;
 }
 
 // g = amax / (6 * 448), or 1 for an all-zero tensor; in place over the cell.
@@ -538,6 +548,28 @@ cudaError_t launch_quantize_small(const uint16_t *X, int64_t rows, int64_t cols,
                               FastDiv(vpr), g_out, q, sf);
 }
 
+cudaError_t launch_cell_reset(uint32_t *cell, cudaStream_t st) {
+    cudaLaunchAttribute attr = pdl_attribute();
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(1, 1, 1);
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.stream = st;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, counter_reset_kernel, reinterpret_cast<unsigned int *>(cell));
+}
+
+cudaError_t launch_amax_cell_to_scale(uint32_t *cell, cudaStream_t st) {
+    cudaLaunchAttribute attr = pdl_attribute();
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(1, 1, 1);
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.stream = st;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, amax_cell_to_scale_kernel, cell);
+}
+
 cudaError_t launch_quantize_cluster(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
                                     float *g_out, uint8_t *q, uint8_t *sf, cudaStream_t st) {
     const uint32_t vpr = static_cast<uint32_t>(cols / 8);
@@ -598,20 +630,17 @@ cudaError_t launch_quantize_fused(const uint16_t *X, int64_t rows, int64_t cols,
     if (grid > kMaxAmaxPartials) grid = kMaxAmaxPartials;
     unsigned int *err = device_error_word();
     if (err == nullptr) return cudaErrorInvalidSymbol;
+    cudaError_t e = launch_cell_reset(counter, st);
+    if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[2];
     attr[0] = pdl_attribute();
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(1, 1, 1);
-    cfg.gridDim = dim3(1, 1, 1);
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, counter_reset_kernel, counter);
-    if (e != cudaSuccess) return e;
     attr[1].id = cudaLaunchAttributeCooperative;
     attr[1].val.cooperative = 1;
+    cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.gridDim = dim3(grid, 1, 1);
+    cfg.stream = st;
+    cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, quantize_fused_kernel, X, static_cast<uint32_t>(rows),
                               rows_pad, kbpr, static_cast<uint64_t>(ldx), FastDiv(kbpr), vpr,

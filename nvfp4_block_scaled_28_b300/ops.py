@@ -381,6 +381,53 @@ def nvfp4_linear_bias_requant(X: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tenso
     return Y, Yq, Ys
 
 
+def nvfp4_linear_bias_requant_dynamic(X: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor,
+                                      g_w: torch.Tensor, bias: torch.Tensor | None = None,
+                                      g_x: torch.Tensor | None = None,
+                                      Y: torch.Tensor | None = None,
+                                      g_y: torch.Tensor | None = None,
+                                      Yq: torch.Tensor | None = None,
+                                      Ys: torch.Tensor | None = None,
+                                      workspace: torch.Tensor | None = None):
+    """nvfp4_linear_bias_requant with the output's global scale computed from
+    the output (the GEMM epilogue folds max |y| into g_y). Returns
+    (Y, g_y, Yq, Ys)."""
+    _check_bf16_2d(X, "X")
+    M, K = X.shape
+    Nn = Wq.shape[0]
+    _check_codes(Wq, Nn, K, "Wq")
+    _check_scales(Ws, Nn, K, SF_MMA_128x4, "Ws")
+    _check_g(g_w, "g_w")
+    if g_x is not None:
+        _check_g(g_x, "g_x")
+    if bias is not None:
+        _require(bias.dtype == torch.bfloat16 and tuple(bias.shape) == (Nn,)
+                 and bias.is_contiguous(), "bias must be a contiguous bfloat16 vector of %d" % Nn)
+    _check_cuda(X, Wq, Ws, g_w, g_x, bias, Y, g_y, Yq, Ys, workspace)
+    if Y is None:
+        Y = torch.empty((M, Nn), dtype=torch.bfloat16, device=X.device)
+    _check_bf16_2d(Y, "Y")
+    _require(tuple(Y.shape) == (M, Nn), "Y must have shape (%d, %d)" % (M, Nn))
+    if g_y is None:
+        g_y = torch.empty(1, dtype=torch.float32, device=X.device)
+    _check_g(g_y, "g_y")
+    if Yq is None:
+        Yq = torch.empty((M, Nn // 2), dtype=torch.uint8, device=X.device)
+    if Ys is None:
+        Ys = torch.empty(sf_shape(M, Nn, SF_MMA_128x4), dtype=torch.uint8, device=X.device)
+    _check_codes(Yq, M, Nn, "Yq")
+    _check_scales(Ys, M, Nn, SF_MMA_128x4, "Ys")
+    need = linear_workspace_bytes(M, Nn, K, LINEAR_UNFUSED)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=X.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    N.check("nvfp4_linear_bias_requant_dynamic", N.load().nvfp4_linear_bias_requant_dynamic(
+        _ptr(X), M, K, X.stride(0), _ptr(Wq), _ptr(Ws), _ptr(g_w), Nn, _ptr(bias), _ptr(Y),
+        Y.stride(0), _ptr(g_y), _ptr(Yq), _ptr(Ys), _ptr(g_x), _ptr(workspace), ws_bytes,
+        _stream()))
+    return Y, g_y, Yq, Ys
+
+
 def nvfp4_device_error(clear: bool = True) -> int:
     """Synchronize and return the device-side status (OK or ERR_TIMEOUT)."""
     return int(N.load().nvfp4_device_error(1 if clear else 0))

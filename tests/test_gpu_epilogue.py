@@ -163,3 +163,72 @@ def test_full_size_prefill_bias_requant(nv, oracle_mod):
     check_gemm_tolerance(y_bits[rows], y_ref, "prefill bias")
     _check_requant(oracle_mod, y_bits, g_y, Yq, Ys, "prefill requant")
     assert nv.nvfp4_device_error() == 0
+
+
+def _f32_bits(v) -> int:
+    return int(np.array([v], np.float32).view(np.uint32)[0])
+
+
+@pytest.mark.parametrize("M,N,K", EPI_SHAPES)
+def test_dynamic_requant_matches_oracle(nv, oracle_mod, M, N, K):
+    """The output's global scale computed from the output (the epilogue's
+    atomic amax): g_y is the oracle's global scale of the GPU's Y, bit for
+    bit, and the codes and scales are the oracle's quantization under it."""
+    c = _case(nv, oracle_mod, M, N, K, seed=M * 5 + N + 3 * K)
+    xq, xs, gx, wq, ws, gw = c["ops"]
+    y_ref = oracle_mod.gemm(xq, xs, gx, wq, ws, gw, bias=c["bb"])
+    Wq, Ws, g_w = c["W"]
+    g_y = torch.full((1,), 123.0, dtype=torch.float32, device="cuda")  # stale value
+    Y, g_y, Yq, Ys = nv.nvfp4_linear_bias_requant_dynamic(c["x"].cuda(), Wq, Ws, g_w,
+                                                          bias=c["b"].cuda(), g_y=g_y)
+    torch.cuda.synchronize()
+    y_bits = bf16_bits(Y)
+    check_gemm_tolerance(y_bits, y_ref, "dynamic bias %dx%dx%d" % (M, N, K))
+    g_expect = oracle_mod.global_scale(y_bits)
+    assert _f32_bits(g_y.item()) == _f32_bits(g_expect), "g_y %r vs %r" % (g_y.item(), g_expect)
+    _check_requant(oracle_mod, y_bits, g_expect, Yq, Ys, "dynamic requant %dx%dx%d" % (M, N, K))
+    assert nv.nvfp4_device_error() == 0
+
+
+def test_dynamic_requant_equals_unfused_sequence(nv):
+    """Bytes equal nvfp4_linear_bias_requant (Y only) + nvfp4_global_scale(Y)
+    + nvfp4_quantize(Y), on the prefill shape, twice in a row on one
+    workspace (the amax cell is zeroed by every call)."""
+    M, N, K = 4096, 5120, 5120
+    w = workloads.make_w(N, K, seed=31)
+    Wq, Ws, g_w = nv.nvfp4_quantize_weight(w.cuda(), nv.SF_MMA_128x4)
+    b = workloads.make_bias(N, seed=32).cuda()
+    ws = torch.empty(nv.linear_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+    for i, kind in enumerate(["outlier", "token_scaled"]):
+        x = workloads.make_x(kind, M, K, seed=40 + i).cuda()
+        Y, g_y, Yq, Ys = nv.nvfp4_linear_bias_requant_dynamic(x, Wq, Ws, g_w, bias=b, workspace=ws)
+        Y2, _, _ = nv.nvfp4_linear_bias_requant(x, Wq, Ws, g_w, None, bias=b)
+        g2 = nv.nvfp4_global_scale(Y2)
+        q2, s2 = nv.nvfp4_quantize(Y2, g2, nv.SF_MMA_128x4)
+        torch.cuda.synchronize()
+        assert torch.equal(Y.view(torch.int16), Y2.view(torch.int16)), "call %d: Y" % i
+        assert torch.equal(g_y.view(torch.int32), g2.view(torch.int32)), "call %d: g_y" % i
+        assert torch.equal(Yq, q2), "call %d: codes" % i
+        assert torch.equal(Ys, s2), "call %d: scales" % i
+    assert nv.nvfp4_device_error() == 0
+
+
+def test_dynamic_requant_ignores_padding_rows(nv, oracle_mod):
+    """Rows past M of the last tile hold the bias alone and must not enter
+    the amax: X >= 0, weight row 0 <= 0 and bias[0] = +1000 make every real
+    y[:, 0] smaller than 1000 while a padding row would be exactly 1000."""
+    M, N, K = 129, 256, 256
+    x = workloads.make_x("normal", M, K, seed=5).abs()
+    w = workloads.make_w(N, K, seed=6)
+    w[0] = -w[0].abs() - 0.1
+    b = torch.zeros(N, dtype=torch.bfloat16)
+    b[0] = 1000.0
+    Wq, Ws, g_w = nv.nvfp4_quantize_weight(w.cuda(), nv.SF_MMA_128x4)
+    Y, g_y, Yq, Ys = nv.nvfp4_linear_bias_requant_dynamic(x.cuda(), Wq, Ws, g_w, bias=b.cuda())
+    torch.cuda.synchronize()
+    y_bits = bf16_bits(Y)
+    assert float(Y[:, 0].float().max()) < 1000.0
+    g_expect = oracle_mod.global_scale(y_bits)
+    assert _f32_bits(g_y.item()) == _f32_bits(g_expect), "g_y %r vs %r" % (g_y.item(), g_expect)
+    _check_requant(oracle_mod, y_bits, g_expect, Yq, Ys, "padding rows")
+    assert nv.nvfp4_device_error() == 0
