@@ -204,3 +204,26 @@ def test_fused_decode_operand(nv, oracle_mod, M, K, given):
     y_u = nv.nvfp4_linear(x.cuda(), Wq, Ws, gw, g_x=g, mode=nv.LINEAR_UNFUSED)
     assert torch.equal(y_f.view(torch.int16), y_u.view(torch.int16))
     assert nv.nvfp4_device_error() == 0
+
+
+@pytest.mark.parametrize("M,K", [(8, 1024), (100, 1024), (300, 3072)])
+def test_strided_activation_workspace(nv, oracle_mod, M, K):
+    """X as a strided view (row pitch K + 64): the small (8 x 1024), the
+    one-cluster (100 x 1024) and the cooperative (300 x 3072) dynamic
+    quantizers leave the oracle's bytes, and Y equals the contiguous call."""
+    N = 256
+    x = _with_special_blocks(workloads.make_x("outlier", M, K, seed=80 + M))
+    big = torch.zeros((M, K + 64), dtype=torch.bfloat16)
+    big[:, 32:32 + K] = x
+    xd = big.cuda()[:, 32:32 + K]
+    assert xd.stride(0) == K + 64
+    Wq, Ws, gw = _weights(nv, N, K, seed=12)
+    ws = torch.full((nv.linear_workspace_bytes(M, N, K),), 0x5A, dtype=torch.uint8,
+                    device="cuda")
+    y_s = nv.nvfp4_linear(xd, Wq, Ws, gw, workspace=ws)
+    torch.cuda.synchronize()
+    q_ref, sf_ref, g_ref = _expect(oracle_mod, x)
+    _check(ws, M, K, q_ref, sf_ref, g_ref, label="strided %dx%d" % (M, K))
+    y_c = nv.nvfp4_linear(x.cuda(), Wq, Ws, gw)
+    assert torch.equal(y_s.view(torch.int16), y_c.view(torch.int16))
+    assert nv.nvfp4_device_error() == 0
