@@ -671,6 +671,43 @@ def extra_rows(torch, nv, D, workloads, peaks):
                 row["path"] = ("one kernel, X quantized in shared memory" if m <= 8 else
                                "unfused sequence (fused mode covers M <= 8)")
             out["decode_linear_M%d_%s" % (m, mode_name)] = row
+    # F1 on a decode layer (M = 8): the bias and the output's re-quantization
+    # in the decode kernel's epilogue (given g_y, and g_y from the output)
+    # against the same layer followed by separate passes
+    m = 8
+    Xm = workloads.make_x(dec.x_kind, m, dec.K, workloads.x_seed(dec) + 1000 + m, device="cuda")
+    bias_d = workloads.make_bias(n, seed=78, device="cuda")
+    Y = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    Yq = torch.empty((m, n // 2), dtype=torch.uint8, device="cuda")
+    Ys = torch.empty(nv.sf_shape(m, n, nv.SF_MMA_128x4), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(nv.linear_workspace_bytes(m, n, dec.K), dtype=torch.uint8, device="cuda")
+    gyd = torch.empty(1, dtype=torch.float32, device="cuda")
+    W0 = wsets[0]
+    _ok(D.linear_bias_requant(Xm, W0[0], W0[1], W0[2], bias_d, Y, None, None, None, ws), "b")
+    gy = nv.nvfp4_global_scale(Y)
+
+    def rot(fn):
+        return lambda i: fn(wsets[i % 3])
+
+    runs = {
+        "bias_requant_fused_us": rot(lambda w: _ok(D.linear_bias_requant(
+            Xm, w[0], w[1], w[2], bias_d, Y, gy, Yq, Ys, ws), "e")),
+        "bias_then_quantize_us": rot(lambda w: (_ok(D.linear_bias_requant(
+            Xm, w[0], w[1], w[2], bias_d, Y, None, None, None, ws), "b"),
+            _ok(D.quantize(Y, gy, Yq, Ys, nv.SF_MMA_128x4), "q"))),
+        "bias_requant_dynamic_g_y_us": rot(lambda w: _ok(D.linear_bias_requant_dynamic(
+            Xm, w[0], w[1], w[2], bias_d, Y, gyd, Yq, Ys, ws), "d")),
+        "bias_then_global_scale_then_quantize_us": rot(lambda w: (_ok(D.linear_bias_requant(
+            Xm, w[0], w[1], w[2], bias_d, Y, None, None, None, ws), "b"),
+            _ok(D.global_scale(Y, gyd), "g"), _ok(D.quantize(Y, gyd, Yq, Ys, nv.SF_MMA_128x4),
+                                                  "q"))),
+    }
+    row = {}
+    for name, fn in runs.items():
+        for i in range(20):
+            fn(i)
+        row[name] = time_region(torch, fn, 200) * 1e3
+    out["decode_linear_M8_epilogue"] = row
     torch.cuda.synchronize()
     return out
 

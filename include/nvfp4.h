@@ -324,8 +324,10 @@ NVFP4_API nvfp4_status nvfp4_linear_noalloc(const void *X, int64_t M, int64_t K,
  * padding rows of the last 128-row group get scale 0.
  * g_y, Yq and Ys are all given or all NULL; Y and Yq are not both NULL.
  * Shapes: K % 256 == 0, N % 256 == 0 (one pair tile of columns, and the
- * next layer's K rule); M > 128 (the CTA-pair kernel that carries this
- * epilogue; fewer rows return UNSUPPORTED_SHAPE).
+ * next layer's K rule); any M >= 1: up to 64 rows the decode kernel
+ * carries this epilogue (a 16-element block of Y spans 16 lanes there),
+ * beyond it the CTA-pair kernel (above 128 rows: UNSUPPORTED_SHAPE while
+ * the single-CTA kernel is selected for comparison).
  * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_SHAPE,
  * WORKSPACE_TOO_SMALL, CUDA.
  */
@@ -355,7 +357,7 @@ NVFP4_API nvfp4_status nvfp4_linear_bias_requant(const void *X, int64_t M, int64
  * g_y_out: device float (4-byte aligned) that receives g_y; its previous
  * value does not matter.
  * Yq, Ys: as nvfp4_linear_bias_requant.
- * Shapes: K % 256 == 0, N % 256 == 0, M > 128.
+ * Shapes: as nvfp4_linear_bias_requant.
  * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_SHAPE,
  * WORKSPACE_TOO_SMALL, CUDA.
  */

@@ -448,9 +448,10 @@ nvfp4_status nvfp4_linear_bias_requant(const void *X, int64_t M, int64_t K, int6
     if (K % 256 != 0 || N % 256 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (M == 0 || N == 0) return NVFP4_OK;
-    // the epilogue lives in the CTA-pair kernel, the one used above 128 rows
-    if (M <= kSkinnyMaxM || gemm_kernel_choice() == kGemmSingle)
-        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    // the epilogue lives in the decode kernel's variants up to 64 rows and
+    // in the CTA-pair kernel (beyond 128 rows unless the single-CTA kernel is
+    // selected for comparison)
+    if (M > kSkinnyMaxM && gemm_kernel_choice() == kGemmSingle) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (M * (K / 16) >= kMaxBlocks || M * (N / 16) >= kMaxBlocks)
         return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (!Wq || !Ws || !g_w) return NVFP4_ERR_INVALID_ARG;
@@ -471,6 +472,25 @@ nvfp4_status nvfp4_linear_bias_requant(const void *X, int64_t M, int64_t K, int6
     if (quantize_activation(static_cast<const uint16_t *>(X), M, K, ldx, &g_x, ws, st) !=
         cudaSuccess)
         return NVFP4_ERR_CUDA;
+    if (M <= kSkinnyExtMaxM) {
+        // the re-quantization in the epilogue for a few rows (or when Y is
+        // not stored, or its rows are not 16-byte aligned for the
+        // quantizer's vector loads), else a dependent quantize pass over Y
+        const bool y_vec = Y != nullptr && aligned(Y, 16) && ldy % 8 == 0;
+        const bool in_epi = requant && (M <= kSkinnyEpiRequantMaxM || !y_vec);
+        SkinnyArgs sa{Wq, Ws, g_w, xq, xs, nullptr, 0, g_x, M, N, K,
+                      static_cast<uint16_t *>(Y), Y ? ldy : N, 0};
+        sa.bias = static_cast<const uint16_t *>(bias);
+        if (in_epi) {
+            sa.g_y = g_y;
+            sa.Yq = Yq;
+            sa.Ys = Ys;
+        }
+        if (launch_gemm_skinny(sa, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+        if (!requant || in_epi) return NVFP4_OK;
+        return from_cuda(launch_quantize(static_cast<const uint16_t *>(Y), M, N, ldy, g_y, Yq, Ys,
+                                         NVFP4_SF_MMA_128x4, st));
+    }
     GemmArgs a{xq, xs, g_x, Wq, Ws, g_w, M, N, K, static_cast<uint16_t *>(Y), Y ? ldy : N};
     a.bias = static_cast<const uint16_t *>(bias);
     a.g_y = g_y;
@@ -495,9 +515,8 @@ nvfp4_status nvfp4_linear_bias_requant_dynamic(const void *X, int64_t M, int64_t
     if (K % 256 != 0 || N % 256 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (M == 0 || N == 0) return NVFP4_OK;
-    // the epilogue lives in the CTA-pair kernel, the one used above 128 rows
-    if (M <= kSkinnyMaxM || gemm_kernel_choice() == kGemmSingle)
-        return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    // the epilogue: the decode kernel up to 64 rows, else the CTA-pair kernel
+    if (M > kSkinnyMaxM && gemm_kernel_choice() == kGemmSingle) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (M * (K / 16) >= kMaxBlocks || M * (N / 16) >= kMaxBlocks)
         return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (!Wq || !Ws || !g_w) return NVFP4_ERR_INVALID_ARG;
@@ -522,10 +541,20 @@ nvfp4_status nvfp4_linear_bias_requant_dynamic(const void *X, int64_t M, int64_t
             cudaSuccess ||
         launch_cell_reset(cell, st) != cudaSuccess)
         return NVFP4_ERR_CUDA;
-    GemmArgs a{xq, xs, g_x, Wq, Ws, g_w, M, N, K, static_cast<uint16_t *>(Y), ldy};
-    a.bias = static_cast<const uint16_t *>(bias);
-    a.y_amax = cell;
-    if (launch_gemm_pair(a, st) != cudaSuccess || launch_amax_cell_to_scale(cell, st) != cudaSuccess)
+    cudaError_t e;
+    if (M <= kSkinnyExtMaxM) {
+        SkinnyArgs sa{Wq, Ws, g_w, xq, xs, nullptr, 0, g_x, M, N, K,
+                      static_cast<uint16_t *>(Y), ldy, 0};
+        sa.bias = static_cast<const uint16_t *>(bias);
+        sa.y_amax = cell;
+        e = launch_gemm_skinny(sa, st);
+    } else {
+        GemmArgs a{xq, xs, g_x, Wq, Ws, g_w, M, N, K, static_cast<uint16_t *>(Y), ldy};
+        a.bias = static_cast<const uint16_t *>(bias);
+        a.y_amax = cell;
+        e = launch_gemm_pair(a, st);
+    }
+    if (e != cudaSuccess || launch_amax_cell_to_scale(cell, st) != cudaSuccess)
         return NVFP4_ERR_CUDA;
     return from_cuda(launch_quantize(static_cast<const uint16_t *>(Y), M, N, ldy, g_y_out, Yq, Ys,
                                      NVFP4_SF_MMA_128x4, st));

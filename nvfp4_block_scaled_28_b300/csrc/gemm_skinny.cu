@@ -137,8 +137,14 @@ struct SkParams {
     const float *g_x;    // fused: null = compute amax(|X|) / (6 * 448) in the kernel
     const float *g_w;    // one per weight group
     WeightGroups groups;
-    uint16_t *Y;
+    uint16_t *Y;         // null: the bfloat16 output is not stored
     int64_t ldy;
+    // epilogue extensions (see SkinnyArgs): bias, re-quantization of Y, amax of Y
+    const uint16_t *bias;
+    const float *g_y;
+    uint8_t *Yq;
+    uint8_t *Ys;
+    uint32_t *y_amax;
     int M, N, K;
     int n_tiles;
     int n_tail;          // SPLIT: tiles of the partial last round split by K (the last n_tail)
@@ -337,6 +343,87 @@ __device__ __forceinline__ void quantize_x_resident(const SkParams &p, SkShared<
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.xready);
     __syncwarp();
+}
+
+// The decode epilogue with the extensions (bias, re-quantization of Y,
+// amax of Y) for one weight row n = lane's row of the tile (lane = weight
+// row, column m = activation row, as the accumulator lies in TMEM), the
+// arithmetic of the CTA-pair epilogue and of the standalone quantizer:
+//   y = bf16(acc * alpha [+ bias[n]])  (fp32, one rounding)
+// A block of 16 consecutive n is 16 lanes of the warp: its amax is a
+// shuffle reduction, every lane takes the same scale byte S and multiplier,
+// the even lane of each pair converts the pair, and the group's first lane
+// gathers the 8 code bytes and stores them with S (tile layout; rows M ..
+// 127 of the 128-row group get scale 0). Requires N % 256 == 0 with Yq,
+// so every lane's n is a column of Y.
+template <int XR, int NX>
+__device__ __forceinline__ void sk_epilogue_ext(const SkParams &p, const float (&acc)[NX],
+                                                float alpha, int n, int n_warp, int lane) {
+    const bool has_bias = p.bias != nullptr;
+    const bool rq = p.Yq != nullptr;
+    const bool in = n < p.N;
+    const float bv =
+        has_bias && in ? __uint_as_float(static_cast<uint32_t>(p.bias[n]) << 16) : 0.0f;
+    const float gy = rq ? *p.g_y : 1.0f;
+    const int gbase = lane & 16;                  // first lane of this lane's 16-lane group
+    const int n_blk = n_warp + gbase;             // first column of the group's block
+    const int kb = n_blk >> 4;
+    const int kb4 = p.N / 64;
+    const uint64_t sf_end = static_cast<uint64_t>((p.M + 127) / 128) * 128 * (p.N / 16);
+    uint32_t am = 0;
+#pragma unroll
+    for (int m = 0; m < XR; ++m) {
+        if (m >= p.M) break;  // the same for every lane
+        const float y = has_bias ? __fadd_rn(__fmul_rn(acc[m], alpha), bv) : acc[m] * alpha;
+        const __nv_bfloat16 v = __float2bfloat16_rn(y);
+        const uint32_t yb = *reinterpret_cast<const uint16_t *>(&v);
+        if (p.Y != nullptr && in) p.Y[static_cast<int64_t>(m) * p.ldy + n] = static_cast<uint16_t>(yb);
+        if (in) am = max(am, yb & 0x7FFFu);
+        if (rq) {
+            uint32_t a = yb & 0x7FFFu;
+            a = max(a, __shfl_xor_sync(kAllLanes, a, 1));
+            a = max(a, __shfl_xor_sync(kAllLanes, a, 2));
+            a = max(a, __shfl_xor_sync(kAllLanes, a, 4));
+            a = max(a, __shfl_xor_sync(kAllLanes, a, 8));
+            const float amax = __uint_as_float(a << 16);
+            const uint32_t S = cvt_e4m3_satfinite(__fdiv_rn(__fdiv_rn(amax, 6.0f), gy));
+            const float r = scale_recip(S, gy);
+            const uint64_t rr =
+                (static_cast<uint64_t>(__float_as_uint(r)) << 32) | __float_as_uint(r);
+            const uint32_t partner = __shfl_xor_sync(kAllLanes, yb, 1);
+            const uint32_t byte = codes2(yb | (partner << 16), rr);  // valid on even lanes
+            uint32_t lo = 0, hi = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                lo |= (__shfl_sync(kAllLanes, byte, gbase + 2 * j) & 0xFFu) << (8 * j);
+                hi |= (__shfl_sync(kAllLanes, byte, gbase + 8 + 2 * j) & 0xFFu) << (8 * j);
+            }
+            if ((lane & 15) == 0) {
+                const int64_t qoff = static_cast<int64_t>(m) * (p.N / 2) + n_blk / 2;
+                if (NVFP4_CHECK(qoff + 8 <= static_cast<int64_t>(p.M) * (p.N / 2)))
+                    *reinterpret_cast<uint2 *>(p.Yq + qoff) = make_uint2(lo, hi);
+                const uint64_t off = ((static_cast<uint64_t>(m >> 7) * kb4 + (kb >> 2)) << 9) +
+                                     ((m & 31) << 4) + (((m & 127) >> 5) << 2) + (kb & 3);
+                if (NVFP4_CHECK(off < sf_end)) p.Ys[off] = static_cast<uint8_t>(S);
+            }
+        }
+    }
+    if (rq) {
+        // padding rows of the 128-row group: scale 0 for this warp's two
+        // blocks, the (row, block) pairs spread over the 32 lanes
+        const int rows_pad = (p.M + 127) / 128 * 128;
+        const int kb0 = n_warp >> 4;
+        for (int i = lane; i < 2 * (rows_pad - p.M); i += 32) {
+            const int m = p.M + (i >> 1), k = kb0 + (i & 1);
+            const uint64_t off = ((static_cast<uint64_t>(m >> 7) * kb4 + (k >> 2)) << 9) +
+                                 ((m & 31) << 4) + (((m & 127) >> 5) << 2) + (k & 3);
+            if (NVFP4_CHECK(off < sf_end)) p.Ys[off] = 0;
+        }
+    }
+    if (p.y_amax != nullptr) {
+        am = __reduce_max_sync(kAllLanes, am);
+        if (lane == 0 && am != 0u) atomicMax(p.y_amax, am);
+    }
 }
 
 template <int NX, int XR, bool FUSED, int KC, int SPLIT>
@@ -602,14 +689,22 @@ __global__ void __launch_bounds__(SkCfg<NX, XR, FUSED, KC, SPLIT>::THREADS, 1)
             const float gx = FUSED ? sh.g_x : *p.g_x;
             const float alpha = __fmul_rn(gx, p.g_w[weight_group_of(p.groups, un.nt * SK_BM)]);
             const int n = un.nt * SK_BM + row;
-            if (n < p.N) {
+            const bool ext = p.bias != nullptr || p.Yq != nullptr || p.y_amax != nullptr;
+            if (!ext) {
+                if (n < p.N) {
 #pragma unroll
-                for (int m = 0; m < XR; ++m) {
-                    if (m < p.M) {
-                        const __nv_bfloat16 v = __float2bfloat16_rn(acc[m] * alpha);
-                        p.Y[static_cast<int64_t>(m) * p.ldy + n] = *reinterpret_cast<const uint16_t *>(&v);
+                    for (int m = 0; m < XR; ++m) {
+                        if (m < p.M) {
+                            const __nv_bfloat16 v = __float2bfloat16_rn(acc[m] * alpha);
+                            p.Y[static_cast<int64_t>(m) * p.ldy + n] =
+                                *reinterpret_cast<const uint16_t *>(&v);
+                        }
                     }
                 }
+            } else if constexpr (NX <= 64) {
+                // (the 128-row variant carries no extensions: the host sends
+                // them only with M <= 64)
+                sk_epilogue_ext<XR, NX>(p, acc, alpha, n, un.nt * SK_BM + quarter * 32, lane);
             }
         }
         __syncwarp();
@@ -668,6 +763,11 @@ cudaError_t launch_sk(const SkinnyArgs &a, cudaStream_t st) {
     p.groups = a.groups;
     p.Y = a.Y;
     p.ldy = a.ldy;
+    p.bias = a.bias;
+    p.g_y = a.g_y;
+    p.Yq = a.Yq;
+    p.Ys = a.Ys;
+    p.y_amax = a.y_amax;
     p.M = static_cast<int>(a.M);
     p.N = static_cast<int>(a.N);
     p.K = static_cast<int>(a.K);
@@ -714,6 +814,9 @@ cudaError_t launch_unfused(const SkinnyArgs &a, cudaStream_t st) {
 cudaError_t launch_gemm_skinny(const SkinnyArgs &a, cudaStream_t st) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
     if (a.M > kSkinnyMaxM) return cudaErrorInvalidValue;
+    // the epilogue extensions live in the variants up to 64 activation rows
+    const bool ext = a.bias != nullptr || a.Yq != nullptr || a.y_amax != nullptr;
+    if (ext && (a.M > kSkinnyExtMaxM || a.fused)) return cudaErrorInvalidValue;
     // a tail to split, whose K halves are whole stages of two chunks. Only
     // for up to 8 activation rows: measured on the 27648 x 5120 weight, the
     // split saves 1.2 us at M = 1 and 2.7 us at M = 8 but costs 2.5 us at

@@ -171,6 +171,12 @@ cudaError_t launch_gemm_plain(const GemmArgs &a, cudaStream_t st);
 constexpr int64_t kSkinnyMaxM = 128;       // activation rows it handles
 constexpr int64_t kSkinnyFusedMaxM = 8;    // ... with in-kernel quantization of X
 constexpr int64_t kSkinnyFusedMaxK = 6144; // ... held resident in shared memory
+constexpr int64_t kSkinnyExtMaxM = 64;     // ... with the bias / re-quantization / amax epilogue
+// ... re-quantizing Y in that epilogue (with a given g_y): a 16-element
+// block spans 16 lanes there and the per-row work sits on few warps, so
+// beyond 2 rows a dependent quantize pass over the stored Y is faster
+// (27648 x 5120: M = 1 25.3 vs 31.4 us, M = 2 27.6 vs 30.2, M = 4 31.2 vs 30.7)
+constexpr int64_t kSkinnyEpiRequantMaxM = 2;
 struct SkinnyArgs {
     const uint8_t *Wq, *Ws;  // weights: codes (N x K/2), scales (128x4 tile layout)
     const float *g_w;
@@ -186,6 +192,15 @@ struct SkinnyArgs {
     // fused, testing hook: where CTA 0 writes the operand it quantized
     uint8_t *dbg_xq = nullptr;
     uint8_t *dbg_xs = nullptr;
+    // Epilogue extensions, as GemmArgs' (N % 256 == 0 with Yq): a bfloat16
+    // bias of N, the NVFP4 re-quantization of the bfloat16 output under *g_y
+    // into Yq / Ys (rows padded to 128), the output's amax into *y_amax;
+    // Y may then be null (not stored)
+    const uint16_t *bias = nullptr;
+    const float *g_y = nullptr;
+    uint8_t *Yq = nullptr;
+    uint8_t *Ys = nullptr;
+    uint32_t *y_amax = nullptr;
 };
 cudaError_t launch_gemm_skinny(const SkinnyArgs &a, cudaStream_t st);
 

@@ -232,3 +232,87 @@ def test_dynamic_requant_ignores_padding_rows(nv, oracle_mod):
     assert _f32_bits(g_y.item()) == _f32_bits(g_expect), "g_y %r vs %r" % (g_y.item(), g_expect)
     _check_requant(oracle_mod, y_bits, g_expect, Yq, Ys, "padding rows")
     assert nv.nvfp4_device_error() == 0
+
+
+# Decode rows: up to 64 the decode kernel's epilogue (a 16-element block of Y
+# spans 16 lanes), 65 .. 128 the CTA-pair kernel; (4, 19200, 1024) has a
+# partial last round whose tiles are split by K across a cluster
+DECODE_EPI_SHAPES = [(1, 512, 512), (8, 768, 1024), (32, 1024, 512), (64, 512, 768),
+                     (100, 512, 512), (4, 19200, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", DECODE_EPI_SHAPES)
+def test_decode_bias_and_requant_match_oracle(nv, oracle_mod, M, N, K):
+    c = _case(nv, oracle_mod, M, N, K, seed=M * 11 + N + K)
+    xq, xs, gx, wq, ws, gw = c["ops"]
+    y_ref = oracle_mod.gemm(xq, xs, gx, wq, ws, gw, bias=c["bb"])
+    g_y = oracle_mod.global_scale(y_ref)
+    Wq, Ws, g_w = c["W"]
+    Ys = torch.full(nv.sf_shape(M, N, nv.SF_MMA_128x4), 0xA5, dtype=torch.uint8, device="cuda")
+    Y, Yq, Ys = nv.nvfp4_linear_bias_requant(c["x"].cuda(), Wq, Ws, g_w, _gy(g_y),
+                                             bias=c["b"].cuda(), Ys=Ys)
+    y_bits = bf16_bits(Y)
+    check_gemm_tolerance(y_bits, y_ref, "decode bias %dx%dx%d" % (M, N, K))
+    _check_requant(oracle_mod, y_bits, g_y, Yq, Ys, "decode requant %dx%dx%d" % (M, N, K))
+    # Y alone (no re-quantization) and the codes alone (no Y) agree with it
+    Y2, _, _ = nv.nvfp4_linear_bias_requant(c["x"].cuda(), Wq, Ws, g_w, None, bias=c["b"].cuda())
+    assert torch.equal(Y2.view(torch.int16), Y.view(torch.int16))
+    _, Yq3, Ys3 = nv.nvfp4_linear_bias_requant(c["x"].cuda(), Wq, Ws, g_w, _gy(g_y),
+                                               bias=c["b"].cuda(), store_y=False)
+    assert torch.equal(Yq3, Yq) and torch.equal(Ys3, Ys)
+    assert nv.nvfp4_device_error() == 0
+
+
+@pytest.mark.parametrize("M,N,K", DECODE_EPI_SHAPES)
+def test_decode_dynamic_requant_matches_oracle(nv, oracle_mod, M, N, K):
+    c = _case(nv, oracle_mod, M, N, K, seed=M * 13 + N + 2 * K)
+    Wq, Ws, g_w = c["W"]
+    Y, g_y, Yq, Ys = nv.nvfp4_linear_bias_requant_dynamic(c["x"].cuda(), Wq, Ws, g_w,
+                                                          bias=c["b"].cuda())
+    torch.cuda.synchronize()
+    y_bits = bf16_bits(Y)
+    g_expect = oracle_mod.global_scale(y_bits)
+    assert _f32_bits(g_y.item()) == _f32_bits(g_expect), "g_y %r vs %r" % (g_y.item(), g_expect)
+    _check_requant(oracle_mod, y_bits, g_expect, Yq, Ys, "decode dynamic %dx%dx%d" % (M, N, K))
+    assert nv.nvfp4_device_error() == 0
+
+
+@pytest.mark.parametrize("M", [1, 8, 32])
+def test_decode_dynamic_requant_equals_unfused_sequence(nv, M):
+    """The decode FFN-up shape (5120 -> 27648): all bytes equal the linear
+    with the bias, then nvfp4_global_scale(Y) and nvfp4_quantize(Y)."""
+    N, K = 27648, 5120
+    w = workloads.make_w(N, K, seed=61)
+    Wq, Ws, g_w = nv.nvfp4_quantize_weight(w.cuda(), nv.SF_MMA_128x4)
+    b = workloads.make_bias(N, seed=62).cuda()
+    x = workloads.make_x("outlier", M, K, seed=63 + M).cuda()
+    Y, g_y, Yq, Ys = nv.nvfp4_linear_bias_requant_dynamic(x, Wq, Ws, g_w, bias=b)
+    Y2, _, _ = nv.nvfp4_linear_bias_requant(x, Wq, Ws, g_w, None, bias=b)
+    g2 = nv.nvfp4_global_scale(Y2)
+    q2, s2 = nv.nvfp4_quantize(Y2, g2, nv.SF_MMA_128x4)
+    torch.cuda.synchronize()
+    assert torch.equal(Y.view(torch.int16), Y2.view(torch.int16))
+    assert torch.equal(g_y.view(torch.int32), g2.view(torch.int32))
+    assert torch.equal(Yq, q2) and torch.equal(Ys, s2)
+    assert nv.nvfp4_device_error() == 0
+
+
+def test_decode_requant_with_unaligned_y(nv, oracle_mod):
+    """A Y whose rows are not 16-byte aligned (ldy = N + 1) keeps the
+    re-quantization in the decode epilogue; the bytes are the same."""
+    M, N, K = 8, 512, 512
+    c = _case(nv, oracle_mod, M, N, K, seed=91)
+    xq, xs, gx, wq, ws, gw = c["ops"]
+    g_y = oracle_mod.global_scale(oracle_mod.gemm(xq, xs, gx, wq, ws, gw, bias=c["bb"]))
+    Wq, Ws, g_w = c["W"]
+    big = torch.zeros((M, N + 1), dtype=torch.bfloat16, device="cuda")
+    Yv = big[:, :N]
+    assert Yv.stride(0) == N + 1
+    Y, Yq, Ys = nv.nvfp4_linear_bias_requant(c["x"].cuda(), Wq, Ws, g_w, _gy(g_y),
+                                             bias=c["b"].cuda(), Y=Yv)
+    _check_requant(oracle_mod, bf16_bits(Y.contiguous()), g_y, Yq, Ys, "unaligned Y")
+    Y2, Yq2, Ys2 = nv.nvfp4_linear_bias_requant(c["x"].cuda(), Wq, Ws, g_w, _gy(g_y),
+                                                bias=c["b"].cuda())
+    assert torch.equal(Y.contiguous().view(torch.int16), Y2.view(torch.int16))
+    assert torch.equal(Yq, Yq2) and torch.equal(Ys, Ys2)
+    assert nv.nvfp4_device_error() == 0
