@@ -357,7 +357,10 @@ NVFP4_API nvfp4_status nvfp4_linear_bias_requant(const void *X, int64_t M, int64
  * g_y_out: device float (4-byte aligned) that receives g_y; its previous
  * value does not matter.
  * Yq, Ys: as nvfp4_linear_bias_requant.
- * Shapes: as nvfp4_linear_bias_requant.
+ * Shapes: as nvfp4_linear_bias_requant. With M = 0 or N = 0 the call only
+ * writes *g_y_out = 1 (the global scale of an empty tensor, as
+ * nvfp4_global_scale gives it); Y, Yq, Ys and the workspace may then be
+ * NULL.
  * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED_SHAPE,
  * WORKSPACE_TOO_SMALL, CUDA.
  */

@@ -508,32 +508,39 @@ nvfp4_status nvfp4_linear_bias_requant_dynamic(const void *X, int64_t M, int64_t
     nvfp4_status s = check_bf16_matrix(X, M, K, ldx);
     if (s != NVFP4_OK) return s;
     if (M < 0 || N < 0 || K <= 0) return NVFP4_ERR_INVALID_ARG;
-    if (!Y || !g_y_out || !Yq || !Ys) return NVFP4_ERR_INVALID_ARG;
+    if (g_y_out == nullptr) return NVFP4_ERR_INVALID_ARG;
     // Y is read back by the quantizer: its rows as that quantizer's input
     s = check_bf16_matrix(Y, M, N, ldy);
     if (s != NVFP4_OK) return s;
     if (K % 256 != 0 || N % 256 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    if (M == 0 || N == 0) return NVFP4_OK;
+    if (!aligned(g_y_out, 4)) return NVFP4_ERR_MISALIGNED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t *cell = reinterpret_cast<uint32_t *>(g_y_out);
+    if (M == 0 || N == 0) {
+        // an empty Y has amax 0, so g_y = 1 (as nvfp4_global_scale gives)
+        return (launch_cell_reset(cell, st) == cudaSuccess &&
+                launch_amax_cell_to_scale(cell, st) == cudaSuccess)
+                   ? NVFP4_OK
+                   : NVFP4_ERR_CUDA;
+    }
+    if (!Y || !Yq || !Ys) return NVFP4_ERR_INVALID_ARG;
     // the epilogue: the decode kernel up to 64 rows, else the CTA-pair kernel
     if (M > kSkinnyMaxM && gemm_kernel_choice() == kGemmSingle) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (M * (K / 16) >= kMaxBlocks || M * (N / 16) >= kMaxBlocks)
         return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (!Wq || !Ws || !g_w) return NVFP4_ERR_INVALID_ARG;
     if (!aligned(Wq, 16) || !aligned(Ws, 16) || !aligned(g_w, 4)) return NVFP4_ERR_MISALIGNED;
-    if (!aligned(bias, 16) || !aligned(Yq, 16) || !aligned(Ys, 16) || !aligned(g_y_out, 4))
-        return NVFP4_ERR_MISALIGNED;
+    if (!aligned(bias, 16) || !aligned(Yq, 16) || !aligned(Ys, 16)) return NVFP4_ERR_MISALIGNED;
     if (g_x != nullptr && !aligned(g_x, 4)) return NVFP4_ERR_MISALIGNED;
     const size_t need = nvfp4_linear_workspace_bytes(M, N, K, NVFP4_LINEAR_UNFUSED);
     if (workspace_bytes < need) return NVFP4_ERR_WORKSPACE_TOO_SMALL;
     if (workspace == nullptr) return NVFP4_ERR_INVALID_ARG;
     if (!aligned(workspace, 256)) return NVFP4_ERR_MISALIGNED;
 
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     uint8_t *xq = ws + kLinearHeader;
     uint8_t *xs = xq + round_up(static_cast<size_t>(M) * static_cast<size_t>(K / 2), 256);
-    uint32_t *cell = reinterpret_cast<uint32_t *>(g_y_out);
     // 1. X's operand; 2. the amax cell zeroed (after 1 completes); 3. the
     // GEMM, whose epilogue folds max |y| into the cell; 4. the cell turned
     // into g_y; 5. Y quantized with it (Y comes back from L2 when it fits)

@@ -190,7 +190,12 @@ def test_linear_bias_requant_argument_checks(lib):
     base = dict(X=A16, M=256, K=512, ldx=512, Wq=A16, Ws=A16, gw=A16, N=512, bias=A16, Y=A16,
                 ldy=512, gy=A16, Yq=A16, Ys=A16, gx=None, ws=A16 * 16, wsb=1 << 30)
     call = lambda **kw: f(*[{**base, **kw}[k] for k in base], None)
-    assert call(M=128) == N.ERR_UNSUPPORTED_SHAPE       # the CTA-pair kernel: M > 128
+    # above 128 rows the epilogue is in the CTA-pair kernel only
+    assert lib.nvfp4_debug_select_gemm_kernel(1) == N.OK
+    try:
+        assert call(M=256) == N.ERR_UNSUPPORTED_SHAPE
+    finally:
+        assert lib.nvfp4_debug_select_gemm_kernel(0) == N.OK
     assert call(N=384, ldy=384) == N.ERR_UNSUPPORTED_SHAPE  # N % 256
     assert call(K=448, ldx=448) == N.ERR_UNSUPPORTED_SHAPE  # K % 256
     assert call(Y=None, gy=None, Yq=None, Ys=None) == N.ERR_INVALID_ARG  # no output at all
@@ -203,6 +208,34 @@ def test_linear_bias_requant_argument_checks(lib):
     assert call(wsb=16) == N.ERR_WORKSPACE_TOO_SMALL
     assert call(ws=A16 + 16) == N.ERR_MISALIGNED
     assert call(M=0) == N.OK and call(N=0, ldy=0) == N.OK  # empty: nothing launched
+
+
+def test_linear_bias_requant_dynamic_argument_checks(lib):
+    f = lib.nvfp4_linear_bias_requant_dynamic
+    base = dict(X=A16, M=256, K=512, ldx=512, Wq=A16, Ws=A16, gw=A16, N=512, bias=A16, Y=A16,
+                ldy=512, gy=A16, Yq=A16, Ys=A16, gx=None, ws=A16 * 16, wsb=1 << 30)
+    call = lambda **kw: f(*[{**base, **kw}[k] for k in base], None)
+    assert call(gy=None) == N.ERR_INVALID_ARG            # g_y_out is always written
+    assert call(gy=None, M=0) == N.ERR_INVALID_ARG
+    assert call(Y=None) == N.ERR_INVALID_ARG             # Y is required (read back)
+    assert call(Yq=None) == N.ERR_INVALID_ARG
+    assert call(Ys=None) == N.ERR_INVALID_ARG
+    assert call(Y=A16 + 8) == N.ERR_MISALIGNED           # the quantizer reads Y 16 bytes at a time
+    assert call(ldy=516) == N.ERR_MISALIGNED
+    assert call(ldy=100) == N.ERR_INVALID_ARG
+    assert call(N=384, ldy=384) == N.ERR_UNSUPPORTED_SHAPE
+    assert call(K=448, ldx=448) == N.ERR_UNSUPPORTED_SHAPE
+    assert call(gy=ODD) == N.ERR_MISALIGNED
+    assert call(gy=ODD, M=0) == N.ERR_MISALIGNED
+    assert call(bias=A16 + 8) == N.ERR_MISALIGNED
+    assert call(Yq=A16 + 8) == N.ERR_MISALIGNED
+    assert call(wsb=16) == N.ERR_WORKSPACE_TOO_SMALL
+    assert call(ws=A16 + 16) == N.ERR_MISALIGNED
+    assert lib.nvfp4_debug_select_gemm_kernel(1) == N.OK
+    try:
+        assert call(M=256) == N.ERR_UNSUPPORTED_SHAPE
+    finally:
+        assert lib.nvfp4_debug_select_gemm_kernel(0) == N.OK
 
 
 def test_linear_grouped_argument_checks(lib):

@@ -234,6 +234,24 @@ def test_dynamic_requant_ignores_padding_rows(nv, oracle_mod):
     assert nv.nvfp4_device_error() == 0
 
 
+def test_dynamic_requant_empty_activation(nv, oracle_mod):
+    """M = 0: nothing to multiply; g_y is the global scale of an empty
+    tensor (1, as the oracle and nvfp4_global_scale give), written over a
+    stale value."""
+    N, K = 256, 512
+    Wq, Ws, g_w = nv.nvfp4_quantize_weight(workloads.make_w(N, K, seed=7).cuda(),
+                                           nv.SF_MMA_128x4)
+    x = torch.empty((0, K), dtype=torch.bfloat16, device="cuda")
+    g_y = _gy(123.0)
+    Y, g_y, Yq, Ys = nv.nvfp4_linear_bias_requant_dynamic(x, Wq, Ws, g_w, g_y=g_y)
+    torch.cuda.synchronize()
+    assert Y.shape == (0, N) and Yq.shape == (0, N // 2) and Ys.numel() == 0
+    g_empty = oracle_mod.global_scale(np.zeros((0, K), dtype=np.uint16))
+    assert _f32_bits(g_y.item()) == _f32_bits(g_empty) == _f32_bits(1.0)
+    assert _f32_bits(nv.nvfp4_global_scale(x).item()) == _f32_bits(1.0)
+    assert nv.nvfp4_device_error() == 0
+
+
 # Decode rows: up to 64 the decode kernel's epilogue (a 16-element block of Y
 # spans 16 lanes), 65 .. 128 the CTA-pair kernel; (4, 19200, 1024) has a
 # partial last round whose tiles are split by K across a cluster
