@@ -30,6 +30,9 @@
  *  - bfloat16 tensors are passed as void* (2 bytes per element), row-major
  *    with the given leading dimension (elements between consecutive rows).
  *  - Packed codes are row-major (rows, K/2) bytes, contiguous.
+ *  - Host threads may call entry points concurrently: the one-time set-up
+ *    of each kernel on a device is serialized inside the library. Calls whose
+ *    work overlaps on the GPU must not share a workspace or an output.
  *  - Errors are returned as nvfp4_status; nothing aborts the process. Checks
  *    on arguments happen before anything is enqueued: on an error return,
  *    no work was launched. A launch failure returns NVFP4_ERR_CUDA.

@@ -23,29 +23,31 @@ int device_slot() {
 }
 
 unsigned int *device_error_word() {
-    static unsigned int *addr[kMaxDevices] = {};
+    static DeviceOnce once;
+    static unsigned int *addr[kMaxDevices + 1] = {};
     const int dev = device_slot();
     if (dev == kMaxDevices) return nullptr;
-    if (addr[dev] == nullptr) {
+    const cudaError_t e = once.run([](int slot) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-        addr[dev] = static_cast<unsigned int *>(p);
-    }
-    return addr[dev];
+        const cudaError_t r = cudaGetSymbolAddress(&p, g_device_error);
+        if (r == cudaSuccess) addr[slot] = static_cast<unsigned int *>(p);
+        return r;
+    });
+    return e == cudaSuccess ? addr[dev] : nullptr;
 }
 
 const LaunchCfg &launch_cfg() {
+    static DeviceOnce once;
     static LaunchCfg cfg[kMaxDevices + 1];
-    static bool init[kMaxDevices + 1] = {};
     const int dev = device_slot();
-    if (!init[dev]) {
+    (void)once.run([](int slot) {
         int sms = 0;
-        if (dev < kMaxDevices &&
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        if (slot < kMaxDevices &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, slot) == cudaSuccess &&
             sms > 0)
-            cfg[dev].num_sms = sms;
-        init[dev] = true;
-    }
+            cfg[slot].num_sms = sms;
+        return cudaSuccess;
+    });
     return cfg[dev];
 }
 

@@ -349,14 +349,16 @@ bool make_operand_map(CUtensorMap *map, const uint8_t *ptr, int64_t rows, int64_
 
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
-    static int max_ctas_of[kMaxDevices + 1] = {};  // 0: not yet set up
-    int &max_ctas = max_ctas_of[device_slot()];
-    if (max_ctas <= 0) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SMEM_ALLOC);
-        if (e != cudaSuccess) return e;
-        max_ctas = launch_cfg().num_sms;
-    }
+    static DeviceOnce once;
+    static int max_ctas_of[kMaxDevices + 1] = {};
+    const cudaError_t e_setup = once.run([](int slot) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+        if (e == cudaSuccess) max_ctas_of[slot] = launch_cfg().num_sms;
+        return e;
+    });
+    if (e_setup != cudaSuccess) return e_setup;
+    const int max_ctas = max_ctas_of[device_slot()];
     CUtensorMap tmA, tmB;
     if (!make_operand_map(&tmA, a.Aq, a.M, a.K, BM)) return cudaErrorInvalidValue;
     if (!make_operand_map(&tmB, a.Bq, a.N, a.K, BN)) return cudaErrorInvalidValue;

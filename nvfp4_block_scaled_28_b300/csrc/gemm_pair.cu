@@ -615,9 +615,9 @@ cudaError_t launch_gemm_plain(const GemmArgs &a, cudaStream_t st) {
 
 cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
-    static int max_clusters_of[kMaxDevices + 1] = {};  // 0: not yet queried
-    int &max_clusters = max_clusters_of[device_slot()];
-    if (max_clusters <= 0) {
+    static DeviceOnce once;
+    static int max_clusters_of[kMaxDevices + 1] = {};
+    const cudaError_t e_setup = once.run([](int slot) {
         cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<0>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
         if (e != cudaSuccess) return e;
@@ -627,7 +627,7 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
         e = cudaFuncSetAttribute(gemm_pair_kernel<2>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
         if (e != cudaSuccess) return e;
-        max_clusters = launch_cfg().num_sms / 2;
+        int max_clusters = launch_cfg().num_sms / 2;
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -643,7 +643,12 @@ cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t st) {
         if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<0>, &cfg) == cudaSuccess && n > 0 &&
             n < max_clusters)
             max_clusters = n;
-    }
+        (void)cudaGetLastError();  // a failed query leaves the default
+        max_clusters_of[slot] = max_clusters;
+        return cudaSuccess;
+    });
+    if (e_setup != cudaSuccess) return e_setup;
+    const int max_clusters = max_clusters_of[device_slot()];
     const int64_t kb4 = a.K / 64;
     const int64_t sf_rows_a = (a.M + 127) / 128 * kb4 * 2;  // 256-byte rows
     const int64_t groups_b = (a.N + 127) / 128;

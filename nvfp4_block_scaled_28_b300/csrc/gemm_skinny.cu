@@ -733,14 +733,12 @@ int tail_tiles(int64_t n_tiles) {
 template <int NX, int XR, bool FUSED, int KC, int SPLIT>
 cudaError_t launch_sk(const SkinnyArgs &a, cudaStream_t st) {
     using C = SkCfg<NX, XR, FUSED, KC, SPLIT>;
-    static bool attr_of[kMaxDevices + 1] = {};
-    bool &attr = attr_of[device_slot()];
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(skinny_kernel<NX, XR, FUSED, KC, SPLIT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static DeviceOnce once;
+    const cudaError_t e_setup = once.run([](int) {
+        return cudaFuncSetAttribute(skinny_kernel<NX, XR, FUSED, KC, SPLIT>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    });
+    if (e_setup != cudaSuccess) return e_setup;
     CUtensorMap tmW, tmX;
     if (!make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wq, a.K / 2, a.N, a.K / 2, 128, SK_BM,
                 CU_TENSOR_MAP_SWIZZLE_128B))

@@ -1,9 +1,11 @@
 // Internal launchers shared by the C-ABI layer (api.cu) and the kernels.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <mutex>
 
 #include "nvfp4.h"
 
@@ -34,6 +36,28 @@ struct FastDiv {
 // kMaxDevices when the device cannot be told.
 constexpr int kMaxDevices = 64;
 int device_slot();
+
+// Per-device one-time set-up (kernel attributes, occupancy queries, device
+// symbols) that host threads may reach concurrently: `init(slot)` runs
+// under a lock until it first succeeds for the current device, and what it
+// wrote is visible to every later caller (release / acquire on the flag).
+class DeviceOnce {
+  public:
+    template <class F>
+    cudaError_t run(F &&init) {
+        const int slot = device_slot();
+        if (ready_[slot].load(std::memory_order_acquire)) return cudaSuccess;
+        std::lock_guard<std::mutex> lock(mu_);
+        if (ready_[slot].load(std::memory_order_relaxed)) return cudaSuccess;
+        const cudaError_t e = init(slot);
+        if (e == cudaSuccess) ready_[slot].store(1, std::memory_order_release);
+        return e;
+    }
+
+  private:
+    std::mutex mu_;
+    std::atomic<int> ready_[kMaxDevices + 1] = {};
+};
 
 struct LaunchCfg {
     int num_sms = 148;

@@ -241,14 +241,12 @@ cudaError_t launch_r(const uint16_t *X, int64_t rows, int64_t K, int64_t ldx, co
                      const float *g_w, float lora_scale, const uint16_t *A, uint8_t *q, uint8_t *sf,
                      float *part, uint16_t *Lp, cudaStream_t st) {
     using C = LoraCfg<R>;
-    static bool attr_set_of[kMaxDevices + 1] = {};
-    bool &attr_set = attr_set_of[device_slot()];
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(quantize_lora_kernel<R>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static DeviceOnce once;
+    const cudaError_t e_setup = once.run([](int) {
+        return cudaFuncSetAttribute(quantize_lora_kernel<R>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    });
+    if (e_setup != cudaSuccess) return e_setup;
     const uint32_t rows_pad = static_cast<uint32_t>((rows + 127) / 128 * 128);
     const Split sp = lora_split(rows_pad, K);
     cudaLaunchAttribute attr = pdl_attribute();

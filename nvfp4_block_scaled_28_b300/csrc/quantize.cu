@@ -587,11 +587,11 @@ cudaError_t launch_quantize_cluster(const uint16_t *X, int64_t rows, int64_t col
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    // 0: not yet known; 1: a cluster of 16 fits on this device; -1: it does
-    // not (the cooperative quantizer is used instead)
-    static int fits_of[kMaxDevices + 1] = {};
-    int &fits = fits_of[device_slot()];
-    if (fits == 0) {
+    // per device: does a cluster of 16 fit (else the cooperative quantizer
+    // is used instead)
+    static DeviceOnce once;
+    static bool fits_of[kMaxDevices + 1] = {};
+    (void)once.run([&](int slot) {
         // 16 CTAs per cluster is beyond the portable 8
         cudaError_t e = cudaFuncSetAttribute(quantize_cluster_kernel,
                                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -601,9 +601,10 @@ cudaError_t launch_quantize_cluster(const uint16_t *X, int64_t rows, int64_t col
         int n = 0;
         if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, quantize_cluster_kernel, &occ);
         if (e != cudaSuccess) (void)cudaGetLastError();
-        fits = (e == cudaSuccess && n >= 1) ? 1 : -1;
-    }
-    if (fits < 0) return cudaErrorNotSupported;
+        fits_of[slot] = e == cudaSuccess && n >= 1;
+        return cudaSuccess;
+    });
+    if (!fits_of[device_slot()]) return cudaErrorNotSupported;
     return cudaLaunchKernelEx(&cfg, quantize_cluster_kernel, X, static_cast<uint32_t>(rows),
                               rows_pad, kbpr, static_cast<uint64_t>(ldx), FastDiv(kbpr), vpr,
                               FastDiv(vpr), g_out, q, sf);
@@ -612,15 +613,17 @@ cudaError_t launch_quantize_cluster(const uint16_t *X, int64_t rows, int64_t col
 cudaError_t launch_quantize_fused(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
                                   uint32_t *partials, unsigned int *counter, float *g_out,
                                   uint8_t *q, uint8_t *sf, cudaStream_t st) {
+    static DeviceOnce once;
     static int per_sm_of[kMaxDevices + 1] = {};
-    int &per_sm = per_sm_of[device_slot()];
-    if (per_sm == 0) {
+    const cudaError_t e_setup = once.run([](int slot) {
         int n = 0;
-        cudaError_t e =
+        const cudaError_t e =
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_fused_kernel, kThreads, 0);
-        if (e != cudaSuccess) return e;
-        per_sm = n < 1 ? 1 : (n > 8 ? 8 : n);
-    }
+        if (e == cudaSuccess) per_sm_of[slot] = n < 1 ? 1 : (n > 8 ? 8 : n);
+        return e;
+    });
+    if (e_setup != cudaSuccess) return e_setup;
+    const int per_sm = per_sm_of[device_slot()];
     const uint32_t vpr = static_cast<uint32_t>(cols / 8);
     const uint32_t kbpr = static_cast<uint32_t>(cols / 16);
     const uint32_t rows_pad = static_cast<uint32_t>((rows + 127) / 128 * 128);
