@@ -11,15 +11,18 @@
 // FP4 products (extra bfloat16 tensor-core steps) before its epilogue
 // multiplies everything by g_x * g_w.
 //
-// Work split: a CTA owns 64 rows (16 per warp) and one K range; the K
-// ranges' partial down projections go to FP32 workspace and a small kernel
-// sums them in range order (deterministic) and applies the scale. X and A
-// chunks of 64 columns stream into a 4-deep shared-memory ring (cp.async,
-// 16-byte pieces, XOR-swizzled rows). From each chunk in shared memory the
-// threads quantize one 16-element block each (the standalone quantizer's
-// arithmetic) and the warps take their 16 x 16 pieces with ldmatrix for the
-// tensor-core product with A (mma.sync m16n8k16), so X is read from HBM once
-// for both.
+// Work split: a CTA owns 128 rows and one K range; the K ranges' partial
+// down projections go to FP32 workspace and a small kernel sums them in
+// range order (deterministic) and applies the scale. X and A chunks of 64
+// columns stream into a shared-memory ring (cp.async, 16-byte pieces, rows
+// XOR-swizzled in the tensor core's 128-byte pattern). Each chunk feeds two
+// consumers: one elected thread issues the chunk's four
+// tcgen05.mma kind::f16 (M = 128 rows of X, N = r rows of A, K = 16 each)
+// into an FP32 accumulator in tensor memory, and meanwhile every thread
+// quantizes 16-element blocks of the chunk (the standalone quantizer's
+// arithmetic), so X is read from HBM once for both and the product costs
+// the quantizing warps nothing. A ring slot is refilled once the MMAs that
+// read it have completed (tcgen05.commit on the slot's mbarrier).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -31,27 +34,11 @@ namespace nvfp4 {
 
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kRows = 16 * kWarps;  // rows per CTA
-constexpr int kStages = 4;          // shared-memory ring depth (64-column chunks)
+constexpr int kWarps = 8;
+constexpr int kRows = 128;          // rows per CTA: one M = 128 tensor-core tile
+constexpr int kStages = 3;          // shared-memory ring depth (64-column chunks)
 constexpr int kMaxSplit = 8;        // K ranges per row tile
-
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
-                                               uint32_t a2, uint32_t a3, uint32_t b0,
-                                               uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1,
-                                            uint32_t &r2, uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
+constexpr int kCtasPerSm = 3;       // what the shared-memory budget allows
 
 // 16-byte global -> shared copy; src_bytes = 0 writes zeros.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
@@ -82,9 +69,14 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 
 template <int R>
 struct LoraCfg {
-    static constexpr int X_TILE = kRows * 128;  // 64 bfloat16 per row (8 KiB)
+    static constexpr int X_TILE = kRows * 128;  // 64 bfloat16 per row (16 KiB)
     static constexpr int A_TILE = R * 128;
-    static constexpr int SMEM = kStages * (X_TILE + A_TILE);
+    static constexpr int TMEM_COLS = R <= 32 ? 32 : 64;  // FP32 accumulator, 128 lanes x R
+    static constexpr int BAR_OFF = kStages * (X_TILE + A_TILE);
+    // + 1024 to align the ring to the swizzle pattern; barriers, TMEM slot
+    static constexpr int SMEM = 1024 + BAR_OFF + 64;
+    static_assert(A_TILE % 1024 == 0 && X_TILE % 1024 == 0, "tiles keep the 1024-byte pattern");
+    static_assert(R % 16 == 0 && R >= 16 && R <= 64, "N of the M = 128 MMA");
 };
 
 // Grid: (row tiles of 128, K ranges). part: FP32 [range][rows_pad][R].
@@ -93,18 +85,37 @@ __global__ void __launch_bounds__(32 * kWarps)
     quantize_lora_kernel(const uint16_t *__restrict__ X, uint32_t rows, uint32_t K, uint64_t ldx,
                          const float *__restrict__ g_x, const uint16_t *__restrict__ A,
                          uint32_t chunks_per_range, uint32_t rows_pad, uint8_t *__restrict__ q,
-                         uint8_t *__restrict__ sf, float *__restrict__ part) {
+                         uint8_t *__restrict__ sf, float *__restrict__ part, uint64_t timeout_ns,
+                         unsigned int *err) {
     using C = LoraCfg<R>;
-    extern __shared__ __align__(128) uint8_t lsmem[];
+    extern __shared__ uint8_t lsmem_raw[];
+    uint8_t *lsmem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(lsmem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t xs0 = smem_addr(lsmem);
     const uint32_t as0 = xs0 + kStages * C::X_TILE;
+    uint64_t *mma_done = reinterpret_cast<uint64_t *>(lsmem + C::BAR_OFF);  // one per slot
+    uint64_t *acc_full = mma_done + kStages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int gq = lane >> 2, c = lane & 3;
     const uint32_t row0 = blockIdx.x * kRows;
     const uint32_t kb4 = K / 64;
     const uint32_t c_begin = blockIdx.y * chunks_per_range;
     const uint32_t c_end = min(kb4, c_begin + chunks_per_range);
     const int nch = static_cast<int>(c_end - c_begin);
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&mma_done[s], 1);
+        mbar_init(acc_full, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
     pdl_launch_dependents();
     pdl_wait();
     const float g = *g_x;
@@ -135,20 +146,36 @@ __global__ void __launch_bounds__(32 * kWarps)
         cp_async_commit();
     }
 
-    float acc[R / 8][4];
-#pragma unroll
-    for (int n = 0; n < R / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
-    const uint32_t ra = row0 + warp * 16 + gq;
-    // ldmatrix lane roles: matrix m = lane / 8, row lane % 8
-    const uint32_t lm = lane >> 3, lr = lane & 7;
-    const uint32_t a_row = warp * 16 + (lm & 1u) * 8 + lr;  // X piece rows of this lane
+    constexpr uint32_t idesc = idesc_bf16(kRows, R);
+    bool ok = true;
     for (int i = 0; i < nch; ++i) {
         cp_async_wait<kStages - 2>();
-        __syncthreads();  // chunk i landed; every warp is done with chunk i - 1
-        if (i + kStages - 1 < nch) load((i + kStages - 1) % kStages, c_begin + i + kStages - 1);
-        cp_async_commit();
+        fence_proxy_async_shared();  // this thread's copies of chunk i, to the tensor core
+        // the slot refilled below held chunk i - 1: its MMAs must have read it
+        const bool refill = i + kStages - 1 < nch;
+        int timed_out = 0;
+        if (tid == 0 && refill && i >= 1)
+            timed_out = !mbar_wait(&mma_done[(i - 1) % kStages], ((i - 1) / kStages) & 1,
+                                   timeout_ns);
+        // chunk i is complete in shared memory and every thread is done
+        // with chunk i - 1
+        if (__syncthreads_or(timed_out)) {
+            if (tid == 0) record_timeout(err);
+            ok = false;
+            break;
+        }
         const int s = i % kStages;
         const uint32_t xs = xs0 + s * C::X_TILE, as = as0 + s * C::A_TILE;
+        if (warp == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_elect(tmem, sdesc_sw128(xs + ks * 32), sdesc_sw128(as + ks * 32), idesc,
+                               (i | ks) != 0);
+            tc_commit_elect(&mma_done[s]);
+        }
+        if (refill) load((i + kStages - 1) % kStages, c_begin + i + kStages - 1);
+        cp_async_commit();
         const uint32_t ch = c_begin + i;
         // quantization: one thread per 16-element block (4 per row of the
         // chunk), the standalone quantizer's arithmetic; the four lanes of a
@@ -171,35 +198,59 @@ __global__ void __launch_bounds__(32 * kWarps)
             if (blk == 0 && NVFP4_CHECK(soff + 4 <= static_cast<uint64_t>(rows_pad) * (K / 16)))
                 *reinterpret_cast<uint32_t *>(sf + soff) = w;
         }
-        // down projection: this warp's 16 rows times the chunk of A
+    }
+    cp_async_wait<0>();
+    // every MMA issued has completed (also after an abort: TMEM is released
+    // only once nothing writes it)
+    if (warp == 0) tc_commit_elect(acc_full);
+    int done = 1;
+    if (tid == 0) done = mbar_wait(acc_full, 0, timeout_ns);
+    if (!__syncthreads_and(done)) {
+        if (tid == 0) record_timeout(err);
+        ok = false;
+    }
+    tc_fence_after();
+    if (ok && warp < 4) {
+        // this K range's partial down projection: warp w reads TMEM lanes
+        // (rows) 32w .. 32w + 31, one row per thread
+        const uint32_t row = row0 + warp * 32 + lane;
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        float *dst = part + (static_cast<uint64_t>(blockIdx.y) * rows_pad + row) * R;
+        if constexpr (R <= 32) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(taddr, v);
+            tmem_ld_wait();
+            if (NVFP4_CHECK(row < rows_pad)) {
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            uint32_t a0, a1, a2, a3;
-            ldmatrix_x4(xs + swz(a_row, 2u * ks + (lm >> 1)), a0, a1, a2, a3);
+                for (int j = 0; j < R; j += 4)
+                    *reinterpret_cast<float4 *>(dst + j) =
+                        make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                    __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+            }
+        } else {
+            uint32_t v[64];
+            tmem_ld_32x32b_x64(taddr, v);
+            tmem_ld_wait();
+            if (NVFP4_CHECK(row < rows_pad)) {
 #pragma unroll
-            for (int pr = 0; pr < R / 16; ++pr) {
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4(as + swz(pr * 16u + (lm >> 1) * 8u + lr, 2u * ks + (lm & 1u)), b0, b1,
-                            b2, b3);
-                mma_bf16_16816(acc[2 * pr], a0, a1, a2, a3, b0, b1);
-                mma_bf16_16816(acc[2 * pr + 1], a0, a1, a2, a3, b2, b3);
+                for (int j = 0; j < R; j += 4)
+                    *reinterpret_cast<float4 *>(dst + j) =
+                        make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                    __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
             }
         }
     }
-    cp_async_wait<0>();
-    // this K range's partial down projection, rows ra and rb
-    float *pa = part + (static_cast<uint64_t>(blockIdx.y) * rows_pad + ra) * R;
-    float *pb = pa + 8 * R;
-    if (NVFP4_CHECK(ra + 8 < rows_pad)) {  // rows ra and ra + 8 of this range's partials
-#pragma unroll
-        for (int n = 0; n < R / 8; ++n) {
-            *reinterpret_cast<float2 *>(pa + n * 8 + 2 * c) = make_float2(acc[n][0], acc[n][1]);
-            *reinterpret_cast<float2 *>(pb + n * 8 + 2 * c) = make_float2(acc[n][2], acc[n][3]);
-        }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
     }
 }
 
 // L'[m, j] = bf16( lora_scale / (g_x g_w) * sum over K ranges, in order ).
+// Four consecutive entries per thread; all ranges' partials are loaded
+// before the ordered sum, so their latencies overlap.
 template <int R>
 __global__ void __launch_bounds__(256)
     lora_finalize_kernel(const float *__restrict__ part, uint32_t rows, uint32_t rows_pad,
@@ -209,14 +260,31 @@ __global__ void __launch_bounds__(256)
     pdl_launch_dependents();
     pdl_wait();
     const float factor = __fdiv_rn(lora_scale, __fmul_rn(*g_x, *g_w));
-    const uint64_t total = static_cast<uint64_t>(rows) * R;
-    for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+    const uint64_t total4 = static_cast<uint64_t>(rows) * R / 4;  // R % 16 == 0
+    const uint64_t range4 = static_cast<uint64_t>(rows_pad) * R / 4;
+    const float4 *p4 = reinterpret_cast<const float4 *>(part);
+    for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total4;
          i += static_cast<uint64_t>(gridDim.x) * blockDim.x) {
-        float sum = part[i];
-        for (uint32_t sidx = 1; sidx < ranges; ++sidx)
-            sum = __fadd_rn(sum, part[static_cast<uint64_t>(sidx) * rows_pad * R + i]);
-        const __nv_bfloat16 v = __float2bfloat16_rn(__fmul_rn(sum, factor));
-        Lp[i] = *reinterpret_cast<const uint16_t *>(&v);
+        float4 v[kMaxSplit];
+#pragma unroll
+        for (int r = 0; r < kMaxSplit; ++r)
+            if (r < static_cast<int>(ranges)) v[r] = p4[r * range4 + i];
+        float4 sum = v[0];
+#pragma unroll
+        for (int r = 1; r < kMaxSplit; ++r) {
+            if (r < static_cast<int>(ranges)) {
+                sum.x = __fadd_rn(sum.x, v[r].x);
+                sum.y = __fadd_rn(sum.y, v[r].y);
+                sum.z = __fadd_rn(sum.z, v[r].z);
+                sum.w = __fadd_rn(sum.w, v[r].w);
+            }
+        }
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(__fmul_rn(sum.x, factor),
+                                                        __fmul_rn(sum.y, factor));
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(__fmul_rn(sum.z, factor),
+                                                        __fmul_rn(sum.w, factor));
+        reinterpret_cast<uint2 *>(Lp)[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&lo),
+                                                      *reinterpret_cast<const uint32_t *>(&hi));
     }
 }
 
@@ -224,12 +292,13 @@ struct Split {
     uint32_t ranges, chunks_per_range;
 };
 
-// K ranges per 64-row tile: about four CTAs per SM in all, at most
+// K ranges per 128-row tile: about kCtasPerSm CTAs per SM in all, at most
 // kMaxSplit, every range non-empty.
 Split lora_split(int64_t rows_pad, int64_t K) {
     const uint32_t kb4 = static_cast<uint32_t>(K / 64);
     const uint32_t tiles = static_cast<uint32_t>(rows_pad / kRows);
-    uint32_t want = (4u * static_cast<uint32_t>(launch_cfg().num_sms) + tiles - 1) / tiles;
+    uint32_t want =
+        (kCtasPerSm * static_cast<uint32_t>(launch_cfg().num_sms) + tiles - 1) / tiles;
     want = want < 1 ? 1 : (want > kMaxSplit ? kMaxSplit : want);
     if (want > kb4) want = kb4;
     const uint32_t cpr = (kb4 + want - 1) / want;
@@ -249,6 +318,8 @@ cudaError_t launch_r(const uint16_t *X, int64_t rows, int64_t K, int64_t ldx, co
     if (e_setup != cudaSuccess) return e_setup;
     const uint32_t rows_pad = static_cast<uint32_t>((rows + 127) / 128 * 128);
     const Split sp = lora_split(rows_pad, K);
+    unsigned int *err = device_error_word();
+    if (err == nullptr) return cudaErrorInvalidSymbol;
     cudaLaunchAttribute attr = pdl_attribute();
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(32 * kWarps, 1, 1);
@@ -260,9 +331,9 @@ cudaError_t launch_r(const uint16_t *X, int64_t rows, int64_t K, int64_t ldx, co
     cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_lora_kernel<R>, X,
                                        static_cast<uint32_t>(rows), static_cast<uint32_t>(K),
                                        static_cast<uint64_t>(ldx), g_x, A, sp.chunks_per_range,
-                                       rows_pad, q, sf, part);
+                                       rows_pad, q, sf, part, debug_state().timeout_ns, err);
     if (e != cudaSuccess) return e;
-    const uint64_t total = static_cast<uint64_t>(rows) * R;
+    const uint64_t total = static_cast<uint64_t>(rows) * R / 4;  // four entries a thread
     uint64_t blocks = (total + 255) / 256;
     const uint64_t cap = static_cast<uint64_t>(launch_cfg().num_sms) * 4;
     if (blocks > cap) blocks = cap;

@@ -120,11 +120,14 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t *__re
 }
 
 // amax(|X|) over 16-byte vectors as a bfloat16 magnitude bit pattern,
-// combined across the grid with atomicMax on `cell` (zeroed beforehand).
+// combined across the grid with atomicMax on `cell` (zeroed by the kernel
+// before it, which this one waits for, as it may also have written X).
 __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t *__restrict__ X,
                                                         uint32_t rows, uint32_t vpr,
                                                         uint64_t ldx, FastDiv div_vpr,
                                                         uint32_t *cell) {
+    pdl_launch_dependents();
+    pdl_wait();
     const uint32_t total = rows * vpr;
     const uint32_t stride = gridDim.x * blockDim.x;
     const uint32_t m = 0x7FFF7FFFu;
@@ -434,17 +437,12 @@ __global__ void counter_reset_kernel(unsigned int *counter) {
 }
 
 // An amax cell (bfloat16 magnitude bits) into the global scale, in place,
-// once the kernel that accumulated it has completed.
+// once the kernel that accumulated it has completed. The next kernel is let
+// in only then: started earlier, its CTAs would sit on the SMs that the
+// amax reduction is still using.
 __global__ void amax_cell_to_scale_kernel(uint32_t *cell) {
-    pdl_launch_dependents();
     pdl_wait();
-    const float amax = __uint_as_float(*cell << 16);
-    const float g = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
-    *reinterpret_cast<float *>(cell) = g;
-}
-
-// g = amax / (6 * 448), or 1 for an all-zero tensor; in place over the cell.
-__global__ void global_scale_finalize(uint32_t *cell) {
+    pdl_launch_dependents();
     const float amax = __uint_as_float(*cell << 16);
     const float g = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
     *reinterpret_cast<float *>(cell) = g;
@@ -481,20 +479,26 @@ int grid_for(uint64_t work_items, int per_thread) {
 
 cudaError_t launch_global_scale(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
                                 float *g_out, cudaStream_t st) {
+    // three programmatic dependents in a row (no memset, which would break
+    // the launch chain): zero the cell, fold the amax into it, turn it into g
     uint32_t *cell = reinterpret_cast<uint32_t *>(g_out);
-    cudaError_t e = cudaMemsetAsync(cell, 0, sizeof(uint32_t), st);
+    cudaError_t e = launch_cell_reset(cell, st);
     if (e != cudaSuccess) return e;
     const uint32_t vpr = static_cast<uint32_t>(cols / 8);
     const uint64_t total = static_cast<uint64_t>(rows) * vpr;
     if (total > 0) {
-        amax_kernel<<<grid_for(total, 4), kThreads, 0, st>>>(X, static_cast<uint32_t>(rows), vpr,
-                                                             static_cast<uint64_t>(ldx),
-                                                             FastDiv(vpr), cell);
-        e = cudaGetLastError();
+        cudaLaunchAttribute attr = pdl_attribute();
+        cudaLaunchConfig_t cfg = {};
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.gridDim = dim3(grid_for(total, 4), 1, 1);
+        cfg.stream = st;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, amax_kernel, X, static_cast<uint32_t>(rows), vpr,
+                               static_cast<uint64_t>(ldx), FastDiv(vpr), cell);
         if (e != cudaSuccess) return e;
     }
-    global_scale_finalize<<<1, 1, 0, st>>>(cell);
-    return cudaGetLastError();
+    return launch_amax_cell_to_scale(cell, st);
 }
 
 cudaError_t launch_quantize(const uint16_t *X, int64_t rows, int64_t cols, int64_t ldx,
