@@ -212,32 +212,29 @@ __global__ void __launch_bounds__(32 * kWarps)
     tc_fence_after();
     if (ok && warp < 4) {
         // this K range's partial down projection: warp w reads TMEM lanes
-        // (rows) 32w .. 32w + 31, one row per thread
+        // (rows) 32w .. 32w + 31, one row per thread (an empty range, which
+        // the split never makes, would contribute zeros)
         const uint32_t row = row0 + warp * 32 + lane;
         const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         float *dst = part + (static_cast<uint64_t>(blockIdx.y) * rows_pad + row) * R;
-        if constexpr (R <= 32) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(taddr, v);
+        constexpr int NCOL = R <= 32 ? 32 : 64;
+        uint32_t v[NCOL];
+        if (nch > 0) {
+            if constexpr (NCOL == 32)
+                tmem_ld_32x32b_x32(taddr, v);
+            else
+                tmem_ld_32x32b_x64(taddr, v);
             tmem_ld_wait();
-            if (NVFP4_CHECK(row < rows_pad)) {
-#pragma unroll
-                for (int j = 0; j < R; j += 4)
-                    *reinterpret_cast<float4 *>(dst + j) =
-                        make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                    __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
-            }
         } else {
-            uint32_t v[64];
-            tmem_ld_32x32b_x64(taddr, v);
-            tmem_ld_wait();
-            if (NVFP4_CHECK(row < rows_pad)) {
 #pragma unroll
-                for (int j = 0; j < R; j += 4)
-                    *reinterpret_cast<float4 *>(dst + j) =
-                        make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                    __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
-            }
+            for (int j = 0; j < NCOL; ++j) v[j] = 0u;
+        }
+        if (NVFP4_CHECK(row < rows_pad)) {
+#pragma unroll
+            for (int j = 0; j < R; j += 4)
+                *reinterpret_cast<float4 *>(dst + j) =
+                    make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
         }
     }
     tc_fence_before();
