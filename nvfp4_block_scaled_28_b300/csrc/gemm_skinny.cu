@@ -369,7 +369,7 @@ __device__ __forceinline__ void sk_epilogue_ext(const SkParams &p, const float (
     const int n_blk = n_warp + gbase;             // first column of the group's block
     const int kb = n_blk >> 4;
     const int kb4 = p.N / 64;
-    const uint64_t sf_end = static_cast<uint64_t>((p.M + 127) / 128) * 128 * (p.N / 16);
+    [[maybe_unused]] const uint64_t sf_end = static_cast<uint64_t>((p.M + 127) / 128) * 128 * (p.N / 16);
     uint32_t am = 0;
 #pragma unroll
     for (int m = 0; m < XR; ++m) {
