@@ -942,7 +942,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--gemm-seconds", type=float, default=1.5,
                     help="length of the GEMM-only roofline loop")
-    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=16)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--mode", choices=["unfused", "fused"], default="unfused")
     ap.add_argument("--no-extras", action="store_true", help="skip the per-row extra numbers")
