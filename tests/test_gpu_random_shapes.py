@@ -9,8 +9,9 @@ quantizers; decode kernel up to 128 rows, with and without the K split of
 its partial last round; CTA-pair kernel beyond), any N from 1 to 1300 (a
 partial last weight tile of any width), K a multiple of 256 up to 2560,
 the dynamic or a given activation scale, and the fused decode mode where it
-applies. The dynamic re-quantizing epilogue gets its own draws (N a
-multiple of 256).
+applies. The dynamic re-quantizing epilogue, the LoRA linear (M > 128, every
+rank it supports) and the grouped projections (1 to 4 groups, each group's
+columns also bitwise equal to its own linear) get their own draws.
 """
 import numpy as np
 import pytest
@@ -123,3 +124,37 @@ def test_random_dynamic_requant_matches_oracle(nv, oracle_mod, M, N, K, bias, se
     q_ref, s_ref = oracle_mod.quantize(y_bits, g_expect)
     assert np.array_equal(to_np_u8(Yq), q_ref), label + ": codes"
     assert np.array_equal(to_np_u8(Ys), sf_rowmajor_to_mma(s_ref)), label + ": scales"
+
+
+def _draw_lora(n_cases, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n_cases):
+        M = int(rng.integers(129, 900))     # the LoRA entry runs the CTA-pair kernel
+        N = int(256 * rng.integers(1, 5))
+        K = int(256 * rng.integers(1, 8))
+        r = int([16, 32, 48, 64][rng.integers(0, 4)])
+        out.append((M, N, K, r, [1.0, 0.5, 16.0][i % 3], KINDS[i % 3], 500 + i))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K,r,scale,kind,seed", _draw_lora(12, 9))
+def test_random_lora_matches_oracle(nv, oracle_mod, M, N, K, r, scale, kind, seed):
+    import test_gpu_lora
+    test_gpu_lora._run(nv, oracle_mod, M, N, K, r, scale, seed=seed, kind=kind)
+
+
+def _draw_grouped(n_cases, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n_cases):
+        M = int([rng.integers(1, 9), rng.integers(9, 129), rng.integers(129, 700)][i % 3])
+        ns = tuple(int(256 * rng.integers(1, 4)) for _ in range(int(rng.integers(1, 5))))
+        out.append((M, ns, int(256 * rng.integers(1, 6)), int(rng.integers(0, 2)), 900 + i))
+    return out
+
+
+@pytest.mark.parametrize("M,ns,K,mode,seed", _draw_grouped(12, 10))
+def test_random_grouped_matches_separate_and_oracle(nv, oracle_mod, M, ns, K, mode, seed):
+    import test_gpu_grouped
+    test_gpu_grouped._check(nv, oracle_mod, M, ns, K, mode, seed=seed)
