@@ -11,7 +11,8 @@ partial last weight tile of any width), K a multiple of 256 up to 2560,
 the dynamic or a given activation scale, and the fused decode mode where it
 applies. The dynamic re-quantizing epilogue, the LoRA linear (M > 128, every
 rank it supports) and the grouped projections (1 to 4 groups, each group's
-columns also bitwise equal to its own linear) get their own draws.
+columns also bitwise equal to its own linear) get their own draws, and so
+does the standalone quantizer (every scale rule, both layouts).
 """
 import numpy as np
 import pytest
@@ -158,3 +159,35 @@ def _draw_grouped(n_cases, seed):
 def test_random_grouped_matches_separate_and_oracle(nv, oracle_mod, M, ns, K, mode, seed):
     import test_gpu_grouped
     test_gpu_grouped._check(nv, oracle_mod, M, ns, K, mode, seed=seed)
+
+
+def _draw_quantize(n_cases, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n_cases):
+        rows = int(rng.integers(1, 700))
+        layout = int(rng.integers(0, 2))
+        K = int((64 if layout else 16) * rng.integers(1, 40))
+        out.append((rows, K, int(i % 3), layout, float([1.0, 0.5, 4.0][i % 3]), KINDS[i % 3],
+                    3000 + i))
+    return out
+
+
+@pytest.mark.parametrize("rows,K,rule,layout,g_factor,kind,seed", _draw_quantize(15, 11))
+def test_random_quantize_matches_oracle(nv, oracle_mod, rows, K, rule, layout, g_factor, kind,
+                                        seed):
+    """The standalone quantizer under every scale rule, both layouts, ragged
+    rows and K (any multiple of 16, of 64 in the tile layout), and a given
+    scale off the tensor's own by the drawn factor."""
+    x = workloads.make_x(kind, rows, K, seed=seed)
+    xb = bf16_bits(x)
+    g = float(np.float32(oracle_mod.global_scale(xb) * g_factor))
+    q_ref, s_ref = oracle_mod.quantize(xb, g, rule)
+    q, s = nv.nvfp4_quantize(x.cuda(), torch.tensor([g], dtype=torch.float32, device="cuda"),
+                             layout, rule=rule)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_device_error() == 0
+    label = "%dx%d rule=%d layout=%d" % (rows, K, rule, layout)
+    assert np.array_equal(to_np_u8(q), q_ref), label + ": codes"
+    want = s_ref if layout == 0 else sf_rowmajor_to_mma(s_ref)
+    assert np.array_equal(to_np_u8(s).reshape(want.shape), want), label + ": scales"
