@@ -185,12 +185,25 @@ def nvfp4_gemm(Aq, As, g_a, Bq, Bs, g_b, K: int, Y: torch.Tensor | None = None,
     return Y
 
 
+def _default_mode(mode, workspace) -> int:
+    """With no mode given: the fused decode kernel where it applies (it
+    produces the same Y, but leaves no quantized X in the workspace), unless
+    the caller passes a workspace, whose contents it may then read."""
+    if mode is not None:
+        return mode
+    return LINEAR_FUSED if workspace is None else LINEAR_UNFUSED
+
+
 def nvfp4_linear(X: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor, g_w: torch.Tensor,
-                 g_x: torch.Tensor | None = None, mode: int = LINEAR_UNFUSED,
+                 g_x: torch.Tensor | None = None, mode: int | None = None,
                  Y: torch.Tensor | None = None,
                  workspace: torch.Tensor | None = None) -> torch.Tensor:
     """NVFP4 linear layer: Y = bf16(quant(X) @ dequant(Wq, Ws, g_w)^T), the
-    activation quantized on the fly (g_x computed from X when None)."""
+    activation quantized on the fly (g_x computed from X when None).
+    ``mode`` None: LINEAR_FUSED when no workspace is passed (the one-kernel
+    decode path for M <= 8, K <= 6144; the same sequence otherwise), else
+    LINEAR_UNFUSED."""
+    mode = _default_mode(mode, workspace)
     _check_bf16_2d(X, "X")
     M, K = X.shape
     Nn = Wq.shape[0]
@@ -234,13 +247,15 @@ def pack_weight_groups(weights):
 
 def nvfp4_linear_grouped(X: torch.Tensor, Wq: torch.Tensor, Ws: torch.Tensor,
                          g_w: torch.Tensor, group_n, g_x: torch.Tensor | None = None,
-                         mode: int = LINEAR_UNFUSED, Y: torch.Tensor | None = None,
+                         mode: int | None = None, Y: torch.Tensor | None = None,
                          workspace: torch.Tensor | None = None) -> torch.Tensor:
     """Several projections of the same X in one call (X quantized once, one
     GEMM launch), group g with its own global scale g_w[g]; Y's columns are
-    the groups' outputs side by side (see pack_weight_groups)."""
+    the groups' outputs side by side (see pack_weight_groups). ``mode`` as
+    in nvfp4_linear."""
     import ctypes
 
+    mode = _default_mode(mode, workspace)
     _check_bf16_2d(X, "X")
     M, K = X.shape
     group_n = [int(n) for n in group_n]

@@ -227,3 +227,23 @@ def test_strided_activation_workspace(nv, oracle_mod, M, K):
     y_c = nv.nvfp4_linear(x.cuda(), Wq, Ws, gw)
     assert torch.equal(y_s.view(torch.int16), y_c.view(torch.int16))
     assert nv.nvfp4_device_error() == 0
+
+
+def test_default_mode_keeps_the_workspace_contract(nv, oracle_mod):
+    """With no mode given, a call without a workspace may take the fused
+    decode kernel (the same Y bits), while a call with a workspace runs the
+    unfused sequence and leaves X's quantized form in it."""
+    M, N, K = 4, 1024, 2048
+    x = _with_special_blocks(workloads.make_x("outlier", M, K, seed=41))
+    Wq, Ws, gw = _weights(nv, N, K, 42)
+    y_default = nv.nvfp4_linear(x.cuda(), Wq, Ws, gw)
+    y_fused = nv.nvfp4_linear(x.cuda(), Wq, Ws, gw, mode=nv.LINEAR_FUSED)
+    ws = torch.full((nv.linear_workspace_bytes(M, N, K),), 0xA5, dtype=torch.uint8,
+                    device="cuda")
+    y_ws = nv.nvfp4_linear(x.cuda(), Wq, Ws, gw, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y_default.view(torch.int16), y_fused.view(torch.int16))
+    assert torch.equal(y_default.view(torch.int16), y_ws.view(torch.int16))
+    q_ref, sf_ref, g_ref = _expect(oracle_mod, x)
+    _check(ws, M, K, q_ref, sf_ref, g_ref, label="default mode with a workspace")
+    assert nv.nvfp4_device_error() == 0
